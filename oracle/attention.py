@@ -1,0 +1,158 @@
+"""Softmax attention over a quantised cache plus the current chunk (oracle, test infrastructure only).
+
+"Quantized Keys Steal Attention" (abstract): in chunk-wise autoregressive video
+diffusion the queries of the current chunk attend to the cache of earlier
+chunks and to the current, unquantised chunk.  Quantisation noise on cached
+keys inflates their expected softmax weight through the convexity of exp (the
+Jensen bias); a per-score correction computed from the cached keys' step sizes
+and the query removes it in expectation, with a second-order Taylor form.
+
+Reading (no formula is printed): with k_hat = k + eps, eps_c ~ U(-s_c/2, s_c/2)
+independent,
+
+    E[exp(tau q.k_hat)] = exp(tau q.k) * prod_c sinh(x_c) / x_c,   x_c = tau q_c s_c / 2
+
+so the corrected cached logit is  tau q.k_hat - delta  with
+
+    delta_exact   = sum_c log(sinh(x_c) / x_c)
+    delta_taylor2 = sum_c x_c^2 / 6 = (tau^2 / 24) sum_c q_c^2 s_c^2
+
+applied to quantised cached keys only (zero for RAW16 windows and the current
+chunk).  All sums and the softmax are fp64; the output is returned in fp64.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .quant import round_to
+
+F64 = np.float64
+
+JENSEN_OFF, JENSEN_TAYLOR2, JENSEN_EXACT = 0, 1, 2
+
+
+def log_sinhc(x):
+    """log(sinh(x)/x) in fp64, stable near 0 (series x^2/6 - x^4/180 + x^6/2835)."""
+    x = np.abs(np.asarray(x, F64))
+    small = x < 1e-3
+    xs = np.where(small, 1.0, x)
+    # log(sinh x / x) = x + log1p(-exp(-2x)) - log(2x)
+    big = xs + np.log1p(-np.exp(-2.0 * xs)) - np.log(2.0 * xs)
+    x2 = x * x
+    ser = x2 / 6.0 - x2 * x2 / 180.0 + x2 * x2 * x2 / 2835.0
+    return np.where(small, ser, big)
+
+
+def jensen_delta(Q, s_groups, tau, mode):
+    """Per (query, key group) Jensen correction.
+
+    Q: [nq, d] queries (fp64 values), s_groups: [G, d] key step sizes per group.
+    Returns delta [nq, G] (fp64).
+    """
+    Q = np.asarray(Q, F64)
+    S = np.asarray(s_groups, F64)
+    if mode == JENSEN_OFF or S.shape[0] == 0:
+        return np.zeros((Q.shape[0], S.shape[0]), F64)
+    if mode == JENSEN_TAYLOR2:
+        return (tau * tau / 24.0) * ((Q * Q) @ (S * S).T)
+    if mode == JENSEN_EXACT:
+        x = 0.5 * tau * Q[:, None, :] * S[None, :, :]
+        return log_sinhc(x).sum(-1)
+    raise ValueError(mode)
+
+
+def softmax_attend(logits, Vall):
+    """Row softmax of fp64 logits [nq, n] against values [n, d] -> (o [nq, d], lse [nq]).
+
+    Uses the max-shifted form; pinned against the direct exp/sum definition on
+    small inputs in the oracle tests.
+    """
+    logits = np.asarray(logits, F64)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = (p @ np.asarray(Vall, F64)) / l
+    lse = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def attention_rows(Q, Kc, Vc, Kn, Vn, tau, delta_keys=None, extra_keys=None):
+    """Attention of queries Q [nq, d] over cached (Kc, Vc) [nc, d] and current (Kn, Vn) [nn, d].
+
+    delta_keys [nq, nc] is subtracted from and extra_keys [nq, nc] added to the
+    cached logits.  All inputs are used as given, in fp64.
+    """
+    Q = np.asarray(Q, F64)
+    lc = tau * (Q @ np.asarray(Kc, F64).T)
+    if delta_keys is not None:
+        lc = lc - delta_keys
+    if extra_keys is not None:
+        lc = lc + extra_keys
+    ln = tau * (Q @ np.asarray(Kn, F64).T)
+    logits = np.concatenate([lc, ln], axis=1)
+    Vall = np.concatenate([np.asarray(Vc, F64), np.asarray(Vn, F64)], axis=0)
+    return softmax_attend(logits, Vall)
+
+
+def lse_merge(ms, ls, os_):
+    """Merge split partials (m_p, l_p, o_p) with o_p already normalised by l_p.
+
+    m = max m_p; l = sum l_p exp(m_p - m); o = sum l_p exp(m_p - m) o_p / l.
+    Splits with l_p == 0 (empty) are skipped.  Returns (o, lse).
+    """
+    ms = np.asarray(ms, F64)
+    ls = np.asarray(ls, F64)
+    os_ = np.asarray(os_, F64)
+    keep = ls > 0
+    m = np.max(np.where(keep, ms, -np.inf), axis=0)
+    w = np.where(keep, ls * np.exp(np.where(keep, ms, 0.0) - m), 0.0)
+    l = w.sum(axis=0)
+    o = (w[..., None] * os_).sum(axis=0) / l[..., None]
+    return o, m + np.log(l)
+
+
+def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN_OFF,
+                         psac_U=None, rows=None):
+    """Reference attention for every (b, q-head).
+
+    cache : oracle.layout.Cache (or codebook cache) holding the dequantised view.
+    Q     : fp32 [B, Hq, nq, d]; Kcur, Vcur: fp32 [B, Hkv, nn, d] (may have nn = 0).
+    io_dtype: 'f32' | 'f16' | 'bf16' -- dequantised cache entries are rounded to it.
+    psac_U: optional fp32 [B, Hkv, d, r]; adds tau (U^T q) . coeff for cached keys.
+    rows  : optional index array of query rows to evaluate (all if None).
+    GQA: q-head h reads kv-head h // (Hq // Hkv).
+    Returns (o [B, Hq, nrows, d], lse [B, Hq, nrows]) in fp64.
+    """
+    Q = np.asarray(Q, np.float32)
+    B, Hq, nq, d = Q.shape
+    Hkv = cache.H
+    assert Hq % Hkv == 0
+    grp = Hq // Hkv
+    if tau is None:
+        tau = 1.0 / np.sqrt(d)
+    if rows is None:
+        rows = np.arange(nq)
+    o = np.zeros((B, Hq, len(rows), d), F64)
+    lse = np.zeros((B, Hq, len(rows)), F64)
+    for b in range(B):
+        for hk in range(Hkv):
+            lg = cache.logical(b, hk)
+            Kc = round_to(lg["khat"], io_dtype)
+            Vc = round_to(lg["vhat"], io_dtype)
+            for hq in range(hk * grp, (hk + 1) * grp):
+                q = Q[b, hq, rows].astype(F64)
+                delta = None
+                if jensen != JENSEN_OFF and Kc.shape[0] > 0:
+                    dg = jensen_delta(q, lg["ks"], tau, jensen)
+                    dg = dg * lg["quantised"][None, :]
+                    delta = dg[:, lg["kgroup"]]
+                extra = None
+                if psac_U is not None and lg["coeff"] is not None and Kc.shape[0] > 0:
+                    U = np.asarray(psac_U[b, hk], F64)
+                    uq = q @ U                                   # [nrows, r]
+                    extra = tau * (uq @ np.asarray(lg["coeff"], F64).T)
+                kn = np.asarray(Kcur[b, hk], F64) if Kcur is not None else np.zeros((0, d))
+                vn = np.asarray(Vcur[b, hk], F64) if Vcur is not None else np.zeros((0, d))
+                o[b, hq], lse[b, hq] = attention_rows(q, Kc, Vc, kn, vn, tau, delta, extra)
+    return o, lse

@@ -1,0 +1,143 @@
+"""QSAC-style codebook keys and the codebook cache (oracle, test infrastructure only).
+
+"QuantWM" (Innovations, item 2; Methodology): INT2 key centroids chosen per
+channel with quantisation-sensitivity-aware clustering that weighs channels by
+the historical queries' sensitivity.  The pages give no algorithm, so the
+reading is a per-(head, channel) 1-D Lloyd k-means with 4 centroids:
+
+* sensitivity weight w_c = mean over historical queries of q_c^2.  It is one
+  constant per channel, so inside that channel's 1-D k-means it cancels from
+  every weighted mean and every assignment: the weighted algorithm equals the
+  unweighted one.  It is computed and reported, and changes nothing.
+* init at quantiles: sort the n values, mu_k = x_(floor((2k+1) n / 8)).
+* 20 iterations: assign each value to the nearest centroid by |x - mu_k| in
+  fp64 (ties to the lower k); mu_k = (exact sum of members) / n_k rounded
+  once to fp64; an empty cluster keeps its centroid.
+* centroids are stored as fp32; the stored index of a value is its nearest
+  fp32 centroid, again by fp64 |x - mu_k| with ties to the lower k.
+
+The exact member sum (``math.fsum``) equals any-order fp64 summation whenever
+that summation is exact, which holds for bf16 inputs of magnitude >= 2^-30 at
+these sizes.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from .quant import quantize_groups, dequantize, pack_codes, F32
+from .layout import BLOCK, CB2, Cache, block_bytes, ceil8
+
+F64 = np.float64
+
+
+def nearest(x, mu):
+    """Index of the nearest centroid by fp64 |x - mu_k|, ties to the lower k."""
+    x = np.asarray(x, F64)
+    mu = np.asarray(mu, F64)
+    dist = np.abs(x[:, None] - mu[None, :])
+    return np.argmin(dist, axis=1)          # argmin returns the first minimum
+
+
+def kmeans_1d(x, k=4, iters=20):
+    """1-D Lloyd k-means of one channel; returns fp64 centroids [k]."""
+    x = np.asarray(x, F64)
+    n = x.shape[0]
+    xs = np.sort(x)
+    mu = np.array([xs[(2 * j + 1) * n // (2 * k)] for j in range(k)], F64)
+    for _ in range(iters):
+        a = nearest(x, mu)
+        for j in range(k):
+            mem = x[a == j]
+            if mem.shape[0] > 0:
+                mu[j] = math.fsum(mem.tolist()) / mem.shape[0]
+    return mu
+
+
+def sensitivity(Qhist):
+    """w_c = mean_t q_{t,c}^2 over historical queries Qhist [n, d] (fp64)."""
+    Q = np.asarray(Qhist, F64)
+    return (Q * Q).mean(axis=0)
+
+
+def fit_centroids(Kh, iters=20):
+    """Centroids fp32 [d, 4] of one head's cached keys Kh [n, d]."""
+    Kh = np.asarray(Kh, F64)
+    return np.stack([kmeans_1d(Kh[:, c], 4, iters) for c in range(Kh.shape[1])]).astype(F32)
+
+
+def encode_cb_blocks(Kb, Vb, cent, coeff, nvalid, r):
+    """Pack N codebook blocks of one head.
+
+    Kb, Vb: fp32 [N, 32, d]; cent fp32 [d, 4]; coeff fp16 [N, 32, r] or None.
+    """
+    Kb = np.asarray(Kb, F32)
+    Vb = np.asarray(Vb, F32)
+    N, T, d = Kb.shape
+    idx = np.zeros((N, T, d), np.uint8)
+    for c in range(d):
+        idx[:, :, c] = nearest(Kb[:, :, c].reshape(-1), cent[c]).reshape(N, T)
+    idx[:, nvalid:] = 0
+    vc, vs, vz = quantize_groups(Vb.reshape(N, T, d // 32, 32), 2)
+    vc[:, nvalid:] = 0
+    vs[:, nvalid:] = 0
+    vz[:, nvalid:] = 0
+    rp = ceil8(r)
+    cq = np.zeros((N, T, rp), np.float16)
+    if r:
+        cq[:, :nvalid, :r] = coeff[:, :nvalid]
+    raw = np.concatenate([pack_codes(idx, 2).reshape(N, -1).view(np.uint8),
+                          pack_codes(vc.reshape(N, T, d), 2).reshape(N, -1).view(np.uint8),
+                          np.stack([vs, vz], -1).astype(F32).reshape(N, -1).view(np.uint8),
+                          cq.reshape(N, -1).view(np.uint8)], axis=1)
+    khat = cent[np.arange(d)[None, None, :], idx].astype(F32)
+    vhat = dequantize(vc, vs[..., None], vz[..., None]).reshape(N, T, d)
+    assert raw.shape[1] == block_bytes(CB2, d, r)
+    return dict(bytes=raw, idx=idx, khat=khat, vhat=vhat, coeff=cq[..., :r])
+
+
+def build_codebook(K, V, cent, U, cap_blocks):
+    """Codebook cache of one prefill of n tokens per (b, head).
+
+    K, V: fp32 [B, H, n, d] (bf16 values); cent fp32 [B, H, d, 4];
+    U: fp32 [B, H, d, r] PSAC basis or None (r = 0).
+    Key step sizes do not exist for codebook keys, so no Jensen term applies.
+    """
+    from .psac import psac_coeff
+    K = np.asarray(K, F32)
+    V = np.asarray(V, F32)
+    B, H, n, d = K.shape
+    r = 0 if U is None else U.shape[-1]
+    c = Cache(B, H, d, [CB2], [cap_blocks], r)
+    nb = (n + BLOCK - 1) // BLOCK
+    assert nb <= cap_blocks
+    npad = nb * BLOCK
+    for b in range(B):
+        for h in range(H):
+            Kp = np.zeros((npad, d), F32)
+            Vp = np.zeros((npad, d), F32)
+            Kp[:n] = K[b, h]
+            Vp[:n] = V[b, h]
+            for j in range(nb):
+                nv = min(BLOCK, n - j * BLOCK)
+                Kb = Kp[j * BLOCK:(j + 1) * BLOCK][None]
+                Vb = Vp[j * BLOCK:(j + 1) * BLOCK][None]
+                co = None
+                if r:
+                    idx = np.stack([nearest(Kb[0, :, ch], cent[b, h, ch]) for ch in range(d)], 1)
+                    khat = cent[b, h][np.arange(d)[None, :], idx]
+                    co = psac_coeff(Kb[0], khat, U[b, h])[None]
+                enc = encode_cb_blocks(Kb, Vb, cent[b, h], co, nv, r)
+                c._put(b, h, 0, j, enc["bytes"][0])
+                rec = dict(pos=j * BLOCK, len=nv, khat=enc["khat"][0], vhat=enc["vhat"][0],
+                           ks=np.zeros(d, F32), quantised=False)
+                rec["coeff"] = enc["coeff"][0].astype(F64) if r else np.zeros((BLOCK, 0))
+                c.blocks[b][h].append(rec)
+                if h == 0:
+                    c.blk_len[b, j] = nv
+                    c.blk_pos[b, j] = j * BLOCK
+    c.n_blocks = [nb]
+    c.n_tokens = n
+    return c
