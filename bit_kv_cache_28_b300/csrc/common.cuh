@@ -1,0 +1,179 @@
+// Shared device/host definitions of libbitkv: block format, dtype helpers,
+// and the dequantisation routine every kernel uses.
+//
+// Block format (32 token slots of one batch row and kv head), head dim d:
+//   INT2/INT4 (b bits): Kc u32[32][d*b/32] token-major | Km float2[d] |
+//                       Vc u32[d][b] channel-major     | Vm float2[d/32][32]
+//   RAW16:              K 16-bit[32][d] | V 16-bit[32][d]
+//   CODEBOOK2:          Kc u32[32][d/16] | Vc u32[d][2] | Vm float2[d/32][32] | Kq fp16[32][rp]
+// Quantiser (step sizes of "Quantized Keys Steal Attention", abstract; INT2/INT4
+// of the WindowQuant note, table in 何が新しいのか):
+//   s = fl32(fl32(M-m)/(2^b-1)), code = clamp(rint(fl32(fl32(x-m)/s))), z = m,
+//   x_hat = fmaf(code, s, z).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bitkv.h"
+
+namespace bitkv {
+
+constexpr int kBlockTokens = 32;
+
+// Everything a kernel needs to address a cache, passed by value.
+struct DevCache {
+    unsigned char* data;
+    int32_t* blk_len;
+    int32_t* blk_pos;
+    const float* centroids;
+    const float* psac_u;
+    int B, Hkv, d, kind, raw_dtype, r, rp;
+    int cap_total;
+    int seg_base[KV_NUM_SEG];      // index of a segment's first block in blk_len / blk_pos rows
+    int n_blocks[KV_NUM_SEG];
+    long long block_bytes[KV_NUM_SEG];
+    long long seg_offset[KV_NUM_SEG];
+    long long stream_bytes;
+};
+
+// Segment class of segment k for a cache kind: 16, 4 or 2 bits, or 3 for codebook.
+enum SegClass { CLS_RAW16 = 0, CLS_INT4 = 1, CLS_INT2 = 2, CLS_CB2 = 3 };
+
+__host__ __device__ inline int seg_class(int kind, int seg) {
+    if (kind == KV_CODEBOOK2) return CLS_CB2;
+    return seg;  // RAW16 / INT4 / INT2 by segment position
+}
+
+__host__ __device__ inline unsigned char* block_ptr(const DevCache& c, int b, int h, int seg, int i) {
+    return c.data + ((long long)b * c.Hkv + h) * c.stream_bytes + c.seg_offset[seg] +
+           (long long)i * c.block_bytes[seg];
+}
+
+// Byte offsets of the sub-arrays inside a block.
+struct IntBlockOffsets {
+    int kc, km, vc, vm;
+};
+__host__ __device__ inline IntBlockOffsets int_offsets(int d, int bits) {
+    IntBlockOffsets o;
+    o.kc = 0;
+    o.km = 4 * d * bits;
+    o.vc = o.km + 8 * d;
+    o.vm = o.vc + 4 * d * bits;
+    return o;
+}
+struct CbBlockOffsets {
+    int kc, vc, vm, kq;
+};
+__host__ __device__ inline CbBlockOffsets cb_offsets(int d) {
+    CbBlockOffsets o;
+    o.kc = 0;
+    o.vc = 8 * d;
+    o.vm = 16 * d;
+    o.kq = 24 * d;
+    return o;
+}
+
+// The one dequantisation rule: one fp32 rounding of code*s + z.
+__device__ __forceinline__ float dequant(uint32_t code, float s, float z) {
+    return __fmaf_rn(__uint2float_rn(code), s, z);
+}
+
+// Key code of (token t, channel c) in a token-major code array.
+__device__ __forceinline__ uint32_t key_code(const uint32_t* kc, int t, int c, int d, int bits) {
+    const int per = 32 / bits;
+    const uint32_t w = kc[t * (d / per) + c / per];
+    return (w >> (bits * (c % per))) & ((1u << bits) - 1u);
+}
+// Value code of (token t, channel c) in a channel-major code array.
+__device__ __forceinline__ uint32_t val_code(const uint32_t* vc, int t, int c, int bits) {
+    const int per = 32 / bits;
+    const uint32_t w = vc[c * bits + t / per];
+    return (w >> (bits * (t % per))) & ((1u << bits) - 1u);
+}
+
+// ---- dtype helpers ---------------------------------------------------------
+__device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype);
+
+// Dequantised (key, value) of token t, channel ch of one block, in fp32 before
+// any rounding to the I/O dtype.  `cent` is the [d][4] centroid table of the
+// block's (batch, kv head) for codebook blocks, else unused.
+__device__ __forceinline__ float2 block_entry(int cls, const unsigned char* blk, int d, int raw_dtype,
+                                              const float* cent, int t, int ch) {
+    if (cls == CLS_RAW16) {
+        const uint16_t* r = reinterpret_cast<const uint16_t*>(blk);
+        return make_float2(raw16_to_f32(r[t * d + ch], raw_dtype),
+                           raw16_to_f32(r[kBlockTokens * d + t * d + ch], raw_dtype));
+    }
+    if (cls == CLS_CB2) {
+        const CbBlockOffsets o = cb_offsets(d);
+        const uint32_t ki = key_code(reinterpret_cast<const uint32_t*>(blk + o.kc), t, ch, d, 2);
+        const float2 sv = reinterpret_cast<const float2*>(blk + o.vm)[(ch / 32) * 32 + t];
+        const uint32_t vq = val_code(reinterpret_cast<const uint32_t*>(blk + o.vc), t, ch, 2);
+        return make_float2(cent[ch * 4 + ki], dequant(vq, sv.x, sv.y));
+    }
+    const int bits = cls == CLS_INT4 ? 4 : 2;
+    const IntBlockOffsets o = int_offsets(d, bits);
+    const float2 sk = reinterpret_cast<const float2*>(blk + o.km)[ch];
+    const float2 sv = reinterpret_cast<const float2*>(blk + o.vm)[(ch / 32) * 32 + t];
+    const uint32_t kq = key_code(reinterpret_cast<const uint32_t*>(blk + o.kc), t, ch, d, bits);
+    const uint32_t vq = val_code(reinterpret_cast<const uint32_t*>(blk + o.vc), t, ch, bits);
+    return make_float2(dequant(kq, sk.x, sk.y), dequant(vq, sv.x, sv.y));
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Round an fp32 value to the I/O dtype and back (the attention consumes
+// dequantised entries at the I/O precision).
+template <typename T> __device__ __forceinline__ float round_io(float x) { return to_f32<T>(from_f32<T>(x)); }
+
+// Raw 16-bit cache entry to fp32.
+__device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype) {
+    if (raw_dtype == KV_BF16) return __uint_as_float(((uint32_t)bits) << 16);
+    return __half2float(__ushort_as_half(bits));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// log(sinh(x)/x): the Taylor series of the log (Bernoulli-number
+// coefficients 1/6, -1/180, 1/2835, -1/37800) below 0.5, where its truncation
+// error is < 1e-8; above, x + log1p(-exp(-2x)) - log(2x).
+__device__ __forceinline__ float log_sinhc(float x) {
+    x = fabsf(x);
+    if (x < 0.5f) {
+        const float x2 = x * x;
+        return x2 * (1.0f / 6.0f + x2 * (-1.0f / 180.0f + x2 * (1.0f / 2835.0f - x2 * (1.0f / 37800.0f))));
+    }
+    return x + log1pf(-expf(-2.0f * x)) - logf(2.0f * x);
+}
+
+// Host-side helpers shared by the launch code.
+DevCache make_dev_cache(const kv_cache* c);
+kv_status set_error(kv_status st, const char* fmt, ...);
+kv_status check_launch(const char* what);
+
+}  // namespace bitkv

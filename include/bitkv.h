@@ -1,0 +1,232 @@
+/*
+ * bitkv.h -- C ABI of libbitkv.so: softmax attention over a 2-bit / mixed
+ * FP16-INT4-INT2 / codebook quantised KV cache on NVIDIA B300 (sm_103a).
+ *
+ * Method sources (web pages on KV-cache quantisation for video generation):
+ *   [JB]  "Quantized Keys Steal Attention: Bias Correction for KV-Cache
+ *         Compression in Video Diffusion", abstract.
+ *   [QWM] "QuantWM: Temporally Consistent 2-Bit KV Cache Quantization for
+ *         Video World Models", Innovations and Methodology.
+ *   [WQ]  WindowQuant paper note (zenn.dev), sections 何が新しいのか,
+ *         技術的に面白い点, 実装者視点で気になった点.
+ *
+ * Conventions for every call:
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     (host) pointers are ordinary host memory.  The library allocates no
+ *     memory and keeps no state except a thread-local error message.
+ *   - Tensors are row-major [B][H][L][d] with d contiguous, 16-byte aligned.
+ *   - GQA: query head h reads kv head h / (Hq / Hkv).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device
+ *     work is enqueued asynchronously; host-only calls are synchronous.
+ *   - Every call returns a kv_status.  On failure nothing is launched (except
+ *     KV_ERR_CUDA, reported after a failed launch) and kv_last_error() gives
+ *     the reason.  Nothing throws across the ABI.
+ */
+#ifndef BITKV_H
+#define BITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,  /* bad size, null pointer, inconsistent arguments */
+    KV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype/d/kind combination) */
+    KV_ERR_CAPACITY = 3,     /* append would exceed the layout's block capacity */
+    KV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than kv_attention_workspace() */
+    KV_ERR_ALIGNMENT = 5,    /* a pointer is not 16-byte aligned */
+    KV_ERR_CUDA = 6,         /* a CUDA launch or query failed */
+    KV_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up */
+} kv_status;
+
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
+
+/* Cache kinds.
+ *   UNIFORM2 / UNIFORM4: every block INT2 / INT4 ([JB] INT2 cache with step sizes).
+ *   MIXED: per-window FP16 / INT4 / INT2 chosen by kv_window_plan ([WQ]).
+ *   CODEBOOK2: 2-bit centroid indices per key channel + INT2 values, with
+ *              optional PSAC coefficients ([QWM]). */
+typedef enum { KV_UNIFORM2 = 0, KV_UNIFORM4 = 1, KV_MIXED = 2, KV_CODEBOOK2 = 3 } kv_kind;
+
+/* Segments of a (batch, kv-head) stream, in memory order ([WQ] 技術的に面白い点:
+ * windows of one bit-width are stored together).  UNIFORM4 uses only the INT4
+ * segment, UNIFORM2 and CODEBOOK2 only the INT2 segment. */
+enum { KV_SEG_RAW16 = 0, KV_SEG_INT4 = 1, KV_SEG_INT2 = 2, KV_NUM_SEG = 3 };
+
+typedef enum {
+    KV_REGION_DATA = 0,      /* packed blocks: B * Hkv * stream_bytes bytes */
+    KV_REGION_BLK_LEN = 1,   /* int32 [B][cap_total]: valid tokens per block */
+    KV_REGION_BLK_POS = 2,   /* int32 [B][cap_total]: logical position of a block's first token */
+    KV_REGION_CENTROIDS = 3, /* float [B][Hkv][d][4]: CODEBOOK2 key centroids */
+    KV_REGION_PSAC_U = 4     /* float [B][Hkv][d][r]: CODEBOOK2 PSAC basis (row-major d x r) */
+} kv_region;
+
+/* Packed block format (32 token slots of one batch row and kv head).
+ *   INT2/INT4 (b bits): Kc uint32[32][d*b/32] key codes token-major (channel c
+ *     of token t at word t*(d*b/32) + c/(32/b), bit b*(c mod 32/b));
+ *     Km float2[d] per-channel (step s, zero z); Vc uint32[d][b] value codes
+ *     channel-major (token t of channel c at word c*b + t/(32/b), bit
+ *     b*(t mod 32/b)); Vm float2[d/32][32] per-(32-channel group, token) (s, z).
+ *   RAW16: K 16-bit[32][d] then V 16-bit[32][d] in raw_dtype.
+ *   CODEBOOK2: Kc uint32[32][d/16] centroid indices token-major; Vc uint32[d][2];
+ *     Vm float2[d/32][32]; Kq fp16[32][ceil8(r)] PSAC coefficients.
+ * Quantisation ([JB] step sizes; [WQ] INT2/INT4): per group m = min, M = max,
+ * s = fl32(fl32(M-m)/(2^b-1)), code = clamp(rint(fl32(fl32(x-m)/s)), 0, 2^b-1),
+ * z = m; dequantised x = fmaf(code, s, z).  Key groups are 32 tokens of one
+ * channel (one block, aligned to each appended chunk); value groups are 32
+ * channels of one token.  Pad slots hold code 0 and zero metadata. */
+typedef struct {
+    int32_t B, Hkv, d;          /* d: multiple of 32, <= 256 */
+    int32_t kind;               /* kv_kind */
+    int32_t raw_dtype;          /* MIXED: dtype of RAW16 blocks (KV_F16 or KV_BF16) */
+    int32_t psac_rank;          /* CODEBOOK2: r in [0, 32] */
+    int32_t cap_blocks[KV_NUM_SEG]; /* capacity per segment, in 32-token blocks */
+    /* derived by kv_layout_init: */
+    int64_t block_bytes[KV_NUM_SEG];
+    int64_t seg_offset[KV_NUM_SEG];
+    int64_t stream_bytes;       /* bytes per (batch, kv head) */
+} kv_layout;
+
+/* A cache: the caller allocates every region (sizes from kv_layout_bytes),
+ * zero-fills DATA, and keeps this struct on the host.  n_blocks / n_tokens
+ * are host-side counters updated by kv_quantize_append. */
+typedef struct {
+    kv_layout layout;
+    void* data;          /* (device) */
+    int32_t* blk_len;    /* (device) */
+    int32_t* blk_pos;    /* (device) */
+    float* centroids;    /* (device) CODEBOOK2 only, else NULL */
+    float* psac_u;       /* (device) CODEBOOK2 with psac_rank > 0, else NULL */
+    int32_t n_blocks[KV_NUM_SEG];
+    int32_t n_tokens;
+} kv_cache;
+
+typedef struct {
+    /* MIXED only: bit-width (16, 4 or 2) of each 32-token window of this
+     * append, [B][ceil(n_tokens/32)], once in host memory (used for counts and
+     * validation) and once on the device (read by the kernel). */
+    const int8_t* window_bits_host;
+    const int8_t* window_bits_dev;
+} kv_append_opts;
+
+typedef enum { KV_JENSEN_OFF = 0, KV_JENSEN_TAYLOR2 = 1, KV_JENSEN_EXACT = 2 } kv_jensen;
+
+typedef enum {
+    KV_PATH_AUTO = 0,   /* decode kernel for n_q == 1, tensor-core kernel for bf16 d=128 chunks, else SIMT */
+    KV_PATH_SIMT = 1,   /* CUDA-core fp32 kernel, any dtype/kind */
+    KV_PATH_TC = 2,     /* tcgen05/TMEM kernel: bf16, d = 128, UNIFORM2 / UNIFORM4 / CODEBOOK2 */
+    KV_PATH_DECODE = 3  /* split-K streaming decode: n_q == 1, f16/bf16, d = 64 or 128 */
+} kv_path;
+
+typedef struct {
+    float scale;         /* logit scale tau; 0 -> 1/sqrt(d) */
+    int32_t jensen;      /* kv_jensen; applies to quantised cached keys only ([JB]) */
+    int32_t psac;        /* 1: add tau (U^T q) . coeff for CODEBOOK2 caches ([QWM] PSAC) */
+    int32_t out_f32;     /* 1: `out` is fp32 whatever the I/O dtype */
+    int32_t num_splits;  /* key-range splits per (batch, head); 0 = automatic */
+    int32_t path;        /* kv_path */
+} kv_attn_opts;
+
+typedef struct {
+    double frac_fp16;    /* share of ranked windows kept FP16 (default 0.2) */
+    double frac_int4;    /* share of ranked windows at INT4 (default 0.3) */
+    int32_t force_first; /* 1: window 0 is FP16 regardless of similarity */
+} kv_thresholds;
+
+/* Fill a layout and its derived sizes.  Host only. */
+kv_status kv_layout_init(kv_layout* out, int B, int Hkv, int d, kv_kind kind, kv_dtype raw_dtype,
+                         const int32_t cap_blocks[KV_NUM_SEG], int psac_rank);
+
+/* Bytes the caller must allocate for `region` (0 if the region is unused). */
+size_t kv_layout_bytes(const kv_layout* layout, kv_region region);
+
+/* Bind caller-allocated regions to a cache and zero its counters.  Host only;
+ * checks null pointers and 16-byte alignment of `data`. */
+kv_status kv_cache_init(kv_cache* cache, const kv_layout* layout, void* data, int32_t* blk_len,
+                        int32_t* blk_pos, float* centroids, float* psac_u);
+
+/* Quantise, pack and append one finished chunk ([JB]: the cache of previously
+ * generated chunks; [WQ]: grouped layout).  K, V (device): [B][Hkv][n_tokens][d]
+ * in `dtype`.  UNIFORM*: the chunk starts new blocks (the last may be partial).
+ * MIXED: the cache position must be a multiple of 32, each window goes to the
+ * segment of its bit-width; per-segment window counts must agree across B.
+ * CODEBOOK2: centroids (and psac_u if r > 0) must be filled first.  Fails with
+ * KV_ERR_CAPACITY before launching if a segment would overflow.  Updates
+ * cache->n_blocks and cache->n_tokens on the host. */
+kv_status kv_quantize_append(const void* K, const void* V, kv_dtype dtype, int n_tokens, kv_cache* cache,
+                             const kv_append_opts* opts, void* stream);
+
+/* Workspace bytes kv_attention needs for the same arguments (split partials). */
+size_t kv_attention_workspace(const kv_cache* cache, kv_dtype dtype, int n_q, int n_cur, int Hq,
+                              const kv_attn_opts* opts);
+
+/* o_i = sum_j softmax_j(l_ij) v_j over the cache's valid tokens and the
+ * current chunk ([JB]: chunk-wise autoregressive attention, current chunk
+ * unquantised and bidirectional).  l_ij = tau q_i.k_hat_j - delta_ij (+ PSAC)
+ * for cached keys, tau q_i.k_j for current keys.  Jensen delta ([JB]):
+ * TAYLOR2 (tau^2/24) sum_c q_c^2 s_c^2, EXACT sum_c log(sinh x_c / x_c) with
+ * x_c = tau q_c s_c / 2, using the step sizes of the key's group; zero for
+ * RAW16 windows and codebook keys.  Dequantised cache entries are rounded to
+ * the I/O dtype before the products.
+ *   Q (device) [B][Hq][n_q][d]; Kcur, Vcur (device) [B][Hkv][n_cur][d] (may be
+ *   NULL when n_cur == 0); out (device) [B][Hq][n_q][d] in dtype (fp32 if
+ *   opts->out_f32); lse (device, nullable) fp32 [B][Hq][n_q] natural-log
+ *   partition function.  workspace (device) of ws_bytes >= kv_attention_workspace(). */
+kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q, int n_cur,
+                       int Hq, const kv_cache* cache, const kv_attn_opts* opts, void* out, float* lse,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* Per-window bit-widths from window/question similarity ([WQ] 何が新しいのか
+ * table, 技術的に面白い点: first window FP16).  Host only.  sim (host) [n_windows];
+ * windows 1..W-1 (0..W-1 if !force_first) ranked by sim descending, ties to
+ * the lower index; ranks [0, floor(f16*n)) FP16, [.., floor((f16+f4)*n)) INT4,
+ * the rest INT2 (fp64 arithmetic).  bits_out (host) [n_windows] in {16,4,2};
+ * perm_out (host, nullable) [n_windows]: window stored at each physical block
+ * (FP16, then INT4, then INT2, ascending window index within each). */
+kv_status kv_window_plan(const float* sim, int n_windows, const kv_thresholds* th, int8_t* bits_out,
+                         int32_t* perm_out);
+
+/* Fit CODEBOOK2 key centroids ([QWM] QSAC): per (b, kv head, channel) 1-D
+ * Lloyd k-means, 4 centroids, quantile init x_(floor((2k+1)n/8)), `iters`
+ * iterations, nearest by fp64 |x - mu| (ties to the lower index), exact fp64
+ * member sums, empty clusters keep their centroid.  K (device)
+ * [B][Hkv][n_tokens][d] (bf16/f16/f32); writes cache->centroids as fp32.
+ * Qhist (device, nullable) [B][Hkv][n_hist][d] in dtype: if given, the
+ * per-channel sensitivity mean q_c^2 is written to weights_out (device,
+ * [B][Hkv][d] fp32); it is a per-channel constant and does not change the
+ * centroids.  workspace (device) >= kv_codebook_workspace(). */
+size_t kv_codebook_workspace(const kv_layout* layout, int n_tokens);
+kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, int iters,
+                          const void* Qhist, int n_hist, float* weights_out, void* workspace, size_t ws_bytes,
+                          void* stream);
+
+/* PSAC basis ([QWM] principal-subspace compensation): for each (b, kv head) the
+ * top-r eigenvectors of the uncentred second moment (1/n) sum q q^T of the
+ * historical queries Qhist (device) [B][Hkv][n_hist][d], largest-magnitude
+ * entry of each made positive.  Writes cache->psac_u (fp32 [d][r]) and, if
+ * eigvals_out (device) is non-null, the r eigenvalues [B][Hkv][r].  Cyclic
+ * Jacobi in fp64 on the device; workspace >= kv_psac_workspace(). */
+size_t kv_psac_workspace(const kv_layout* layout);
+kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache* cache, float* eigvals_out,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Debug: write the cache's dequantised entries as fp32 in logical token
+ * order, K_out and V_out (device) [B][Hkv][n_tokens][d], computed by the same
+ * device dequantisation routine the attention kernels use (before rounding
+ * to the I/O dtype).  Positions never appended are left untouched. */
+kv_status kv_dequantize(const kv_cache* cache, float* K_out, float* V_out, void* stream);
+
+/* Message of the last failure on this thread ("" if none). */
+const char* kv_last_error(void);
+
+/* Library version string. */
+const char* kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BITKV_H */

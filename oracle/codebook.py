@@ -89,8 +89,9 @@ def encode_cb_blocks(Kb, Vb, cent, coeff, nvalid, r):
     if r:
         cq[:, :nvalid, :r] = coeff[:, :nvalid]
     raw = np.concatenate([pack_codes(idx, 2).reshape(N, -1).view(np.uint8),
-                          pack_codes(vc.reshape(N, T, d), 2).reshape(N, -1).view(np.uint8),
-                          np.stack([vs, vz], -1).astype(F32).reshape(N, -1).view(np.uint8),
+                          pack_codes(vc.reshape(N, T, d).transpose(0, 2, 1), 2).reshape(N, -1).view(np.uint8),
+                          np.ascontiguousarray(np.stack([vs, vz], -1).astype(F32).transpose(0, 2, 1, 3))
+                          .reshape(N, -1).view(np.uint8),
                           cq.reshape(N, -1).view(np.uint8)], axis=1)
     khat = cent[np.arange(d)[None, None, :], idx].astype(F32)
     vhat = dequantize(vc, vs[..., None], vz[..., None]).reshape(N, T, d)

@@ -11,17 +11,21 @@ byte.
 Block: 32 token slots of one (batch, kv-head).  Classes and their bytes, for
 head dim d:
 
-  INT2 / INT4 (b bits):  Kc  uint32[32][d*b/32]   key codes, slot-major
+  INT2 / INT4 (b bits):  Kc  uint32[32][d*b/32]   key codes, token-major: channel c of
+                                                  token t at word t*(d*b/32) + c/(32/b)
                          Km  float2[d]            per-channel (s, z) of the block
-                         Vc  uint32[32][d*b/32]   value codes
-                         Vm  float2[32][d/32]     per-token, per-32-channel (s, z)
+                         Vc  uint32[d][b]         value codes, channel-major: token t of
+                                                  channel c at word c*b + t/(32/b)
+                         Vm  float2[d/32][32]     per-(32-channel group, token) (s, z)
   RAW16:                 K   16-bit[32][d], then V 16-bit[32][d]  (fp16 or bf16)
-  CODEBOOK2:             Kc  uint32[32][d/16]     2-bit centroid indices
-                         Vc  uint32[32][d/16]     INT2 value codes
-                         Vm  float2[32][d/32]
+  CODEBOOK2:             Kc  uint32[32][d/16]     2-bit centroid indices, token-major
+                         Vc  uint32[d][2]         INT2 value codes, channel-major
+                         Vm  float2[d/32][32]
                          Kq  fp16[32][rp]         PSAC coefficients, rp = ceil8(r)
 
-Code c of a row sits at bit b*(c mod 32/b) of word c div (32/b).  Pad slots
+Within a word, element i (channel for Kc, token for Vc) sits at bit
+b*(i mod 32/b).  Keys are token-major because a key row feeds Q K^T;
+values are channel-major because a value column feeds P V.  Pad slots
 (a block's valid length < 32) hold code 0, zero value metadata and zero raw
 entries.  Key groups are the blocks themselves: each appended chunk starts a
 new block, so a 1560-token chunk gives 48 full blocks and one of 24 tokens.
@@ -93,9 +97,9 @@ def encode_int_blocks(Kb, Vb, bits, nvalid):
     vs[:, nvalid:] = 0
     vz[:, nvalid:] = 0
     kw = pack_codes(kc, bits)                                  # [N,32,d*b/32]
-    vw = pack_codes(vc.reshape(N, T, d), bits)
+    vw = pack_codes(vc.reshape(N, T, d).transpose(0, 2, 1), bits)   # [N,d,b]
     km = np.stack([ks, kz], -1).astype(F32)                    # [N,d,2]
-    vm = np.stack([vs, vz], -1).astype(F32)                    # [N,32,d/32,2]
+    vm = np.stack([vs, vz], -1).astype(F32).transpose(0, 2, 1, 3)   # [N,d/32,32,2]
     raw = np.concatenate([kw.reshape(N, -1).view(np.uint8), km.reshape(N, -1).view(np.uint8),
                           vw.reshape(N, -1).view(np.uint8), vm.reshape(N, -1).view(np.uint8)], axis=1)
     khat = dequantize(kc, ks[:, None, :], kz[:, None, :])

@@ -81,7 +81,7 @@ def quantize_groups(x, bits, n_valid=None):
     mx = xv.max(axis=-1).astype(F32)
     m = (m + F32(0.0)).astype(F32)               # -0.0 -> +0.0
     D = (mx - m).astype(F32)
-    s = (D / qmax).astype(F32)
+    s = ((D / qmax).astype(F32) + F32(0.0)).astype(F32)   # -0.0 -> +0.0
     s_safe = np.where(s > 0, s, F32(1.0)).astype(F32)
     t = ((xv - m[..., None]).astype(F32) / s_safe[..., None]).astype(F32)
     code = np.clip(np.rint(t), 0, qmax)

@@ -70,8 +70,12 @@ def test_uniform_builder_chunk_alignment_and_bytes():
     assert (kc == codes.T).all() and (km[:, 0] == s).all() and (km[:, 1] == z).all()
     # pad slots of the 18-token block are zero
     raw1 = cache.data[0, 0, bb:2 * bb]
-    vm = raw1[1536:2048].view(np.float32).reshape(32, 2, 2)
-    assert (vm[18:] == 0).all()
+    vm = raw1[1536:2048].view(np.float32).reshape(2, 32, 2)     # [group][token][s,z]
+    assert (vm[:, 18:] == 0).all() and (vm[:, :18, 0] > 0).all()
+    vc = quant.unpack_codes(raw1[1024:1536].view(np.uint32).reshape(64, 2), 2, 32)   # [channel][token]
+    V = c["V_cache"][0, 0, 32:50]
+    codes_v, _, _ = quant.quantize_groups(V.reshape(18, 2, 32), 2)
+    assert (vc[:, :18] == codes_v.reshape(18, 64).T).all() and (vc[:, 18:] == 0).all()
     lg = cache.logical(0, 1)
     assert lg["khat"].shape == (90, 64)
 
