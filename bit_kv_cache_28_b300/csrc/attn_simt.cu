@@ -107,7 +107,7 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
                 const int t = e / D, ch = e % D;
                 const float2 kv = t < len ? block_entry(cls, blk, D, c.raw_dtype, cent, t, ch) : make_float2(0.f, 0.f);
                 Ks[t * ld + ch] = round_io<T>(kv.x);
-                Vs[t * ld + ch] = round_io<T>(kv.y);
+                Vs[t * ld + ch] = round_val<T>(kv.y);
             }
             if (cls == CLS_INT2 || cls == CLS_INT4) {
                 quantised = 1;
@@ -240,6 +240,23 @@ __global__ void lse_merge_kernel(const float* __restrict__ ws_o, const float2* _
 }
 
 }  // namespace
+
+kv_status launch_lse_merge(kv_dtype dt, const float* ws_o, const float2* ws_ml, int n_splits, long long rows, int d,
+                           void* out, int out_f32, float* lse, cudaStream_t st) {
+    switch (dt) {
+        case KV_F32:
+            lse_merge_kernel<float><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out, out_f32, lse);
+            break;
+        case KV_F16:
+            lse_merge_kernel<__half><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out, out_f32, lse);
+            break;
+        case KV_BF16:
+            lse_merge_kernel<__nv_bfloat16><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out,
+                                                                            out_f32, lse);
+            break;
+    }
+    return check_launch("lse_merge_kernel");
+}
 
 int simt_units_cache(const kv_cache* c) { return c->n_blocks[0] + c->n_blocks[1] + c->n_blocks[2]; }
 

@@ -137,6 +137,11 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // dequantised entries at the I/O precision).
 template <typename T> __device__ __forceinline__ float round_io(float x) { return to_f32<T>(from_f32<T>(x)); }
 
+// Dequantised cache values enter P V at fp16 for 16-bit I/O (11 significant bits
+// for the attention weights) and at fp32 for fp32 I/O.
+template <typename T> __device__ __forceinline__ float round_val(float x) { return __half2float(__float2half_rn(x)); }
+template <> __device__ __forceinline__ float round_val<float>(float x) { return x; }
+
 // Raw 16-bit cache entry to fp32.
 __device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype) {
     if (raw_dtype == KV_BF16) return __uint_as_float(((uint32_t)bits) << 16);

@@ -112,13 +112,26 @@ def lse_merge(ms, ls, os_):
     return o, m + np.log(l)
 
 
+def value_dtype(io_dtype):
+    """Precision of the dequantised cache values entering P V.
+
+    Keys are consumed at the I/O dtype (the Q K^T operands).  The P V product of
+    16-bit inputs runs in fp16: attention weights carry 11 significant bits
+    there, where bf16 would leave 8 and an output error of up to 2^-9 |v|.  So
+    for 16-bit I/O the dequantised values are rounded to fp16, and for fp32
+    I/O they stay fp32.
+    """
+    return "f32" if io_dtype == "f32" else "f16"
+
+
 def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN_OFF,
                          psac_U=None, rows=None):
     """Reference attention for every (b, q-head).
 
     cache : oracle.layout.Cache (or codebook cache) holding the dequantised view.
     Q     : fp32 [B, Hq, nq, d]; Kcur, Vcur: fp32 [B, Hkv, nn, d] (may have nn = 0).
-    io_dtype: 'f32' | 'f16' | 'bf16' -- dequantised cache entries are rounded to it.
+    io_dtype: 'f32' | 'f16' | 'bf16' -- dequantised cache keys are rounded to it, cache
+              values to value_dtype(io_dtype).
     psac_U: optional fp32 [B, Hkv, d, r]; adds tau (U^T q) . coeff for cached keys.
     rows  : optional index array of query rows to evaluate (all if None).
     GQA: q-head h reads kv-head h // (Hq // Hkv).
@@ -139,7 +152,7 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
         for hk in range(Hkv):
             lg = cache.logical(b, hk)
             Kc = round_to(lg["khat"], io_dtype)
-            Vc = round_to(lg["vhat"], io_dtype)
+            Vc = round_to(lg["vhat"], value_dtype(io_dtype))
             for hq in range(hk * grp, (hk + 1) * grp):
                 q = Q[b, hq, rows].astype(F64)
                 delta = None

@@ -130,3 +130,55 @@ def test_chunk_workload_simt_sampled():
         ro, rl = OA.attention_over_cache(view, case["Q"][:, h:h + 1], case["K_cur"][:, h:h + 1],
                                          case["V_cur"][:, h:h + 1], "bf16", jensen=1, rows=rows)
         check(o[:, h:h + 1], l[:, h:h + 1], ro, rl, "bf16", True, rows=rows)
+
+
+# ------------------------------------------------------ tensor-core path -----
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("jensen", [0, 1, 2])
+def test_chunk_small_tc(bits, jensen):
+    """tcgen05 kernel: ragged cache blocks, ragged current tile, partial query tile, GQA."""
+    case = synth.chunk_case(61, B=2, Hkv=2, Hq=4, d=128, chunks=[300, 77], n_cur=150, n_q=150, dtype="bf16")
+    tc = gpu_uniform(case, bits)
+    oc = oracle_uniform(case, bits)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen)
+    for splits in (1, 3):
+        for out_f32 in (True, False):
+            o, l = run_attention(tc, case, jensen=jensen, out_f32=out_f32, path=B.KV_PATH_TC, splits=splits)
+            check(o, l, ro, rl, "bf16", out_f32)
+
+
+def test_tc_only_current_or_only_cache():
+    case = synth.chunk_case(62, B=1, Hkv=2, d=128, chunks=[200], n_cur=130, n_q=64, dtype="bf16")
+    empty = B.TorchCache(1, 2, 128, B.KV_UNIFORM2, (0, 0, 8))
+    oc0 = OL.build_uniform(case["K_cache"][:, :, :0], case["V_cache"][:, :, :0], 2, [], 8)
+    ro, rl = OA.attention_over_cache(oc0, case["Q"], case["K_cur"], case["V_cur"], "bf16")
+    o, l = run_attention(empty, case, out_f32=True, path=B.KV_PATH_TC)
+    check(o, l, ro, rl, "bf16", True)
+    tc = gpu_uniform(case, 2)
+    oc = oracle_uniform(case, 2)
+    z = np.zeros((1, 2, 0, 128), np.float32)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], z, z, "bf16", jensen=1)
+    o, l = run_attention(tc, case, out_f32=True, jensen=1, path=B.KV_PATH_TC, Kcur=z, Vcur=z)
+    check(o, l, ro, rl, "bf16", True)
+
+
+@pytest.mark.parametrize("jensen", [0, 1])
+def test_chunk_workload_tc_sampled(jensen):
+    """Full chunk workload through the dispatch the benchmark uses: sampled rows vs the oracle,
+    and every row vs the CUDA-core kernel."""
+    case = synth.chunk()
+    tc = gpu_uniform(case, 2)
+    oc = oracle_uniform(case, 2)
+    o_tc, l_tc = run_attention(tc, case, jensen=jensen, out_f32=True)              # auto path
+    o_bf, _ = run_attention(tc, case, jensen=jensen, out_f32=False)
+    o_si, l_si = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_SIMT)
+    assert np.abs(o_tc - o_si).max() < 2e-3 and np.abs(l_tc - l_si).max() < 2e-3
+    rows = np.random.default_rng(1).choice(1560, 40, replace=False)
+    for h in [0, 11, 23]:
+        view = OL.Cache(1, 1, 128, oc.classes, oc.caps)
+        view.blocks = [[oc.blocks[0][h]]]
+        ro, rl = OA.attention_over_cache(view, case["Q"][:, h:h + 1], case["K_cur"][:, h:h + 1],
+                                         case["V_cur"][:, h:h + 1], "bf16", jensen=jensen, rows=rows)
+        check(o_tc[:, h:h + 1], l_tc[:, h:h + 1], ro, rl, "bf16", True, rows=rows)
+        check(o_bf[:, h:h + 1], l_tc[:, h:h + 1], ro, rl, "bf16", False, rows=rows)
