@@ -150,14 +150,10 @@ class Runner:
         self.ws_bytes = B.kv_attention_workspace(self.tc.c, self.dt, spec["n_q"], spec["n_cur"], spec["Hq"],
                                                  self.opts)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
-        path = self.tc  # noqa: F841
-        self.launches_per_step = self._launches()
-
-    def _launches(self):
-        from bit_kv_cache_28_b300 import bitkv as B
+        self.path, self.splits = B.kv_attention_plan(self.tc.c, self.dt, spec["n_q"], spec["n_cur"], spec["Hq"],
+                                                     self.opts)
         # attention kernel (+ one merge launch when the key range is split) + one append launch
-        splits_ws = self.ws_bytes > 0
-        return 2 + (1 if splits_ws else 0)
+        self.launches_per_step = 2 + (1 if self.splits > 1 else 0)
 
     def rewind(self):
         n_blocks, n_tok = self.saved
@@ -264,7 +260,8 @@ def run_own(args, rank, world, dist):
         "append_gbs": spec["append_bytes"] / t_app / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": traffic_for("attn", spec["name"]),
-                     "kernel": "attention", "peak_source": peak_src,
+                     "kernel": {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_decode_kernel"}.get(r.path),
+                     "splits": r.splits, "peak_source": peak_src,
                      "roofline_frac_of_step": (max(spec["cache_bytes"] / (peaks["hbm_gbs"] * 1e9),
                                                    flops / (tc_peak * 1e12)) / t_step)},
         "e2e": {"value": world * rows / t_e2e, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,

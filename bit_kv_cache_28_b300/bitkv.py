@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3:
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_append", "kv_attention_workspace",
-           "kv_attention", "kv_window_plan", "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
+           "kv_attention_plan", "kv_attention", "kv_window_plan", "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
            "kv_psac_basis", "kv_dequantize", "kv_last_error", "kv_version"]
 
 
@@ -81,6 +81,8 @@ def lib():
             "kv_cache_init": (C.c_int, [C.POINTER(kv_cache), C.POINTER(kv_layout), P, P, P, P, P]),
             "kv_quantize_append": (C.c_int, [P, P, I, I, C.POINTER(kv_cache), C.POINTER(kv_append_opts), P]),
             "kv_attention_workspace": (S, [C.POINTER(kv_cache), I, I, I, I, C.POINTER(kv_attn_opts)]),
+            "kv_attention_plan": (C.c_int, [C.POINTER(kv_cache), I, I, I, I, C.POINTER(kv_attn_opts),
+                                            C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
             "kv_attention": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P, P, P, S, P]),
             "kv_window_plan": (C.c_int, [P, I, C.POINTER(kv_thresholds), P, P]),
             "kv_codebook_workspace": (S, [C.POINTER(kv_layout), I]),
@@ -154,6 +156,14 @@ def kv_quantize_append(K, V, dtype, n_tokens, cache: kv_cache, opts: kv_append_o
 def kv_attention_workspace(cache, dtype, n_q, n_cur, Hq, opts: kv_attn_opts | None = None) -> int:
     return int(lib().kv_attention_workspace(C.byref(cache), dtype, n_q, n_cur, Hq,
                                             C.byref(opts) if opts is not None else None))
+
+
+def kv_attention_plan(cache, dtype, n_q, n_cur, Hq, opts: kv_attn_opts | None = None):
+    """(path, splits) kv_attention would use; launches nothing."""
+    path, splits = C.c_int32(0), C.c_int32(0)
+    _check(lib().kv_attention_plan(C.byref(cache), dtype, n_q, n_cur, Hq,
+                                   C.byref(opts) if opts is not None else None, C.byref(path), C.byref(splits)))
+    return path.value, splits.value
 
 
 def kv_attention(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, opts, out, lse=None, workspace=None, ws_bytes=0,

@@ -289,6 +289,17 @@ size_t kv_attention_workspace(const kv_cache* cache, kv_dtype dt, int n_q, int n
     return simt_workspace(cache, n_q, Hq, sp);
 }
 
+kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int n_cur, int Hq,
+                            const kv_attn_opts* opts, int32_t* path_out, int32_t* splits_out) {
+    kv_status s = check_cache(cache);
+    if (s != KV_OK) return s;
+    if (n_q <= 0 || n_cur < 0 || Hq <= 0) return set_error(KV_ERR_INVALID_ARG, "bad sizes");
+    const int path = pick_path(cache, dtype, n_q, Hq, opts);
+    if (path_out) *path_out = path;
+    if (splits_out) *splits_out = pick_splits(cache, path, n_q, n_cur, Hq, opts);
+    return KV_OK;
+}
+
 kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q, int n_cur, int Hq,
                        const kv_cache* cache, const kv_attn_opts* opts, void* out, float* lse, void* workspace,
                        size_t ws_bytes, void* stream) {

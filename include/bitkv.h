@@ -164,6 +164,12 @@ kv_status kv_quantize_append(const void* K, const void* V, kv_dtype dtype, int n
 size_t kv_attention_workspace(const kv_cache* cache, kv_dtype dtype, int n_q, int n_cur, int Hq,
                               const kv_attn_opts* opts);
 
+/* The kernel path (kv_path) and number of key-range splits kv_attention would
+ * use for these arguments.  Host only; launches nothing.  One attention call
+ * launches one kernel, plus one merge kernel when *splits_out > 1. */
+kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int n_cur, int Hq,
+                            const kv_attn_opts* opts, int32_t* path_out, int32_t* splits_out);
+
 /* o_i = sum_j softmax_j(l_ij) v_j over the cache's valid tokens and the
  * current chunk ([JB]: chunk-wise autoregressive attention, current chunk
  * unquantised and bidirectional).  l_ij = tau q_i.k_hat_j - delta_ij (+ PSAC)
