@@ -13,10 +13,13 @@
 //              row from TMEM, applies scale, Jensen delta and the key mask,
 //              keeps a lazily rescaled running max (O is rescaled in TMEM only
 //              when the max grows by more than 2^8), writes P (fp16) to smem.
-//   warps 4-7  producers: dequantise a cache tile (4 blocks) into K_hat
-//              [128 keys x 128] (bf16) and V_hat^T [128 channels x 128 keys]
-//              (fp16) tiles in the 128-byte-swizzled K-major layout, or copy
-//              (and transpose) a current-chunk tile; double-buffered.
+//   warps 4-7  producers: thread 0 bulk-copies (TMA engine) each packed cache
+//              tile -- 4 contiguous blocks -- into a double-buffered staging
+//              area two tiles ahead; all 128 threads dequantise the staged
+//              tile into K_hat [128 keys x 128] (bf16, single buffer: free once
+//              Q K_hat^T of the tile completes) and V_hat^T [128 channels x 128
+//              keys] (fp16, double buffer), 128-byte-swizzled K-major; a
+//              current-chunk tile is read from global memory and transposed.
 //   warp 8     TMEM owner; lane 0 issues S = Q K_hat^T (bf16) and O += P V_hat (fp16).
 // TMEM: S double buffer (columns 0-255), O (256-383).  Every wait is bounded;
 // every warp-collective tcgen05 load/store runs with the whole warp converged.
@@ -47,19 +50,31 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int kTile = kM * kD * 2;          // 32 KB: one 16-bit 128 x 128 operand tile
+constexpr int kStage = 4 * 6144;            // packed bytes of 4 INT4 blocks (INT2: 4 x 4096)
 constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kTile;        // 2 stages
-constexpr int kVOff = kKOff + 2 * kTile;    // 2 stages
+constexpr int kKOff = kQOff + kTile;        // 1 buffer
+constexpr int kVOff = kKOff + kTile;        // 2 stages
 constexpr int kPOff = kVOff + 2 * kTile;
-constexpr int kWOff = kPOff + kTile;        // 2 stages x 4 groups x 128 floats (Jensen weights)
+constexpr int kStgOff = kPOff + kTile;      // 2 staging slots of packed blocks
+constexpr int kWOff = kStgOff + 2 * kStage; // 2 stages x 4 groups x 128 floats (Jensen weights)
 constexpr int kInfoOff = kWOff + 2 * 4 * kD * 4;
-constexpr int kBarOff = kInfoOff + 2 * 32;
-constexpr int kNumBars = 8;
+constexpr int kStgLenOff = kInfoOff + 2 * 32;   // [2][4] valid lengths of the staged blocks
+constexpr int kBarOff = kStgLenOff + 2 * 16;
+constexpr int kNumBars = 13;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kSlotOff + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
 
-enum { BAR_KV_FULL = 0, BAR_KV_EMPTY = 2, BAR_S_FULL = 4, BAR_P_FULL = 6, BAR_O_DONE = 7 };
+enum {
+    BAR_KV_FULL = 0,   // [2] producers -> MMA/softmax: K_hat, V_hat[s], weights[s], info[s] ready
+    BAR_V_EMPTY = 2,   // [2] PV of the stage's tile completed
+    BAR_S_FULL = 4,    // [2] S = Q K_hat^T of the tile in TMEM
+    BAR_P_FULL = 6,    // softmax -> MMA: P written
+    BAR_O_DONE = 7,    // PV completed
+    BAR_K_EMPTY = 8,   // Q K_hat^T completed (K_hat may be overwritten)
+    BAR_STG_FULL = 9,  // [2] staging slot filled by the bulk copy
+    BAR_STG_EMPTY = 11,  // [2] all producers finished reading the staging slot
+};
 
 struct TileInfo {
     int nvalid[4];
@@ -95,84 +110,40 @@ __device__ __forceinline__ uint4 dq8_pack(const uint32_t codes[8], const float s
 }
 
 // ------------------------------------------------------------- producers ----
+// A staged cache tile: 4 consecutive blocks (the missing ones of a short last
+// tile count as empty) in staging slot `stage`, their valid lengths in stg_len.
+struct StagedTile {
+    const unsigned char* stg;
+    const int* len;
+    int nb;   // blocks present
+};
+
+// Values: thread p dequantises channel p of all 128 keys into V_hat^T[stage] and
+// records the tile's key-validity info.
 template <int BITS>
-__device__ void fill_cache_tile(unsigned char* sm, int stage, const DevCache& c, int b, int h, int seg, int tile,
-                                int p, int jensen) {
+__device__ void fill_cache_values(unsigned char* sm, int stage, const StagedTile& st, int p) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    unsigned char* Kt = sm + kKOff + stage * kTile;
+    constexpr int kBlockBytes = 8 * kD * BITS + 16 * kD;
     unsigned char* Vt = sm + kVOff + stage * kTile;
-    float* W = reinterpret_cast<float*>(sm + kWOff) + stage * 4 * kD;
     TileInfo* info = reinterpret_cast<TileInfo*>(sm + kInfoOff) + stage;
-    const int jc = p & 15, r0 = p >> 4;
-    const int nblk = c.n_blocks[seg];
-    constexpr int kWordsPerKey = kD * BITS / 32;
+    if (p < 4) info->nvalid[p] = p < st.nb ? st.len[p] : 0;
+    if (p == 0) info->quantised = 1;
+    const int cc = p;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
-        const int idx = tile * 4 + q;
-        const bool exists = idx < nblk;
-        int len = 0;
-        const unsigned char* blk = nullptr;
-        if (exists) {
-            len = c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + idx];
-            blk = block_ptr(c, b, h, seg, idx);
-        }
-        if (p == 0) info->nvalid[q] = len;
-        // ---- keys: 8 channels (8jc..8jc+7) of 4 tokens of this block
-        float s[8], z[8];
-        if (exists) {
-            const float4* km = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = __ldg(km + k);
-                s[2 * k] = v.x;
-                z[2 * k] = v.y;
-                s[2 * k + 1] = v.z;
-                z[2 * k + 1] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) s[k] = z[k] = 0.0f;
-        }
-        if (r0 == 0) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                W[q * kD + jc * 8 + k] = jensen == KV_JENSEN_EXACT ? s[k] : s[k] * s[k];
-        }
-        const uint32_t* kc = exists ? reinterpret_cast<const uint32_t*>(blk + o.kc) : nullptr;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = r0 + 8 * i;
-            const int row = 32 * q + t;
-            uint4 pk = make_uint4(0, 0, 0, 0);
-            if (exists) {
-                uint32_t codes[8];
-                if (BITS == 2) {
-                    const uint32_t w = __ldg(kc + t * kWordsPerKey + (jc >> 1)) >> (16 * (jc & 1));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (2 * k)) & 3u;
-                } else {
-                    const uint32_t w = __ldg(kc + t * kWordsPerKey + jc);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (4 * k)) & 15u;
-                }
-                pk = dq8_pack<false>(codes, s, z);
-            }
-            *reinterpret_cast<uint4*>(Kt + sw_off(row, jc)) = pk;
-        }
-        // ---- values: channel p, 32 tokens of this block -> 4 chunks of 8 keys
-        const int cc = p;
-        if (exists) {
+        if (q < st.nb) {
+            const unsigned char* blk = st.stg + q * kBlockBytes;
             const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc) + cc * BITS;
             const float4* vm = reinterpret_cast<const float4*>(blk + o.vm) + (cc >> 5) * 16;  // 32 float2
             uint32_t wv[BITS];
 #pragma unroll
-            for (int k = 0; k < BITS; ++k) wv[k] = __ldg(vc + k);
+            for (int k = 0; k < BITS; ++k) wv[k] = vc[k];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 float vs[8], vz[8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float4 v = __ldg(vm + kk * 4 + k);
+                    const float4 v = vm[kk * 4 + k];
                     vs[2 * k] = v.x;
                     vz[2 * k] = v.y;
                     vs[2 * k + 1] = v.z;
@@ -196,7 +167,64 @@ __device__ void fill_cache_tile(unsigned char* sm, int stage, const DevCache& c,
                 *reinterpret_cast<uint4*>(Vt + sw_off(cc, 4 * q + kk)) = make_uint4(0, 0, 0, 0);
         }
     }
-    if (p == 0) info->quantised = 1;
+}
+
+// Keys: thread p dequantises channels 8jc..8jc+7 of keys r0, r0+8, ... into the
+// single K_hat buffer and stores the Jensen weights of its channels.
+template <int BITS>
+__device__ void fill_cache_keys(unsigned char* sm, int stage, const StagedTile& st, int p, int jensen) {
+    const IntBlockOffsets o = int_offsets(kD, BITS);
+    constexpr int kBlockBytes = 8 * kD * BITS + 16 * kD;
+    constexpr int kWordsPerKey = kD * BITS / 32;
+    unsigned char* Kt = sm + kKOff;
+    float* W = reinterpret_cast<float*>(sm + kWOff) + stage * 4 * kD;
+    const int jc = p & 15, r0 = p >> 4;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+        const bool exists = q < st.nb;
+        const unsigned char* blk = st.stg + q * kBlockBytes;
+        float s[8], z[8];
+        if (exists) {
+            const float4* km = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = km[k];
+                s[2 * k] = v.x;
+                z[2 * k] = v.y;
+                s[2 * k + 1] = v.z;
+                z[2 * k + 1] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s[k] = z[k] = 0.0f;
+        }
+        if (r0 == 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                W[q * kD + jc * 8 + k] = jensen == KV_JENSEN_EXACT ? s[k] : s[k] * s[k];
+        }
+        const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = r0 + 8 * i;
+            const int row = 32 * q + t;
+            uint4 pk = make_uint4(0, 0, 0, 0);
+            if (exists) {
+                uint32_t codes[8];
+                if (BITS == 2) {
+                    const uint32_t w = kc[t * kWordsPerKey + (jc >> 1)] >> (16 * (jc & 1));
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (2 * k)) & 3u;
+                } else {
+                    const uint32_t w = kc[t * kWordsPerKey + jc];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (4 * k)) & 15u;
+                }
+                pk = dq8_pack<false>(codes, s, z);
+            }
+            *reinterpret_cast<uint4*>(Kt + sw_off(row, jc)) = pk;
+        }
+    }
 }
 
 // Two bf16 values (half `hf` of two words) converted to an fp16 pair.
@@ -206,49 +234,61 @@ __device__ __forceinline__ uint32_t f16_pair_from_bf16(uint32_t lo_word, uint32_
     return pack_f16(lo, hi);
 }
 
-__device__ void fill_current_tile(unsigned char* sm, int stage, const __nv_bfloat16* Kcur,
-                                  const __nv_bfloat16* Vcur, long long row0, int valid, int p) {
-    unsigned char* Kt = sm + kKOff + stage * kTile;
+// Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T, and
+// the key-validity info.
+__device__ void fill_current_values(unsigned char* sm, int stage, const __nv_bfloat16* Vcur, long long row0,
+                                    int valid, int p) {
     unsigned char* Vt = sm + kVOff + stage * kTile;
     TileInfo* info = reinterpret_cast<TileInfo*>(sm + kInfoOff) + stage;
-    const int jc = p & 15, r0 = p >> 4;
     if (p < 4) info->nvalid[p] = min(32, max(0, valid - 32 * p));
     if (p == 0) info->quantised = 0;
-    const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
     const uint4* Vg = reinterpret_cast<const uint4*>(Vcur + row0 * kD);
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-        const int row = r0 + 8 * i;
-        const uint4 v = row < valid ? __ldg(Kg + row * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Kt + sw_off(row, jc)) = v;
-    }
-    // V^T: 8 keys x 8 channels per step, transposed in registers, bf16 -> fp16
-#pragma unroll 1
+    uint32_t x[2][8][4];                 // both 8x8 blocks' loads in flight before any store
+#pragma unroll
     for (int rep = 0; rep < 2; ++rep) {
         const int bi = p + 128 * rep;
         const int kc8 = bi >> 4, cch = bi & 15;
-        uint32_t x[8][4];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int key = 8 * kc8 + k;
             const uint4 v = key < valid ? __ldg(Vg + key * (kD / 8) + cch) : make_uint4(0, 0, 0, 0);
-            x[k][0] = v.x;
-            x[k][1] = v.y;
-            x[k][2] = v.z;
-            x[k][3] = v.w;
+            x[rep][k][0] = v.x;
+            x[rep][k][1] = v.y;
+            x[rep][k][2] = v.z;
+            x[rep][k][3] = v.w;
         }
+    }
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+        const int bi = p + 128 * rep;
+        const int kc8 = bi >> 4, cch = bi & 15;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             // channel 8cch+i: element i of every key row (word i/2, half i&1)
             const int wi = i >> 1, hf = i & 1;
             uint4 y;
-            y.x = f16_pair_from_bf16(x[0][wi], x[1][wi], hf);
-            y.y = f16_pair_from_bf16(x[2][wi], x[3][wi], hf);
-            y.z = f16_pair_from_bf16(x[4][wi], x[5][wi], hf);
-            y.w = f16_pair_from_bf16(x[6][wi], x[7][wi], hf);
+            y.x = f16_pair_from_bf16(x[rep][0][wi], x[rep][1][wi], hf);
+            y.y = f16_pair_from_bf16(x[rep][2][wi], x[rep][3][wi], hf);
+            y.z = f16_pair_from_bf16(x[rep][4][wi], x[rep][5][wi], hf);
+            y.w = f16_pair_from_bf16(x[rep][6][wi], x[rep][7][wi], hf);
             *reinterpret_cast<uint4*>(Vt + sw_off(8 * cch + i, kc8)) = y;
         }
     }
+}
+
+// Current-chunk keys: bf16 rows copied into the swizzled K_hat buffer.
+__device__ void fill_current_keys(unsigned char* sm, const __nv_bfloat16* Kcur, long long row0, int valid, int p) {
+    unsigned char* Kt = sm + kKOff;
+    const int jc = p & 15, r0 = p >> 4;
+    const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
+    uint4 kv[16];                        // all loads in flight before the first store
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int row = r0 + 8 * i;
+        kv[i] = row < valid ? __ldg(Kg + row * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 8 * i, jc)) = kv[i];
 }
 
 // --------------------------------------------------------------- kernel -----
@@ -272,20 +312,27 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     const int seg = BITS == 4 ? KV_SEG_INT4 : KV_SEG_INT2;
     const int n_cache_tiles = (c.n_blocks[seg] + 3) / 4;
     const int n_tiles = n_cache_tiles + (n_cur + kN - 1) / kN;
-    const int t_begin = (int)((long long)split * n_tiles / n_splits);
-    const int T = (int)((long long)(split + 1) * n_tiles / n_splits) - t_begin;
+    // split s takes tiles s, s + n_splits, ...: every split gets an even share of
+    // cache and current-chunk tiles, and its cache tiles still come first.
+    const int T = split < n_tiles ? (n_tiles - split + n_splits - 1) / n_splits : 0;
+    auto tile_of = [&](int j) { return split + j * n_splits; };
     auto bar = [&](int i) { return sbase + kBarOff + 8 * i; };
 
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(bar(BAR_KV_FULL + 0), 128);
         mbar_init(bar(BAR_KV_FULL + 1), 128);
-        mbar_init(bar(BAR_KV_EMPTY + 0), 1);
-        mbar_init(bar(BAR_KV_EMPTY + 1), 1);
+        mbar_init(bar(BAR_V_EMPTY + 0), 1);
+        mbar_init(bar(BAR_V_EMPTY + 1), 1);
         mbar_init(bar(BAR_S_FULL + 0), 1);
         mbar_init(bar(BAR_S_FULL + 1), 1);
         mbar_init(bar(BAR_P_FULL), 128);
         mbar_init(bar(BAR_O_DONE), 1);
+        mbar_init(bar(BAR_K_EMPTY), 1);
+        mbar_init(bar(BAR_STG_FULL + 0), 1);
+        mbar_init(bar(BAR_STG_FULL + 1), 1);
+        mbar_init(bar(BAR_STG_EMPTY + 0), 128);
+        mbar_init(bar(BAR_STG_EMPTY + 1), 128);
         mbar_fence_init();
     }
     if (warp == 8) tmem_alloc(sbase + kSlotOff, kTmemCols);
@@ -323,7 +370,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                                 (jj > 0 || kk > 0));
                 }
                 mma_commit(bar(BAR_O_DONE));
-                mma_commit(bar(BAR_KV_EMPTY + (jj & 1)));
+                mma_commit(bar(BAR_V_EMPTY + (jj & 1)));
                 return true;
             };
             bool ok = true;
@@ -331,13 +378,14 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 const int s = j & 1;
                 if (!mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 1)) break;
                 fence_after();
-                const uint32_t sK = sbase + kKOff + s * kTile;
+                const uint32_t sK = sbase + kKOff;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
                     mma_f16kind(tmem + s * kN, desc_sw128(sQ + off), desc_sw128(sK + off), kIdescQK, kk > 0);
                 }
                 mma_commit(bar(BAR_S_FULL + s));
+                mma_commit(bar(BAR_K_EMPTY));
                 if (j > 0) ok = issue_pv(j - 1);
             }
             if (ok && T > 0 && !abort_flag) issue_pv(T - 1);
@@ -346,19 +394,57 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     } else if (warp >= 4) {
         // ----------------------------------------------------------- producers
         const int p = tid - 128;
+        const int nblk = c.n_blocks[seg];
+        int* stg_len = reinterpret_cast<int*>(sm + kStgLenOff);
+        // Bulk-copy cache tile j (if it is one) into staging slot j & 1, with its
+        // blocks' valid lengths; run by producer thread 0 two tiles ahead.
+        auto stage_copy = [&](int j) {
+            const int tile = tile_of(j);
+            if (j >= T || tile >= n_cache_tiles) return;
+            const int nb = min(4, nblk - tile * 4);
+            for (int q = 0; q < 4; ++q)
+                stg_len[(j & 1) * 4 + q] = q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
+            const uint32_t bytes = (uint32_t)(nb * c.block_bytes[seg]);
+            const uint32_t sbar = bar(BAR_STG_FULL + (j & 1));
+            mbar_expect_tx(sbar, bytes);
+            bulk_g2s(sbase + kStgOff + (j & 1) * kStage, block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
+        };
+        if (p == 0) {
+            stage_copy(0);
+            stage_copy(1);
+        }
         for (int j = 0; j < T; ++j) {
             const int s = j & 1;
-            if (j >= 2 && !mbar_wait(bar(BAR_KV_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2)) break;
-            const int tile = t_begin + j;
-            if (tile < n_cache_tiles) {
-                fill_cache_tile<BITS>(sm, s, c, b, h, seg, tile, p, jensen);
-            } else {
-                const int t0 = (tile - n_cache_tiles) * kN;
-                fill_current_tile(sm, s, Kcur, Vcur, ((long long)b * c.Hkv + h) * n_cur + t0, min(kN, n_cur - t0),
-                                  p);
-            }
+            const int tile = tile_of(j);
+            const bool cached = tile < n_cache_tiles;
+            bool ok = true;
+            if (j >= 2) ok = mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
+            if (ok && cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            StagedTile st;
+            st.stg = sm + kStgOff + s * kStage;
+            st.len = stg_len + s * 4;
+            st.nb = cached ? min(4, nblk - tile * 4) : 0;
+            const int t0 = (tile - n_cache_tiles) * kN;
+            const long long row0 = ((long long)b * c.Hkv + h) * n_cur + t0;
+            // values first: they only need the V_hat stage, free since PV of tile j - 2
+            if (cached) fill_cache_values<BITS>(sm, s, st, p);
+            else fill_current_values(sm, s, Vcur, row0, min(kN, n_cur - t0), p);
+            // keys: the single K_hat buffer is free once Q K_hat^T of tile j - 1 completed
+            const bool ok2 = j == 0 || mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
+            if (!__all_sync(0xffffffffu, ok2)) break;
+            if (cached) fill_cache_keys<BITS>(sm, s, st, p, jensen);
+            else fill_current_keys(sm, Kcur, row0, min(kN, n_cur - t0), p);
             fence_proxy_async();
             mbar_arrive(bar(BAR_KV_FULL + s));
+            if (cached) {
+                // staging slot s is consumed; thread 0 refills it with tile j + 2 once
+                // every producer has arrived (a bounded wait, like all others)
+                mbar_arrive(bar(BAR_STG_EMPTY + s));
+                if (p == 0 && j + 2 < T && tile_of(j + 2) < n_cache_tiles &&
+                    mbar_wait(bar(BAR_STG_EMPTY + s), (j >> 1) & 1, &abort_flag, err, 10))
+                    stage_copy(j + 2);
+            }
         }
         __syncwarp();
     } else {
@@ -373,37 +459,42 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         float x[kN];
         for (int j = 0; j < T; ++j) {
             const int s = j & 1;
-            const bool ok1 = mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 4) &&
-                             mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
-            if (!__all_sync(0xffffffffu, ok1)) break;
-            fence_after();
-#pragma unroll
-            for (int g = 0; g < 4; ++g) tmem_ld32(tmem + lane_addr + s * kN + 32 * g, x + 32 * g);
+            // the tile's metadata is ready: compute the Jensen terms while Q K^T runs
+            const bool ok0 = mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 4);
+            if (!__all_sync(0xffffffffu, ok0)) break;
             const TileInfo info = reinterpret_cast<const TileInfo*>(sm + kInfoOff)[s];
             float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (info.quantised && jensen != KV_JENSEN_OFF) {
-                const float* W = reinterpret_cast<const float*>(sm + kWOff) + s * 4 * kD;
-#pragma unroll 1
+                const float4* W4 = reinterpret_cast<const float4*>(sm + kWOff) + s * kD;   // [4][32] float4
+#pragma unroll 2
                 for (int ch = 0; ch < 16; ++ch) {
                     const uint4 qv = *reinterpret_cast<const uint4*>(sm + kQOff + sw_off(i, ch));
                     const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                    float qf[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float qf = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
-                        const int cidx = ch * 8 + k;
+                    for (int k = 0; k < 8; ++k)
+                        qf[k] = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float4 wa = W4[g * 32 + 2 * ch], wb = W4[g * 32 + 2 * ch + 1];
+                        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                         if (jensen == KV_JENSEN_TAYLOR2) {
-                            const float q2 = qf * qf;
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) dl[g] = fmaf(q2, W[g * kD + cidx], dl[g]);
+                            for (int k = 0; k < 8; ++k) dl[g] = fmaf(qf[k] * qf[k], w[k], dl[g]);
                         } else {
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(jt * qf * W[g * kD + cidx]);
+                            for (int k = 0; k < 8; ++k) dl[g] += log_sinhc(jt * qf[k] * w[k]);
                         }
                     }
                 }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) dl[g] *= (jensen == KV_JENSEN_TAYLOR2 ? jt : kLog2e);
             }
+            const bool ok1 = mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
+            if (!__all_sync(0xffffffffu, ok1)) break;
+            fence_after();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) tmem_ld32(tmem + lane_addr + s * kN + 32 * g, x + 32 * g);
             float mt = -INFINITY;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
