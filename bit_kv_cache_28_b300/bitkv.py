@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3:
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_append", "kv_attention_workspace",
-           "kv_attention_plan", "kv_attention", "kv_window_plan", "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
+           "kv_attention_plan", "kv_attention", "kv_attention_noalloc", "kv_window_plan", "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
            "kv_psac_basis", "kv_dequantize", "kv_last_error", "kv_version"]
 
 
@@ -84,6 +84,8 @@ def lib():
             "kv_attention_plan": (C.c_int, [C.POINTER(kv_cache), I, I, I, I, C.POINTER(kv_attn_opts),
                                             C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
             "kv_attention": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P, P, P, S, P]),
+            "kv_attention_noalloc": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P,
+                                               P, P]),
             "kv_window_plan": (C.c_int, [P, I, C.POINTER(kv_thresholds), P, P]),
             "kv_codebook_workspace": (S, [C.POINTER(kv_layout), I]),
             "kv_codebook_fit": (C.c_int, [P, I, I, C.POINTER(kv_cache), I, P, I, P, P, S, P]),
@@ -171,6 +173,13 @@ def kv_attention(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, opts, out, lse=Non
     _check(lib().kv_attention(_ptr(Q), _ptr(Kcur), _ptr(Vcur), dtype, n_q, n_cur, Hq, C.byref(cache),
                               C.byref(opts) if opts is not None else None, _ptr(out), _ptr(lse), _ptr(workspace),
                               ws_bytes, _stream(stream)))
+
+
+def kv_attention_noalloc(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, opts, out, lse=None, stream=None):
+    """kv_attention with its scratch in the library's fixed device array (no workspace argument)."""
+    _check(lib().kv_attention_noalloc(_ptr(Q), _ptr(Kcur), _ptr(Vcur), dtype, n_q, n_cur, Hq, C.byref(cache),
+                                      C.byref(opts) if opts is not None else None, _ptr(out), _ptr(lse),
+                                      _stream(stream)))
 
 
 def kv_window_plan(sim, n_windows, thresholds: kv_thresholds | None, bits_out, perm_out=None):

@@ -186,6 +186,32 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
                        int Hq, const kv_cache* cache, const kv_attn_opts* opts, void* out, float* lse,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* kv_attention without a workspace argument, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is unavailable or not allowed
+ * (a host callback, an allocator hook, a plug-in given only its input and
+ * output buffers, a process whose device memory belongs to another
+ * framework).  The source pages have no counterpart; this is a library
+ * convenience.
+ *   Arguments, layouts, results and errors are those of kv_attention.  The
+ *   scratch kv_attention would take from `workspace` comes from one fixed
+ *   device array of KV_NOALLOC_SCRATCH_BYTES inside the library, which every
+ *   GPU that loads the library holds until the process exits.  The call
+ *   allocates and frees nothing.
+ *   With opts->num_splits == 0 the key range is split as kv_attention would
+ *   split it, or less where the partials would not fit; sizes whose scratch
+ *   still exceeds the array (or an explicit num_splits that does) are rejected
+ *   with KV_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  All calls share the one array and find the previous call's
+ *   contents in it (the kernels clear what must start at zero), so calls that
+ *   overlap on the GPU -- on different streams, or from several host threads
+ *   -- race and give wrong results: serialise them. */
+#define KV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+kv_status kv_attention_noalloc(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q,
+                               int n_cur, int Hq, const kv_cache* cache, const kv_attn_opts* opts, void* out,
+                               float* lse, void* stream);
+
 /* Per-window bit-widths from window/question similarity ([WQ] 何が新しいのか
  * table, 技術的に面白い点: first window FP16).  Host only.  sim (host) [n_windows];
  * windows 1..W-1 (0..W-1 if !force_first) ranked by sim descending, ties to
