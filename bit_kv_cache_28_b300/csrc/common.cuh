@@ -4,7 +4,8 @@
 // Block format (32 token slots of one batch row and kv head), head dim d:
 //   INT2/INT4 (b bits): Kc u32[32][d*b/32] token-major | Km float2[d] |
 //                       Vc u32[d][b] channel-major     | Vm float2[d/32][32]
-//   RAW16:              K 16-bit[32][d] | V 16-bit[32][d]
+//   RAW16:              K 16-bit[32][d] | V 16-bit[32][d], 16-byte chunk j of row t
+//                       stored at chunk position j ^ (t mod min(8, d/8))
 //   CODEBOOK2:          Kc u32[32][d/16] | Vc u32[d][2] | Vm float2[d/32][32] | Kq fp16[32][rp]
 // Quantiser (step sizes of "Quantized Keys Steal Attention", abstract; INT2/INT4
 // of the WindowQuant note, table in 何が新しいのか):
@@ -94,6 +95,14 @@ __device__ __forceinline__ uint32_t val_code(const uint32_t* vc, int t, int c, i
     return (w >> (bits * (t % per))) & ((1u << bits) - 1u);
 }
 
+// 16-bit slot of element (t, c) inside the K (or V) half of a RAW16 block: the
+// row's 16-byte chunks are XOR-permuted by the token index so that eight
+// consecutive rows of one chunk column occupy distinct shared-memory banks.
+__host__ __device__ __forceinline__ int raw16_slot(int t, int c, int d) {
+    const int m = (d >= 64 ? 8 : d / 8) - 1;
+    return t * d + ((((c >> 3) ^ (t & m))) << 3) + (c & 7);
+}
+
 // ---- dtype helpers ---------------------------------------------------------
 __device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype);
 
@@ -104,8 +113,8 @@ __device__ __forceinline__ float2 block_entry(int cls, const unsigned char* blk,
                                               const float* cent, int t, int ch) {
     if (cls == CLS_RAW16) {
         const uint16_t* r = reinterpret_cast<const uint16_t*>(blk);
-        return make_float2(raw16_to_f32(r[t * d + ch], raw_dtype),
-                           raw16_to_f32(r[kBlockTokens * d + t * d + ch], raw_dtype));
+        const int slot = raw16_slot(t, ch, d);
+        return make_float2(raw16_to_f32(r[slot], raw_dtype), raw16_to_f32(r[kBlockTokens * d + slot], raw_dtype));
     }
     if (cls == CLS_CB2) {
         const CbBlockOffsets o = cb_offsets(d);

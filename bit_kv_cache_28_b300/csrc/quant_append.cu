@@ -185,14 +185,17 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, De
     const int cls = seg_class(c.kind, seg);
 
     if (cls == CLS_RAW16) {
-        // 16-bit windows keep the input bits unchanged (the dtype equals raw_dtype)
-        uint16_t* rk = reinterpret_cast<uint16_t*>(blk);
-        const uint16_t* Kb = reinterpret_cast<const uint16_t*>(K) + row0;
-        const uint16_t* Vb = reinterpret_cast<const uint16_t*>(V) + row0;
-        for (int e = threadIdx.x; e < kBlockTokens * d; e += blockDim.x) {
-            const int t = e / d;
-            rk[e] = t < nv ? Kb[e] : 0;
-            rk[kBlockTokens * d + e] = t < nv ? Vb[e] : 0;
+        // 16-bit windows keep the input bits unchanged (the dtype equals raw_dtype),
+        // each row's 16-byte chunks moved to their permuted positions
+        uint4* rk = reinterpret_cast<uint4*>(blk);
+        const uint4* Kb = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(K) + row0);
+        const uint4* Vb = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(V) + row0);
+        const int nch = d / 8;
+        for (int e = threadIdx.x; e < kBlockTokens * nch; e += blockDim.x) {
+            const int t = e / nch, j = e % nch;
+            const int dst = raw16_slot(t, 8 * j, d) >> 3;
+            rk[dst] = t < nv ? Kb[e] : make_uint4(0, 0, 0, 0);
+            rk[kBlockTokens * nch + dst] = t < nv ? Vb[e] : make_uint4(0, 0, 0, 0);
         }
     } else {
         for (int e = threadIdx.x; e < kBlockTokens * d; e += blockDim.x) {

@@ -1,10 +1,5 @@
 #include "common.cuh"
 namespace bitkv {
-kv_status launch_attn_decode(const void*, const void*, const void*, kv_dtype, int, int, const kv_cache*, float, int, int,
-                             void*, int, float*, void*, cudaStream_t) { return set_error(KV_ERR_UNSUPPORTED, "decode not built"); }
-size_t decode_workspace(const kv_cache*, int, int) { return 0; }
-int decode_auto_splits(const kv_cache*, int) { return 1; }
-bool decode_supported(const kv_cache*, kv_dtype, int, int) { return false; }
 kv_status launch_codebook_fit(const void*, kv_dtype, int, const kv_cache*, int, const void*, int, float*, void*, cudaStream_t) { return set_error(KV_ERR_UNSUPPORTED, "codebook not built"); }
 size_t codebook_ws_bytes(const kv_layout*, int) { return 0; }
 kv_status launch_psac_basis(const void*, kv_dtype, int, const kv_cache*, float*, void*, cudaStream_t) { return set_error(KV_ERR_UNSUPPORTED, "psac not built"); }

@@ -71,7 +71,9 @@ typedef enum {
  *     Km float2[d] per-channel (step s, zero z); Vc uint32[d][b] value codes
  *     channel-major (token t of channel c at word c*b + t/(32/b), bit
  *     b*(t mod 32/b)); Vm float2[d/32][32] per-(32-channel group, token) (s, z).
- *   RAW16: K 16-bit[32][d] then V 16-bit[32][d] in raw_dtype.
+ *   RAW16: K 16-bit[32][d] then V 16-bit[32][d] in raw_dtype; within each row
+ *     the 16-byte chunk j of token t is stored at chunk position j XOR (t mod m),
+ *     m = min(8, d/8) (so staged rows read conflict-free from shared memory).
  *   CODEBOOK2: Kc uint32[32][d/16] centroid indices token-major; Vc uint32[d][2];
  *     Vm float2[d/32][32]; Kq fp16[32][ceil8(r)] PSAC coefficients.
  * Quantisation ([JB] step sizes; [WQ] INT2/INT4): per group m = min, M = max,

@@ -125,7 +125,7 @@ def value_dtype(io_dtype):
 
 
 def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN_OFF,
-                         psac_U=None, rows=None):
+                         psac_U=None, rows=None, operands="io"):
     """Reference attention for every (b, q-head).
 
     cache : oracle.layout.Cache (or codebook cache) holding the dequantised view.
@@ -134,6 +134,12 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
               values to value_dtype(io_dtype).
     psac_U: optional fp32 [B, Hkv, d, r]; adds tau (U^T q) . coeff for cached keys.
     rows  : optional index array of query rows to evaluate (all if None).
+    operands: 'io' -- dequantised cache keys rounded to io_dtype and values to
+              value_dtype(io_dtype) before the products (what a kernel that
+              builds 16-bit operand tiles consumes); 'f32' -- the dequantised
+              fp32 entries themselves (what a kernel consumes that folds the
+              step sizes and zero points into the query and the attention
+              weights instead of forming k_hat, v_hat).
     GQA: q-head h reads kv-head h // (Hq // Hkv).
     Returns (o [B, Hq, nrows, d], lse [B, Hq, nrows]) in fp64.
     """
@@ -151,8 +157,12 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
     for b in range(B):
         for hk in range(Hkv):
             lg = cache.logical(b, hk)
-            Kc = round_to(lg["khat"], io_dtype)
-            Vc = round_to(lg["vhat"], value_dtype(io_dtype))
+            if operands == "f32":
+                Kc = np.asarray(lg["khat"], np.float32)
+                Vc = np.asarray(lg["vhat"], np.float32)
+            else:
+                Kc = round_to(lg["khat"], io_dtype)
+                Vc = round_to(lg["vhat"], value_dtype(io_dtype))
             for hq in range(hk * grp, (hk + 1) * grp):
                 q = Q[b, hq, rows].astype(F64)
                 delta = None

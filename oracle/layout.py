@@ -17,7 +17,9 @@ head dim d:
                          Vc  uint32[d][b]         value codes, channel-major: token t of
                                                   channel c at word c*b + t/(32/b)
                          Vm  float2[d/32][32]     per-(32-channel group, token) (s, z)
-  RAW16:                 K   16-bit[32][d], then V 16-bit[32][d]  (fp16 or bf16)
+  RAW16:                 K   16-bit[32][d], then V 16-bit[32][d]  (fp16 or bf16),
+                         each row's 16-byte chunks permuted: chunk j of token t's
+                         row is stored at chunk position j XOR (t mod m), m = min(8, d/8)
   CODEBOOK2:             Kc  uint32[32][d/16]     2-bit centroid indices, token-major
                          Vc  uint32[d][2]         INT2 value codes, channel-major
                          Vm  float2[d/32][32]
@@ -108,14 +110,42 @@ def encode_int_blocks(Kb, Vb, bits, nvalid):
                 khat=khat, vhat=vhat)
 
 
+def raw16_chunk_order(d):
+    """Stored position of each 16-byte chunk of token t's row: ``order[t, j]`` for chunk j.
+
+    The permutation is this library's own format choice: chunk j of row t goes
+    to position j XOR (t mod m), m = min(8, d/8), so that eight consecutive rows
+    of one chunk column fall into distinct shared-memory banks when a block is
+    staged byte for byte.
+    """
+    nch = d // 8
+    m = min(8, nch)
+    t = np.arange(BLOCK)[:, None]
+    j = np.arange(nch)[None, :]
+    return j ^ (t % m)
+
+
+def _swizzle_rows(rows16, d):
+    """rows16: uint8 [N, 32, 2d] natural row bytes -> chunk-permuted rows."""
+    N = rows16.shape[0]
+    ch = rows16.reshape(N, BLOCK, d // 8, 16)
+    out = np.empty_like(ch)
+    order = raw16_chunk_order(d)
+    for t in range(BLOCK):
+        out[:, t, order[t]] = ch[:, t]
+    return out.reshape(N, -1)
+
+
 def encode_raw_blocks(Kb, Vb, nvalid, dtype):
-    """RAW16 blocks: the 16-bit inputs unchanged, pad rows zero."""
+    """RAW16 blocks: the 16-bit inputs unchanged (chunk-permuted per row), pad rows zero."""
     Kb = np.array(Kb, F32)
     Vb = np.array(Vb, F32)
     Kb[:, nvalid:] = 0
     Vb[:, nvalid:] = 0
-    N = Kb.shape[0]
-    raw = np.concatenate([_bits16(Kb, dtype).reshape(N, -1), _bits16(Vb, dtype).reshape(N, -1)], axis=1)
+    N, _, d = Kb.shape
+    kr = _bits16(Kb, dtype).reshape(N, BLOCK, 2 * d)
+    vr = _bits16(Vb, dtype).reshape(N, BLOCK, 2 * d)
+    raw = np.concatenate([_swizzle_rows(kr, d), _swizzle_rows(vr, d)], axis=1)
     return dict(bytes=raw, khat=Kb, vhat=Vb)
 
 

@@ -1,0 +1,116 @@
+"""GPU parity of the split-K decode kernel (one query per sequence) against the oracle.
+
+The decode kernel never forms dequantised 16-bit key or value tiles: it folds the
+step sizes and zero points into the query and the attention weights, so it
+consumes the dequantised entries at fp32 and the oracle is run with
+operands='f32'.
+"""
+
+import numpy as np
+import pytest
+
+from bit_kv_cache_28_b300 import bitkv as B
+from bit_kv_cache_28_b300 import synth
+from oracle import layout as OL, window as OW
+from oracle import attention as OA
+from helpers import gpu_mixed, gpu_uniform, run_attention, out_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def check(out, lse, ref_o, ref_lse, dtype, out_f32):
+    err = np.abs(out - ref_o)
+    tol = out_tol(dtype, out_f32, ref_o)
+    worst = np.unravel_index(np.argmax(err - tol), err.shape)
+    assert (err <= tol).all(), f"max err {err.max():.3e} at {worst} (tol {tol[worst]:.3e})"
+    fin = np.isfinite(ref_lse)
+    assert (np.isfinite(lse) == fin).all()
+    assert np.abs(lse[fin] - ref_lse[fin]).max(initial=0.0) < 2e-3
+
+
+def mixed_case(case, frac16=0.2, frac4=0.3):
+    bits = np.stack([OW.window_plan(case["sim"][b], frac16, frac4)[0] for b in range(case["B"])])
+    caps = [int((bits[0] == k).sum()) for k in (16, 4, 2)]
+    tc = gpu_mixed(case, bits, caps)
+    oc = OL.build_mixed(case["K_cache"], case["V_cache"], bits, caps, case["dtype"])
+    return tc, oc
+
+
+def test_decode_workload_full():
+    """Batch 8, 28 query heads over 4 kv heads, d 64, 19600 cached tokens in 613 windows
+    (FP16 / INT4 / INT2 by similarity), fp16: every output row against the oracle."""
+    case = synth.decode_case()
+    tc, oc = mixed_case(case)
+    path, splits = B.kv_attention_plan(tc.c, B.KV_F16, 1, 1, 28)
+    assert path == B.KV_PATH_DECODE and splits > 1
+    for jensen in (0, 1):
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=jensen, operands="f32")
+        o, l = run_attention(tc, case, jensen=jensen, out_f32=True)
+        check(o, l, ro, rl, "f16", True)
+        o16, l16 = run_attention(tc, case, jensen=jensen, out_f32=False)
+        check(o16, l16, ro, rl, "f16", False)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("n_cur", [0, 1, 5])
+def test_decode_mixed_ragged(dtype, n_cur):
+    """1000 cached tokens (last window 8 tokens), GQA 3:1, explicit split counts."""
+    case = synth.decode_case(seed=81, B=3, Hq=6, Hkv=2, d=64, n_cache=1000, dtype=dtype)
+    if n_cur != 1:
+        rng = np.random.default_rng(n_cur)
+        case["K_cur"] = synth.to_dtype_values(rng.standard_normal((3, 2, n_cur, 64)), dtype)
+        case["V_cur"] = synth.to_dtype_values(rng.standard_normal((3, 2, n_cur, 64)), dtype)
+    tc, oc = mixed_case(case)
+    for jensen in (0, 1, 2):
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], dtype, jensen=jensen, operands="f32")
+        for splits in (1, 3, 7):
+            o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
+            check(o, l, ro, rl, dtype, True)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 3, 3), (64, 32, 2), (128, 16, 1)])
+def test_decode_uniform(bits, d, Hq, Hkv):
+    """Uniform INT2 / INT4 chunk caches (ragged chunk ends), bf16, including 16 heads per kv head."""
+    case = synth.chunk_case(82, B=2, Hkv=Hkv, Hq=Hq, d=d, chunks=[300, 77, 5], n_cur=1, n_q=1, dtype="bf16")
+    tc = gpu_uniform(case, bits)
+    oc = OL.build_uniform(case["K_cache"], case["V_cache"], bits, case["chunks"],
+                          sum((n + 31) // 32 for n in case["chunks"]))
+    for jensen in (0, 1):
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen, operands="f32")
+        for splits in (0, 2):
+            o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
+            check(o, l, ro, rl, "bf16", True)
+        o, l = run_attention(tc, case, jensen=jensen, out_f32=False, path=B.KV_PATH_DECODE)
+        check(o, l, ro, rl, "bf16", False)
+
+
+def test_decode_mixed_d128_f16():
+    case = synth.decode_case(seed=83, B=2, Hq=8, Hkv=2, d=128, n_cache=700)
+    tc, oc = mixed_case(case)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=1, operands="f32")
+    o, l = run_attention(tc, case, jensen=1, out_f32=True)
+    check(o, l, ro, rl, "f16", True)
+
+
+def test_decode_empty_cache_and_single_block():
+    case = synth.decode_case(seed=84, B=1, Hq=4, Hkv=1, d=64, n_cache=20)
+    empty = B.TorchCache(1, 1, 64, B.KV_MIXED, (1, 1, 1), raw_dtype=B.KV_F16)
+    oc0 = OL.build_mixed(case["K_cache"][:, :, :0], case["V_cache"][:, :, :0], np.zeros((1, 0), int),
+                         [1, 1, 1], "f16")
+    ro, rl = OA.attention_over_cache(oc0, case["Q"], case["K_cur"], case["V_cur"], "f16", operands="f32")
+    o, l = run_attention(empty, case, out_f32=True, path=B.KV_PATH_DECODE)
+    check(o, l, ro, rl, "f16", True)
+    tc, oc = mixed_case(case)          # one window of 20 tokens, FP16 (window 0)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", operands="f32")
+    o, l = run_attention(tc, case, out_f32=True, path=B.KV_PATH_DECODE, splits=4)
+    check(o, l, ro, rl, "f16", True)
+
+
+def test_decode_matches_simt_path():
+    """Same cache through the decode kernel and the CUDA-core kernel."""
+    case = synth.decode_case(seed=85, B=2, Hq=14, Hkv=2, d=64, n_cache=3000)
+    tc, _ = mixed_case(case, 0.1, 0.4)
+    o_d, l_d = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_DECODE)
+    o_s, l_s = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_SIMT)
+    assert np.abs(o_d - o_s).max() < 2e-3 and np.abs(l_d - l_s).max() < 2e-3

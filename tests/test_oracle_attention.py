@@ -218,3 +218,20 @@ def test_jensen_applies_only_to_quantised_keys():
     a0, _ = A.attention_over_cache(cache_raw, Q, c["K_cur"], c["V_cur"], "f16", jensen=0)
     a1, _ = A.attention_over_cache(cache_raw, Q, c["K_cur"], c["V_cur"], "f16", jensen=1)
     assert np.abs(a0 - a1).max() == 0
+
+
+def test_operand_precision_option():
+    """operands='f32' feeds the dequantised fp32 entries; 'io' rounds them first.  For fp32 I/O
+    the two coincide; for bf16 I/O they differ by less than the bf16 rounding of the keys allows."""
+    c = synth.chunk_case(9, Hkv=1, d=64, chunks=[64], n_cur=8, n_q=4, dtype="bf16")
+    cache = layout.build_uniform(c["K_cache"], c["V_cache"], 2, [64], 2)
+    a = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "f32")
+    b = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "f32", operands="f32")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    io = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16")
+    ex = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16", operands="f32")
+    assert not np.array_equal(io[0], ex[0])
+    kh = cache.logical(0, 0)["khat"]
+    tau = 1 / 8
+    bound = tau * np.abs(c["Q"][0, 0]).astype(np.float64) @ np.abs(kh).T.astype(np.float64) * 2.0 ** -8
+    assert np.abs(io[1] - ex[1]).max() <= bound.max()

@@ -80,6 +80,31 @@ def test_uniform_builder_chunk_alignment_and_bytes():
     assert lg["khat"].shape == (90, 64)
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_raw16_chunk_permutation(d):
+    """RAW16 rows: element (t, c) sits at 16-bit slot t*d + 8*((c//8) ^ (t % m)) + c % 8, m = min(8, d/8),
+    written out element by element from the format definition."""
+    rng = np.random.default_rng(5)
+    K = synth.to_dtype_values(rng.standard_normal((1, 32, d)), "f16")
+    V = synth.to_dtype_values(rng.standard_normal((1, 32, d)), "f16")
+    enc = layout.encode_raw_blocks(K, V, 30, "f16")
+    words = enc["bytes"][0].view(np.float16)
+    m = min(8, d // 8)
+    for part, X in ((0, K[0]), (1, V[0])):
+        for t in range(32):
+            for c in range(d):
+                slot = part * 32 * d + t * d + 8 * ((c // 8) ^ (t % m)) + c % 8
+                want = X[t, c] if t < 30 else 0.0
+                assert float(words[slot]) == want
+    # for d >= 64, eight consecutive rows of one chunk column land in eight distinct
+    # 16-byte bank groups of a 128-byte bank line
+    if d >= 64:
+        order = layout.raw16_chunk_order(d)
+        for j in range(d // 8):
+            banks = {((t * 2 * d + 16 * order[t, j]) % 128) // 16 for t in range(8)}
+            assert len(banks) == 8
+
+
 def test_bytes_of_workloads():
     """Algorithmic cache bytes (codes of valid tokens + all metadata) of the chunk workload."""
     H, d, n = 24, 128, 4680
