@@ -1,14 +1,22 @@
 """Benchmark of the quantised-KV attention hot path (one JSON line on rank 0).
 
-A step is one pass of the hot path over one chunk of the workload: attention
-of the current chunk's queries over the packed cache plus the chunk itself
-(Jensen correction on), then quantise-and-append of the finished chunk.  The
-cache is rewound on the host after each step so every step sees the same
-cache.  Inputs are seeded synthetic tensors (no dataset exists for this
-workload; shapes follow the chunk-wise video-diffusion setting).
+Workloads (seeded synthetic inputs; no dataset exists for this path, shapes
+follow the chunk-wise video-diffusion and video-VLM settings of the pages):
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|tiny|codebook]
-    python bench.py --impl reference ...   # the CPU oracle timed on the host cores
+* ``chunk`` (default): 24 heads, d 128, bf16; the 1560 queries of the current
+  chunk attend to a cache of 3 INT2 chunks (4680 tokens) plus the chunk itself
+  with the Jensen correction on, then the finished chunk is quantised and
+  appended.  One step = attention + append; the cache is rewound on the host
+  after each step so every step sees the same cache.
+* ``rollout``: the same with 40 heads and 21 cached chunks (32760 tokens).
+* ``decode``: batch 8, 28 query heads over 4 kv heads, d 64, fp16; one query per
+  sequence attends to 19600 cached tokens in 613 windows of FP16 / INT4 / INT2
+  (planned by kv_window_plan from a seeded similarity) plus its own token.
+  One step = one split-K decode attention.
+* ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|tiny]
+    python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 N > 1 runs independent replicas (weak scaling): every rank owns its own
 workload; no data moves between ranks, the process group only carries the
@@ -22,6 +30,7 @@ import json
 import os
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -36,7 +45,7 @@ L2_FLUSH_BYTES = 512 << 20
 # ------------------------------------------------------------ workloads ----
 
 def workload_spec(name):
-    """Shapes, algorithmic bytes/FLOPs of one step."""
+    """Shapes and algorithmic bytes / FLOPs of one step."""
     if name in ("chunk", "rollout"):
         H = 24 if name == "chunk" else 40
         n_chunks = 3 if name == "chunk" else 21
@@ -47,15 +56,23 @@ def workload_spec(name):
         flops = 4.0 * n * (n_cache + n) * d * H
         append_read = 2 * H * n * d * 2
         append_write = H * ((n + 31) // 32) * 4096
-        return dict(name=name, B=1, Hkv=H, Hq=H, d=d, n_q=n, n_cur=n, chunks=[n] * n_chunks, dtype="bf16",
-                    cache_bytes=cache_bytes, attn_flops=flops, append_bytes=append_read + append_write,
-                    jensen=1, seed=2 if name == "chunk" else 3)
+        return dict(name=name, kind="chunk", B=1, Hkv=H, Hq=H, d=d, n_q=n, n_cur=n, chunks=[n] * n_chunks,
+                    dtype="bf16", cache_bytes=cache_bytes, attn_flops=flops, append_bytes=append_read + append_write,
+                    jensen=1, seed=2 if name == "chunk" else 3,
+                    label=f"{name}: B1 H{H} d{d} chunk {n} cache {n_cache} INT2, Jensen taylor2")
     if name == "tiny":
         d, n_cache, n = 64, 1024, 64
         cache_bytes = n_cache * d * 2 * 2 / 8 + (n_cache // 32) * d * 8 + n_cache * (d // 32) * 8
-        return dict(name=name, B=1, Hkv=1, Hq=1, d=d, n_q=n, n_cur=n, chunks=[1024], dtype="f32",
+        return dict(name=name, kind="chunk", B=1, Hkv=1, Hq=1, d=d, n_q=n, n_cur=n, chunks=[1024], dtype="f32",
                     cache_bytes=cache_bytes, attn_flops=4.0 * n * (n_cache + n) * d,
-                    append_bytes=2 * n * d * 4 + 2 * 2048, jensen=1, seed=1)
+                    append_bytes=2 * n * d * 4 + 2 * 2048, jensen=1, seed=1,
+                    label="tiny: B1 H1 d64 chunk 64 cache 1024 INT2 fp32, Jensen taylor2")
+    if name == "decode":
+        B, Hq, Hkv, d, n_cache = 8, 28, 4, 64, 19600
+        return dict(name=name, kind="decode", B=B, Hkv=Hkv, Hq=Hq, d=d, n_q=1, n_cur=1, n_cache=n_cache,
+                    dtype="f16", jensen=0, seed=4, attn_flops=4.0 * B * Hq * (n_cache + 1) * d,
+                    label=f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} 1 query, cache {n_cache} tokens in 32-token "
+                          "windows FP16/INT4/INT2 20/30/50%, split-K")
     raise ValueError(f"unknown workload {name}")
 
 
@@ -63,34 +80,114 @@ def make_inputs(spec):
     from bit_kv_cache_28_b300 import synth
     if spec["name"] == "tiny":
         return synth.tiny(spec["seed"])
+    if spec["kind"] == "decode":
+        return synth.decode_case(spec["seed"])
     return synth.chunk_case(spec["seed"], Hkv=spec["Hkv"], chunks=spec["chunks"], n_cur=spec["n_cur"])
 
 
 # --------------------------------------------------------------- clocks ----
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM clock, maximum
+    SM clock and the active clock-event reasons."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes as C
+        self.C = C
+        self.lib = C.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+
+    def handle(self, dev_index):
+        C = self.C
+        h = C.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.lib.nvmlDeviceGetHandleByUUID(C.c_char_p(uuid.encode()), C.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(C.c_uint(dev_index), C.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def clock(self, h, maximum=False):
+        v = self.C.c_uint()
+        f = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if f(h, self.C.c_int(self.NVML_CLOCK_SM), self.C.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return float(v.value)
+
+    def reasons(self, h):
+        v = self.C.c_ulonglong()
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if f(h, self.C.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clock and throttle reasons of this process's GPU, sampled through NVML every 2 ms on
+    a background thread from before the warm-up to the end of the timed steps (nvidia-smi
+    every 200 ms if NVML cannot be loaded)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, dev_index):
+        self.dev_index = dev_index
+        self.rows = []
+        self.nvml = None
+        self.stop = threading.Event()
+        self.thread = None
         self.proc = None
-        self.path = os.path.join("/tmp", f"bitkv_clocks_{os.getpid()}.csv")
+        self.error = None
+
+    def _loop(self, h):
+        try:
+            mx = self.nvml.clock(h, maximum=True)
+        except Exception as e:  # pragma: no cover - depends on the driver
+            mx, self.error = float("nan"), repr(e)
+        while not self.stop.is_set():
+            try:
+                sm = self.nvml.clock(h)
+                try:
+                    rs = self.nvml.reasons(h)
+                except Exception as e:
+                    rs, self.error = 0, repr(e)
+                self.rows.append((sm, mx, rs))
+            except Exception as e:
+                self.error = repr(e)
+            self.stop.wait(0.002)
 
     def __enter__(self):
         try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            self.nvml = _Nvml()
+            h = self.nvml.handle(self.dev_index)
+            self.thread = threading.Thread(target=self._loop, args=(h,), daemon=True)
+            self.thread.start()
+        except Exception as e:
+            self.error = repr(e)
+            self.nvml = None
+            self.path = os.path.join("/tmp", f"bitkv_clocks_{os.getpid()}.csv")
+            try:
+                self.fh = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.dev_index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=self.fh, stderr=subprocess.DEVNULL)
+            except (OSError, FileNotFoundError):
+                self.proc = None
         return self
 
     def __exit__(self, *a):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -98,32 +195,28 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            for line in open(self.path):
+                p = [x.strip() for x in line.split(",")]
+                try:
+                    self.rows.append((float(p[0]), float(p[1]), int(p[2], 16)))
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
-                continue
-            try:
-                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
-            except ValueError:
-                continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [r[0] for r in rows]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[2 + i].lower().startswith("active")})
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "error": self.error}
+        sm = [r[0] for r in self.rows]
+        reasons = sorted({name for r in self.rows for bit, name in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in self.rows), "reasons": reasons,
+                "samples": len(self.rows), "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 # ----------------------------------------------------------- own arm -------
 
-class Runner:
-    """Device state of one replica: the cache after the workload's cached chunks, the step inputs."""
+class ChunkRunner:
+    """Device state of one replica of a chunk workload: the cache after the
+    workload's cached chunks, and the step inputs."""
 
     def __init__(self, spec, inputs, dev):
         import torch
@@ -131,7 +224,6 @@ class Runner:
         self.B, self.spec, self.dev = B, spec, dev
         tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[spec["dtype"]]
         self.dt = {"bf16": B.KV_BF16, "f16": B.KV_F16, "f32": B.KV_F32}[spec["dtype"]]
-        self.tdt = tdt
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(tdt)
         nb_cache = sum((n + 31) // 32 for n in spec["chunks"])
         nb_cur = (spec["n_cur"] + 31) // 32
@@ -143,7 +235,8 @@ class Runner:
                                  self.dt, n, self.tc.c)
             t0 += n
         self.saved = (list(self.tc.c.n_blocks), self.tc.c.n_tokens)
-        self.Q, self.Kc, self.Vc = to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])
+        self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
+        self.Q, self.Kc, self.Vc = self.inputs
         self.opts = B.kv_attn_opts(0.0, spec["jensen"], 0, 0, 0, B.KV_PATH_AUTO)
         self.out = torch.empty_like(self.Q)
         self.lse = torch.empty(self.Q.shape[:3], dtype=torch.float32, device=dev)
@@ -154,6 +247,7 @@ class Runner:
                                                      self.opts)
         # attention kernel (+ one merge launch when the key range is split) + one append launch
         self.launches_per_step = 2 + (1 if self.splits > 1 else 0)
+        self.cache_bytes = spec["cache_bytes"]
 
     def rewind(self):
         n_blocks, n_tok = self.saved
@@ -172,6 +266,54 @@ class Runner:
         self.rewind()
 
 
+class DecodeRunner:
+    """Device state of one replica of the decode workload: the mixed cache of one prefill
+    (window bit-widths from kv_window_plan) and the step's query and current token."""
+
+    def __init__(self, spec, inputs, dev):
+        import torch
+        from bit_kv_cache_28_b300 import bitkv as B
+        self.B, self.spec, self.dev = B, spec, dev
+        self.dt = B.KV_F16
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.float16)
+        Bn, n, d, Hkv = spec["B"], spec["n_cache"], spec["d"], spec["Hkv"]
+        W = (n + 31) // 32
+        bits = np.zeros((Bn, W), np.int8)
+        th = B.kv_thresholds(0.2, 0.3, 1)
+        for b in range(Bn):
+            B.kv_window_plan(np.ascontiguousarray(inputs["sim"][b], np.float32), W, th, bits[b])
+        caps = [int((bits[0] == k).sum()) for k in (16, 4, 2)]
+        self.tc = B.TorchCache(Bn, Hkv, d, B.KV_MIXED, caps, raw_dtype=B.KV_F16, device=dev)
+        bits_dev = torch.from_numpy(bits).to(dev)
+        B.kv_quantize_append(to(inputs["K_cache"]), to(inputs["V_cache"]), self.dt, n, self.tc.c,
+                             B.kv_append_opts(bits.ctypes.data, bits_dev.data_ptr()))
+        torch.cuda.synchronize(dev)
+        # algorithmic cache bytes: codes of valid tokens + all metadata; 16-bit windows' valid rows
+        bl = self.tc.blk_len.cpu().numpy().reshape(Bn, -1)
+        nb = list(self.tc.c.n_blocks)
+        lens = [bl[:, :nb[0]], bl[:, nb[0]:nb[0] + nb[1]], bl[:, nb[0] + nb[1]:nb[0] + nb[1] + nb[2]]]
+        per_b = (lens[0].sum(1) * 2 * d * 2 + lens[1].sum(1) * 2 * d * 4 / 8 + nb[1] * 16 * d
+                 + lens[2].sum(1) * 2 * d * 2 / 8 + nb[2] * 16 * d)
+        self.cache_bytes = float(per_b.sum() * Hkv)
+        self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
+        self.Q, self.Kc, self.Vc = self.inputs
+        self.opts = B.kv_attn_opts(0.0, spec["jensen"], 0, 0, 0, B.KV_PATH_AUTO)
+        self.out = torch.empty_like(self.Q)
+        self.lse = torch.empty(self.Q.shape[:3], dtype=torch.float32, device=dev)
+        self.ws_bytes = B.kv_attention_workspace(self.tc.c, self.dt, 1, 1, spec["Hq"], self.opts)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        self.path, self.splits = B.kv_attention_plan(self.tc.c, self.dt, 1, 1, spec["Hq"], self.opts)
+        self.launches_per_step = 1   # the decode kernel merges its splits itself
+
+    def attention(self, stream):
+        s = self.spec
+        self.B.kv_attention(self.Q, self.Kc, self.Vc, self.dt, 1, 1, s["Hq"], self.tc.c, self.opts, self.out,
+                            self.lse, self.ws, self.ws_bytes, stream)
+
+    def append(self, stream):
+        pass
+
+
 def run_own(args, rank, world, dist):
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -179,19 +321,19 @@ def run_own(args, rank, world, dist):
     torch.cuda.set_device(dev)
     spec = workload_spec(args.workload)
     inputs = make_inputs(spec)
-    r = Runner(spec, inputs, dev)
+    r = (DecodeRunner if spec["kind"] == "decode" else ChunkRunner)(spec, inputs, dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    for _ in range(args.warmup):
-        r.attention(sh)
-        r.append(sh)
-    torch.cuda.synchronize(dev)
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     with sampler:
+        for _ in range(args.warmup):
+            r.attention(sh)
+            r.append(sh)
+        torch.cuda.synchronize(dev)
+
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         if dist:
             dist.barrier()
         torch.cuda.synchronize(dev)
@@ -210,10 +352,9 @@ def run_own(args, rank, world, dist):
     t_app = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps * 1e-3
 
     # end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of the output
-    pin = lambda t: t.cpu().pin_memory()
-    hQ, hK, hV = pin(r.Q), pin(r.Kc), pin(r.Vc)
+    hin = [t.cpu().pin_memory() for t in r.inputs]
     hO = torch.empty_like(r.out, device="cpu").pin_memory()
-    h2d = (hQ.numel() + hK.numel() + hV.numel()) * hQ.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = hO.numel() * hO.element_size()
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
@@ -222,9 +363,8 @@ def run_own(args, rank, world, dist):
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
         e_ev[k][0].record(stream)
-        r.Q.copy_(hQ, non_blocking=True)
-        r.Kc.copy_(hK, non_blocking=True)
-        r.Vc.copy_(hV, non_blocking=True)
+        for dst, src in zip(r.inputs, hin):
+            dst.copy_(src, non_blocking=True)
         r.attention(sh)
         r.append(sh)
         hO.copy_(r.out, non_blocking=True)
@@ -242,33 +382,38 @@ def run_own(args, rank, world, dist):
     if rank != 0:
         return
     rows = spec["B"] * spec["Hq"] * spec["n_q"]
-    value = world * rows / t_step
     peaks = load_peaks()
-    flops = spec["attn_flops"]
-    tc_peak, peak_src = peaks["bf16_tflops"], peaks["source"]
-    achieved = flops / t_attn / 1e12
+    kernel = {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_decode_kernel"}.get(r.path)
+    cache_gbs = r.cache_bytes / t_attn / 1e9
+    if spec["kind"] == "decode":
+        roof = {"bound": "hbm", "achieved": cache_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": cache_gbs / peaks["hbm_gbs"]}
+    else:
+        achieved = spec["attn_flops"] / t_attn / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    roof.update({"traffic": traffic_for(kernel, spec["name"]), "kernel": kernel, "splits": r.splits,
+                 "peak_source": peaks["source"],
+                 "algorithmic": ("cache bytes (codes of valid tokens + all metadata) per launch"
+                                 if spec["kind"] == "decode" else "4 n_q (n_cache + n_cur) d FLOPs per head"),
+                 "roofline_time_frac_of_step": max(r.cache_bytes / (peaks["hbm_gbs"] * 1e9),
+                                                   spec["attn_flops"] / (peaks["bf16_tflops"] * 1e12)) / t_step})
     line = {
-        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic (seeded, PCG64)",
-        "config": {"workload": f"{spec['name']}: B{spec['B']} H{spec['Hq']} d{spec['d']} chunk {spec['n_cur']} "
-                               f"cache {sum(spec['chunks'])} INT2, Jensen taylor2",
-                   "query_tokens": "B*Hq*n_q per step (one row per head)", "l2": "flushed between steps (512 MiB write)",
-                   "parallelism": f"replicas x{world}"},
-        "cache_gbs": world * spec["cache_bytes"] / t_attn / 1e9,
+        "metric": METRIC, "value": world * rows / t_step, "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic (seeded, PCG64)",
+        "config": {"workload": spec["label"], "query_tokens": "B*Hq*n_q per step (one row per query head)",
+                   "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+        "cache_gbs": world * cache_gbs,
         "attn_ms": t_attn * 1e3, "append_ms": t_app * 1e3,
-        "append_gbs": spec["append_bytes"] / t_app / 1e9,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tc_peak, "traffic": traffic_for("attn", spec["name"]),
-                     "kernel": {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_decode_kernel"}.get(r.path),
-                     "splits": r.splits, "peak_source": peak_src,
-                     "roofline_frac_of_step": (max(spec["cache_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                                                   flops / (tc_peak * 1e12)) / t_step)},
+        "roofline": roof,
         "e2e": {"value": world * rows / t_e2e, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": r.launches_per_step * args.steps,
         "clocks": sampler.summary(),
     }
+    if spec["kind"] == "chunk":
+        line["append_gbs"] = spec["append_bytes"] / t_app / 1e9
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, inputs)
     print(json.dumps(line), flush=True)
@@ -284,9 +429,9 @@ def load_peaks():
 
 
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if one matches the current kernel source."""
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kernel is None:
         return None
     d = json.load(open(p)).get(f"{kernel}:{workload}")
     if not d:
@@ -301,8 +446,22 @@ def traffic_for(kernel, workload):
 # ------------------------------------------------------- oracle arms -------
 
 def oracle_sample_step(spec, inputs, heads):
-    """One bounded sample of the step on the CPU oracle: `heads` heads of append + attention."""
-    from oracle import layout as OL, attention as OA
+    """One bounded sample of the step on the CPU oracle; returns the query rows it covered.
+
+    chunk workloads: `heads` heads of cache build + attention + append.
+    decode: `heads` kv heads of sequence 0 (cache build + attention of their query heads).
+    """
+    from oracle import layout as OL, attention as OA, window as OW
+    if spec["kind"] == "decode":
+        sl = slice(0, heads)
+        b = slice(0, 1)
+        bits, _ = OW.window_plan(inputs["sim"][0], 0.2, 0.3)
+        caps = [int((bits == k).sum()) for k in (16, 4, 2)]
+        oc = OL.build_mixed(inputs["K_cache"][b, sl], inputs["V_cache"][b, sl], bits[None], caps, "f16")
+        g = spec["Hq"] // spec["Hkv"]
+        OA.attention_over_cache(oc, inputs["Q"][b, :heads * g], inputs["K_cur"][b, sl], inputs["V_cur"][b, sl],
+                                "f16", operands="f32")
+        return heads * g
     sl = slice(0, heads)
     oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
                           sum((n + 31) // 32 for n in spec["chunks"]))
@@ -321,8 +480,16 @@ def oracle_threads():
         return os.cpu_count() or 1
 
 
+def sample_text(spec, heads):
+    if spec["kind"] == "decode":
+        return (f"{heads} kv head of sequence 0 ({heads * spec['Hq'] // spec['Hkv']} query heads): mixed cache "
+                f"build of {spec['n_cache']} tokens + decode attention, fp64 numpy")
+    return (f"{heads} head of {spec['Hq']}: cache build + attention of {spec['n_q']} queries + append, "
+            f"fp64 numpy")
+
+
 def cpu_baseline(spec, inputs):
-    heads = 1 if spec["Hq"] <= 24 else 1
+    heads = 1
     t = time.perf_counter()
     rows = 0
     n = 0
@@ -333,8 +500,7 @@ def cpu_baseline(spec, inputs):
             break
     dt = time.perf_counter() - t
     return {"value": rows / dt, "unit": "query-tokens/s", "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"{n} x ({heads} head of {spec['Hq']}: cache build + attention of {spec['n_q']} queries + "
-                      f"append), fp64 numpy"}
+            "sample": f"{n} x ({sample_text(spec, heads)})"}
 
 
 def run_reference(args, rank, world):
@@ -351,15 +517,13 @@ def run_reference(args, rank, world):
         rows += oracle_sample_step(spec, inputs, heads)
     dt = time.perf_counter() - t
     value = rows / dt
-    sample = f"per step: {heads} head of {spec['Hq']} (cache build + attention of {spec['n_q']} queries + append)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, PCG64)",
-            "config": {"workload": f"{spec['name']}: B{spec['B']} H{spec['Hq']} d{spec['d']} chunk {spec['n_cur']} "
-                                   f"cache {sum(spec['chunks'])} INT2, Jensen taylor2", "parallelism": "host cores"},
+            "config": {"workload": spec["label"], "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": oracle_threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": f"per step: {sample_text(spec, heads)}"},
             "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -184,10 +184,9 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 // ---- one quantised block ------------------------------------------------------
 // q[r][4 kk + e]: query of row r at channels 16 kk + 2 tig + {0, 1, 8, 9}.
-template <int D, int BITS, bool TWO>
+template <int D, int BITS, bool TWO, int JENSEN>
 __device__ __forceinline__ void int_block(const unsigned char* blk, int len, const LaneConst& lc,
-                                          const float (&q)[2][D / 4], float c1, float tau, int jensen,
-                                          DecState<D>& st) {
+                                          const float (&q)[2][D / 4], float c1, float tau, DecState<D>& st) {
     const IntBlockOffsets o = int_offsets(D, BITS);
     // A = q o s as an fp16 pair hi + lo (hi = fp16(q s), lo = fp16(q s - hi): the
     // product keeps ~22 bits, enough for outlier channels with large steps), the
@@ -211,8 +210,8 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
             for (int e = 0; e < 4; ++e) {
                 qs[e] = q[r][4 * kk + e] * s[e];
                 qz[r] = fmaf(q[r][4 * kk + e], z[e], qz[r]);
-                if (jensen == KV_JENSEN_TAYLOR2) jd[r] = fmaf(qs[e], qs[e], jd[r]);
-                else if (jensen == KV_JENSEN_EXACT) jd[r] += log_sinhc(0.5f * tau * qs[e]);
+                if (JENSEN == KV_JENSEN_TAYLOR2) jd[r] = fmaf(qs[e], qs[e], jd[r]);
+                else if (JENSEN == KV_JENSEN_EXACT) jd[r] += log_sinhc(0.5f * tau * qs[e]);
             }
             aqk[kk][r] = pack_f16(qs[0], qs[1]);
             aqk[kk][2 + r] = pack_f16(qs[2], qs[3]);
@@ -227,9 +226,9 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
     for (int r = 0; r < 2; ++r) {
         const float z = quad_sum(qz[r]);
         float dl = 0.0f;
-        if (jensen != KV_JENSEN_OFF) {
+        if (JENSEN != KV_JENSEN_OFF) {
             dl = quad_sum(jd[r]);
-            if (jensen == KV_JENSEN_TAYLOR2) dl *= tau * tau * (1.0f / 24.0f);
+            if (JENSEN == KV_JENSEN_TAYLOR2) dl *= tau * tau * (1.0f / 24.0f);
         }
         bias[r] = (tau * z - dl) * kLog2e;
     }
@@ -438,10 +437,10 @@ struct DecShape {
     int rows;         // merge rows per warp (8 or 16)
 };
 
-template <typename T, int D, bool TWO>
-__global__ void __launch_bounds__(kDThreads)
+template <typename T, int D, bool TWO, int JENSEN>
+__global__ void __launch_bounds__(kDThreads, D == 64 ? 3 : 1)
 attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* __restrict__ Vcur, int n_cur, int Hq,
-                   DevCache c, float tau, int jensen, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
+                   DevCache c, float tau, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
                    float* __restrict__ lse, float* __restrict__ part, int* __restrict__ tickets, int* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
@@ -515,17 +514,27 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     if (lane == 0)
         for (int k = 0; k < nw && k < nsw; ++k) issue(k);
     __syncwarp();
-    int k = 0;
+    int k = 0, len_next = 0;
     for (; k < nw; ++k) {
+        if ((k & 31) == 0) {
+            // valid lengths of the next 32 blocks, one per lane, fetched before the wait
+            const int kl = k + lane;
+            len_next = 0;
+            if (kl < nw) {
+                int sg, ix;
+                locate(lo + warp + kDW * kl, sg, ix);
+                len_next = c.blk_len[(long long)b * c.cap_total + c.seg_base[sg] + ix];
+            }
+        }
         const bool ok = mbar_wait(bar(k % nsw), (k / nsw) & 1, &abort_flag, err, 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         int seg, idx;
         locate(lo + warp + kDW * k, seg, idx);
-        const int len = c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + idx];
+        const int len = __shfl_sync(0xffffffffu, len_next, k & 31);
         const unsigned char* blk = slots + (warp * nsw + k % nsw) * slot_bytes;
         const int cls = seg_class(c.kind, seg);
-        if (cls == CLS_INT2) int_block<D, 2, TWO>(blk, len, lc, q, c1, tau, jensen, st);
-        else if (cls == CLS_INT4) int_block<D, 4, TWO>(blk, len, lc, q, c1, tau, jensen, st);
+        if (cls == CLS_INT2) int_block<D, 2, TWO, JENSEN>(blk, len, lc, q, c1, tau, st);
+        else if (cls == CLS_INT4) int_block<D, 4, TWO, JENSEN>(blk, len, lc, q, c1, tau, st);
         else raw_block<T, D, TWO>(smem_u32(blk), len, lc, aq, c1, st);
         __syncwarp();
         if (lane == 0 && k + nsw < nw) issue(k + nsw);
@@ -662,7 +671,7 @@ DecShape dec_shape(const kv_cache* cache, int Hq) {
     if (slot == 0) slot = 16;
     DecShape sh;
     sh.slot_bytes = (int)((slot + 127) / 128 * 128);
-    int nsw = (int)(96 * 1024 / (kDW * (long long)sh.slot_bytes));
+    int nsw = (int)(64 * 1024 / (kDW * (long long)sh.slot_bytes));
     sh.nsw = nsw < 2 ? 2 : (nsw > 8 ? 8 : nsw);
     sh.rows = Hq / L.Hkv > 8 ? 16 : 8;
     return sh;
@@ -677,17 +686,16 @@ size_t dec_ticket_bytes(const kv_cache* cache) {
     return ((size_t)cache->layout.B * cache->layout.Hkv * sizeof(int) + 255) / 256 * 256;
 }
 
-template <typename T, int D, bool TWO>
+template <typename T, int D, bool TWO, int JENSEN>
 kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur, int Hq, const kv_cache* cache,
-                       float tau, int jensen, int n_splits, void* out, int out_f32, float* lse, void* ws,
-                       cudaStream_t st) {
+                       float tau, int n_splits, void* out, int out_f32, float* lse, void* ws, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     const DecShape sh = dec_shape(cache, Hq);
     const size_t smem = dec_smem_bytes(sh, D);
     static size_t attr_bytes = 0;
     if (smem > attr_bytes) {
         const cudaError_t e =
-            cudaFuncSetAttribute(attn_decode_kernel<T, D, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(attn_decode_kernel<T, D, TWO, JENSEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return set_error(KV_ERR_CUDA, "attn_decode_kernel: %zu bytes of shared memory: %s", smem,
                              cudaGetErrorString(e));
@@ -699,9 +707,9 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     float* part = reinterpret_cast<float*>(w + 256 + dec_ticket_bytes(cache));
     cudaMemsetAsync(w, 0, 256 + dec_ticket_bytes(cache), st);
     dim3 grid(n_splits, c.Hkv, c.B);
-    attn_decode_kernel<T, D, TWO><<<grid, kDThreads, smem, st>>>(
-        static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, jensen,
-        n_splits, sh, out, out_f32, lse, part, tickets, err);
+    attn_decode_kernel<T, D, TWO, JENSEN><<<grid, kDThreads, smem, st>>>(
+        static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
+        sh, out, out_f32, lse, part, tickets, err);
     kv_status s = check_launch("attn_decode_kernel");
     if (s != KV_OK) return s;
     if (getenv("BITKV_DEBUG_SYNC")) {
@@ -752,14 +760,25 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
                              float* lse, void* ws, cudaStream_t st) {
     const int d = cache->layout.d;
     const bool two = Hq / cache->layout.Hkv > 8;
-#define BITKV_DEC(T, D, TWO) \
-    return launch_dec_t<T, D, TWO>(Q, Kc, Vc, n_cur, Hq, cache, tau, jensen, n_splits, out, out_f32, lse, ws, st)
+    using F16 = __half;
+    using BF16 = __nv_bfloat16;
+#define BITKV_DEC(T, D, TWO)                                                                                    \
+    do {                                                                                                        \
+        if (jensen == KV_JENSEN_TAYLOR2)                                                                        \
+            return launch_dec_t<T, D, TWO, KV_JENSEN_TAYLOR2>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,  \
+                                                              out_f32, lse, ws, st);                            \
+        if (jensen == KV_JENSEN_EXACT)                                                                          \
+            return launch_dec_t<T, D, TWO, KV_JENSEN_EXACT>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
+                                                            out_f32, lse, ws, st);                              \
+        return launch_dec_t<T, D, TWO, KV_JENSEN_OFF>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out, out_f32, \
+                                                      lse, ws, st);                                             \
+    } while (0)
     if (dt == KV_F16) {
-        if (d == 64) { if (two) BITKV_DEC(__half, 64, true); else BITKV_DEC(__half, 64, false); }
-        else { if (two) BITKV_DEC(__half, 128, true); else BITKV_DEC(__half, 128, false); }
+        if (d == 64) { if (two) BITKV_DEC(F16, 64, true); else BITKV_DEC(F16, 64, false); }
+        else { if (two) BITKV_DEC(F16, 128, true); else BITKV_DEC(F16, 128, false); }
     } else {
-        if (d == 64) { if (two) BITKV_DEC(__nv_bfloat16, 64, true); else BITKV_DEC(__nv_bfloat16, 64, false); }
-        else { if (two) BITKV_DEC(__nv_bfloat16, 128, true); else BITKV_DEC(__nv_bfloat16, 128, false); }
+        if (d == 64) { if (two) BITKV_DEC(BF16, 64, true); else BITKV_DEC(BF16, 64, false); }
+        else { if (two) BITKV_DEC(BF16, 128, true); else BITKV_DEC(BF16, 128, false); }
     }
 #undef BITKV_DEC
 }
