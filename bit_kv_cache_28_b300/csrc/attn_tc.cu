@@ -9,20 +9,33 @@
 // the compression): packed blocks are expanded into shared-memory operand tiles.
 //
 // One CTA = 128 queries of one (batch, head) x a range of 128-key tiles.
-//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  Loads the S
-//              row from TMEM, applies scale, Jensen delta and the key mask,
-//              keeps a lazily rescaled running max (O is rescaled in TMEM only
-//              when the max grows by more than 2^8), writes P (fp16) to smem.
-//   warps 4-7  producers: thread 0 bulk-copies (TMA engine) each packed cache
-//              tile -- 4 contiguous blocks -- into a double-buffered staging
-//              area two tiles ahead; all 128 threads dequantise the staged
-//              tile into K_hat [128 keys x 128] (bf16, single buffer: free once
-//              Q K_hat^T of the tile completes) and V_hat^T [128 channels x 128
-//              keys] (fp16, double buffer), 128-byte-swizzled K-major; a
-//              current-chunk tile is read from global memory and transposed.
-//   warp 8     TMEM owner; lane 0 issues S = Q K_hat^T (bf16) and O += P V_hat (fp16).
-// TMEM: S double buffer (columns 0-255), O (256-383).  Every wait is bounded;
-// every warp-collective tcgen05 load/store runs with the whole warp converged.
+//   warps 0-3   softmax: thread i owns query row i = TMEM lane i.  Two passes
+//               over the S row in TMEM (row maximum per 32-key group, then
+//               p = 2^(S c1 - (m + delta_g))), a lazily rescaled running max (O is
+//               rescaled only when the max grows by more than 2^8), P written
+//               back to TMEM as fp16.
+//   warps 4-11  producers: thread 0 bulk-copies (TMA engine) each packed cache
+//               tile -- 4 contiguous blocks -- into a double-buffered staging
+//               area two tiles ahead; all 256 threads expand the staged codes
+//               into K_hat [128 keys x 128] (bf16, single buffer: free once
+//               Q K_hat^T of the tile completes) and V_hat^T [128 channels x 128
+//               keys] (fp16, double buffer), 128-byte-swizzled K-major, plus the
+//               Jensen weights W [4 groups, hi/lo] of the tile; a current-chunk
+//               tile is read from global memory (values transposed).
+//   warp 12     TMEM owner; lane 0 issues S = Q K_hat^T (bf16, Q read from
+//               tensor memory), the Jensen term Delta = (q^2) W^T (bf16, N = 16;
+//               q^2 of a bf16 q is split exactly into bf16 high and low parts,
+//               two MMAs; W columns g and 4 + g hold the high and low bf16 parts
+//               of group g's weights), and O += P V_hat with P read from tensor
+//               memory (fp16).
+// TMEM columns: S double buffer 0-255 (a tile's P overwrites the first 64
+// columns of its S once they are read), O 256-383, Delta double buffer
+// 384-415, Q 448-511.  Every wait is bounded; every warp-collective tcgen05
+// load/store runs with the whole warp converged.
+//
+// Dequantisation is exact: a code c at bits [b i, b i + b) of a word becomes the
+// float c 2^(b i) by or-ing it into the mantissa of 2^23 and subtracting 2^23,
+// and fmaf(c 2^(b i), s 2^(-b i), z) rounds c s + z once, as fmaf(c, s, z) does.
 #include <cstdio>
 #include <cstdlib>
 
@@ -41,36 +54,44 @@ using namespace tc;
 constexpr int kM = 128;
 constexpr int kN = 128;
 constexpr int kD = 128;
-constexpr int kThreads = 288;
+constexpr int kSoftWarps = 4;
+constexpr int kProdWarps = 8;
+constexpr int kProd = 32 * kProdWarps;
+constexpr int kMmaWarp = kSoftWarps + kProdWarps;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescQK = idesc_bf16(kM, kN);   // S = Q K_hat^T, bf16 operands
-constexpr uint32_t kIdescPV = idesc_f16(kM, kD);    // O += P V_hat, fp16 operands
+constexpr uint32_t kColS = 0, kColO = 256, kColD = 384, kColQ = 448;
+constexpr uint32_t kIdescQK = idesc_bf16(kM, kN);   // S = Q K_hat^T
+constexpr uint32_t kIdescJ = idesc_bf16(kM, 16);    // Delta = (q^2) W^T
+constexpr uint32_t kIdescPV = idesc_f16(kM, kD);    // O += P V_hat
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int kTile = kM * kD * 2;          // 32 KB: one 16-bit 128 x 128 operand tile
-constexpr int kStage = 4 * 6144;            // packed bytes of 4 INT4 blocks (INT2: 4 x 4096)
-constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kTile;        // 1 buffer
+constexpr int kWBytes = 16 * kD * 2;        // 4 KB: 16 x 128 bf16 Jensen weights
+constexpr int kQ2hOff = 0;                  // bf16 high part of q^2
+constexpr int kQ2lOff = kQ2hOff + kTile;    // bf16 low part of q^2 (q^2 = high + low exactly)
+constexpr int kKOff = kQ2lOff + kTile;      // 1 buffer
 constexpr int kVOff = kKOff + kTile;        // 2 stages
-constexpr int kPOff = kVOff + 2 * kTile;
-constexpr int kStgOff = kPOff + kTile;      // 2 staging slots of packed blocks
-constexpr int kWOff = kStgOff + 2 * kStage; // 2 stages x 4 groups x 128 floats (Jensen weights)
-constexpr int kInfoOff = kWOff + 2 * 4 * kD * 4;
-constexpr int kStgLenOff = kInfoOff + 2 * 32;   // [2][4] valid lengths of the staged blocks
-constexpr int kBarOff = kStgLenOff + 2 * 16;
+constexpr int kWOff = kVOff + 2 * kTile;    // 2 stages
+constexpr int kStgOff = kWOff + 2 * kWBytes;
+
+template <int BITS> constexpr int block_bytes() { return 8 * kD * BITS + 16 * kD; }
+template <int BITS> constexpr int stage_bytes() { return 4 * block_bytes<BITS>(); }
+template <int BITS> constexpr int info_off() { return kStgOff + 2 * stage_bytes<BITS>(); }
+template <int BITS> constexpr int stglen_off() { return info_off<BITS>() + 2 * 32; }
+template <int BITS> constexpr int bar_off() { return stglen_off<BITS>() + 2 * 16; }
 constexpr int kNumBars = 13;
-constexpr int kSlotOff = kBarOff + kNumBars * 8;
-constexpr int kSmemUsed = kSlotOff + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
+template <int BITS> constexpr int slot_off() { return bar_off<BITS>() + kNumBars * 8; }
+template <int BITS> constexpr int smem_bytes() { return slot_off<BITS>() + 16 + 1024; }   // + alignment slack
 
 enum {
-    BAR_KV_FULL = 0,   // [2] producers -> MMA/softmax: K_hat, V_hat[s], weights[s], info[s] ready
-    BAR_V_EMPTY = 2,   // [2] PV of the stage's tile completed
-    BAR_S_FULL = 4,    // [2] S = Q K_hat^T of the tile in TMEM
+    BAR_KV_FULL = 0,   // [2] producers -> MMA/softmax: K_hat, V_hat[s], W[s], info[s] ready
+    BAR_V_EMPTY = 2,   // [2] P V of the stage's tile completed
+    BAR_S_FULL = 4,    // [2] S and Delta of the tile in TMEM
     BAR_P_FULL = 6,    // softmax -> MMA: P written
-    BAR_O_DONE = 7,    // PV completed
+    BAR_O_DONE = 7,    // P V completed
     BAR_K_EMPTY = 8,   // Q K_hat^T completed (K_hat may be overwritten)
     BAR_STG_FULL = 9,  // [2] staging slot filled by the bulk copy
     BAR_STG_EMPTY = 11,  // [2] all producers finished reading the staging slot
@@ -82,220 +103,206 @@ struct TileInfo {
     int pad[3];
 };
 
-// Byte offset of 16-byte chunk `ch` (0..15) of row `row` in a 128-row x 128-column
+// Byte offset of 16-byte chunk `ch` of row `row` in a `rows`-row x 128-column
 // 16-bit tile stored as two 64-column, 128-byte-swizzled K-major halves.
-__device__ __forceinline__ uint32_t sw_off(int row, int ch) {
-    return (uint32_t)((ch >> 3) * (kM * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+__device__ __forceinline__ uint32_t sw_off(int row, int ch, int rows = kM) {
+    return (uint32_t)((ch >> 3) * (rows * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
 
-// Dequantise 8 codes and pack them as bf16 (keys, F16OUT = false) or fp16 (values).
-template <bool F16OUT>
-__device__ __forceinline__ uint4 dq8_pack(const uint32_t codes[8], const float s[8], const float z[8]) {
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = dequant(codes[k], s[k], z[k]);
-    uint4 r;
-    if (F16OUT) {
-        r.x = pack_f16(v[0], v[1]);
-        r.y = pack_f16(v[2], v[3]);
-        r.z = pack_f16(v[4], v[5]);
-        r.w = pack_f16(v[6], v[7]);
-    } else {
-        r.x = pack_bf16(v[0], v[1]);
-        r.y = pack_bf16(v[2], v[3]);
-        r.z = pack_bf16(v[4], v[5]);
-        r.w = pack_bf16(v[6], v[7]);
-    }
-    return r;
+// 2^e for an integer e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// The b-bit code at bits [b i, b i + b) of x as the exact float c 2^(b i) (b i + b <= 23).
+template <int BITS>
+__device__ __forceinline__ float code_scaled(uint32_t x, int i) {
+    const uint32_t m = x & (((1u << BITS) - 1u) << (BITS * i));
+    return __uint_as_float(0x4B000000u | m) - 8388608.0f;
 }
 
 // ------------------------------------------------------------- producers ----
-// A staged cache tile: 4 consecutive blocks (the missing ones of a short last
-// tile count as empty) in staging slot `stage`, their valid lengths in stg_len.
-struct StagedTile {
-    const unsigned char* stg;
-    const int* len;
-    int nb;   // blocks present
-};
-
-// Values: thread p dequantises channel p of all 128 keys into V_hat^T[stage] and
-// records the tile's key-validity info.
+// Values of a staged cache tile.  Warp pw expands value group g = pw & 3
+// (channels 32 g .. 32 g + 31, one per lane) of blocks 2 (pw >> 2) and
+// 2 (pw >> 2) + 1 into V_hat^T[stage] (fp16).  The group's per-token steps are
+// first pre-scaled in the staging copy by 2^(-b i), i = the token's slot in its
+// half word.
 template <int BITS>
-__device__ void fill_cache_values(unsigned char* sm, int stage, const StagedTile& st, int p) {
+__device__ __forceinline__ void fill_cache_values(unsigned char* sm, int stage, unsigned char* stg, int nb, int pw,
+                                                  int lane) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    constexpr int kBlockBytes = 8 * kD * BITS + 16 * kD;
     unsigned char* Vt = sm + kVOff + stage * kTile;
-    TileInfo* info = reinterpret_cast<TileInfo*>(sm + kInfoOff) + stage;
-    if (p < 4) info->nvalid[p] = p < st.nb ? st.len[p] : 0;
-    if (p == 0) info->quantised = 1;
-    const int cc = p;
+    const int g = pw & 3, c = 32 * g + lane;
+    constexpr int kSlots = 16 / BITS;    // tokens per half word
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        if (q < st.nb) {
-            const unsigned char* blk = st.stg + q * kBlockBytes;
-            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc) + cc * BITS;
-            const float4* vm = reinterpret_cast<const float4*>(blk + o.vm) + (cc >> 5) * 16;  // 32 float2
-            uint32_t wv[BITS];
+    for (int bb = 0; bb < 2; ++bb) {
+        const int q = 2 * (pw >> 2) + bb;
+        if (q < nb) {
+            unsigned char* blk = stg + q * block_bytes<BITS>();
+            float2* vm = reinterpret_cast<float2*>(blk + o.vm) + g * 32;
+            float2 e = vm[lane];
+            e.x *= pow2i(-BITS * (lane % kSlots));
+            vm[lane] = e;
+            __syncwarp();
+            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc) + c * BITS;
+            uint32_t w[BITS];
 #pragma unroll
-            for (int k = 0; k < BITS; ++k) wv[k] = vc[k];
+            for (int k = 0; k < BITS; ++k) w[k] = vc[k];
+            const float4* sz = reinterpret_cast<const float4*>(vm);   // (s'_t, z_t, s'_t+1, z_t+1)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                float vs[8], vz[8];
+            for (int k8 = 0; k8 < 4; ++k8) {         // tokens 8 k8 .. 8 k8 + 7
+                float v[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 v = vm[kk * 4 + k];
-                    vs[2 * k] = v.x;
-                    vz[2 * k] = v.y;
-                    vs[2 * k + 1] = v.z;
-                    vz[2 * k + 1] = v.w;
+                for (int i = 0; i < 8; ++i) {
+                    const int t = 8 * k8 + i;
+                    const uint32_t x = BITS == 2 ? (w[t >> 4] >> (16 * ((t >> 3) & 1))) : (w[t >> 3] >> (16 * ((t >> 2) & 1)));
+                    const float4 p = sz[t >> 1];
+                    const float sp = (t & 1) ? p.z : p.x, zp = (t & 1) ? p.w : p.y;
+                    v[i] = fmaf(code_scaled<BITS>(x, t % kSlots), sp, zp);
                 }
-                uint32_t codes[8];
-                if (BITS == 2) {
-                    const uint32_t w = wv[kk >> 1] >> (16 * (kk & 1));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (2 * k)) & 3u;
-                } else {
-                    const uint32_t w = wv[kk];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (4 * k)) & 15u;
-                }
-                *reinterpret_cast<uint4*>(Vt + sw_off(cc, 4 * q + kk)) = dq8_pack<true>(codes, vs, vz);
+                uint4 r;
+                r.x = pack_f16(v[0], v[1]);
+                r.y = pack_f16(v[2], v[3]);
+                r.z = pack_f16(v[4], v[5]);
+                r.w = pack_f16(v[6], v[7]);
+                *reinterpret_cast<uint4*>(Vt + sw_off(c, 4 * q + k8)) = r;
             }
         } else {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                *reinterpret_cast<uint4*>(Vt + sw_off(cc, 4 * q + kk)) = make_uint4(0, 0, 0, 0);
+            for (int k8 = 0; k8 < 4; ++k8) *reinterpret_cast<uint4*>(Vt + sw_off(c, 4 * q + k8)) = make_uint4(0, 0, 0, 0);
         }
     }
 }
 
-// Keys: thread p dequantises channels 8jc..8jc+7 of keys r0, r0+8, ... into the
-// single K_hat buffer and stores the Jensen weights of its channels.
+// Keys of a staged cache tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
+// 8 kg .. 8 kg + 7 (one block) into K_hat (bf16).
 template <int BITS>
-__device__ void fill_cache_keys(unsigned char* sm, int stage, const StagedTile& st, int p, int jensen) {
+__device__ __forceinline__ void fill_cache_keys(unsigned char* sm, const unsigned char* stg, int nb, int p) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    constexpr int kBlockBytes = 8 * kD * BITS + 16 * kD;
-    constexpr int kWordsPerKey = kD * BITS / 32;
     unsigned char* Kt = sm + kKOff;
-    float* W = reinterpret_cast<float*>(sm + kWOff) + stage * 4 * kD;
-    const int jc = p & 15, r0 = p >> 4;
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        const bool exists = q < st.nb;
-        const unsigned char* blk = st.stg + q * kBlockBytes;
-        float s[8], z[8];
-        if (exists) {
-            const float4* km = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
+    const int jc = p & 15, kg = p >> 4, q = kg >> 2, t0 = 8 * (kg & 3);
+    if (q >= nb) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = km[k];
-                s[2 * k] = v.x;
-                z[2 * k] = v.y;
-                s[2 * k + 1] = v.z;
-                z[2 * k + 1] = v.w;
-            }
+        for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(8 * kg + r, jc)) = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const unsigned char* blk = stg + q * block_bytes<BITS>();
+    constexpr int kSlots = 16 / BITS;
+    const float4* km4 = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
+    float s[8], z[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 v = km4[k];
+        s[2 * k] = v.x;
+        z[2 * k] = v.y;
+        s[2 * k + 1] = v.z;
+        z[2 * k + 1] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] *= pow2i(-BITS * (i % kSlots));
+    constexpr int KW = kD * BITS / 32;   // code words per key
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int t = t0 + r;
+        float v[8];
+        if (BITS == 2) {
+            const uint32_t x = kc[t * KW + (jc >> 1)] >> (16 * (jc & 1));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = fmaf(code_scaled<2>(x, i), s[i], z[i]);
         } else {
+            const uint32_t w = kc[t * KW + jc];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s[k] = z[k] = 0.0f;
+            for (int i = 0; i < 8; ++i) v[i] = fmaf(code_scaled<4>(i < 4 ? w : (w >> 16), i & 3), s[i], z[i]);
         }
-        if (r0 == 0) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                W[q * kD + jc * 8 + k] = jensen == KV_JENSEN_EXACT ? s[k] : s[k] * s[k];
-        }
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = r0 + 8 * i;
-            const int row = 32 * q + t;
-            uint4 pk = make_uint4(0, 0, 0, 0);
-            if (exists) {
-                uint32_t codes[8];
-                if (BITS == 2) {
-                    const uint32_t w = kc[t * kWordsPerKey + (jc >> 1)] >> (16 * (jc & 1));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (2 * k)) & 3u;
-                } else {
-                    const uint32_t w = kc[t * kWordsPerKey + jc];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) codes[k] = (w >> (4 * k)) & 15u;
-                }
-                pk = dq8_pack<false>(codes, s, z);
-            }
-            *reinterpret_cast<uint4*>(Kt + sw_off(row, jc)) = pk;
-        }
+        uint4 rr;
+        rr.x = pack_bf16(v[0], v[1]);
+        rr.y = pack_bf16(v[2], v[3]);
+        rr.z = pack_bf16(v[4], v[5]);
+        rr.w = pack_bf16(v[6], v[7]);
+        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t, jc)) = rr;
     }
 }
 
-// Two bf16 values (half `hf` of two words) converted to an fp16 pair.
-__device__ __forceinline__ uint32_t f16_pair_from_bf16(uint32_t lo_word, uint32_t hi_word, int hf) {
-    const float lo = __uint_as_float(hf ? (lo_word & 0xFFFF0000u) : (lo_word << 16));
-    const float hi = __uint_as_float(hf ? (hi_word & 0xFFFF0000u) : (hi_word << 16));
-    return pack_f16(lo, hi);
+// Jensen weights of a staged tile.  TAYLOR2: W rows g and 4 + g hold the bf16
+// high and low parts of w_c = s_c^2 tau^2 / 24 log2(e) of block g (zero for
+// missing blocks); rows 8-15 stay zero.  EXACT: the block steps s_c as fp32 [4][128].
+template <int BITS, int JENSEN>
+__device__ __forceinline__ void fill_weights(unsigned char* sm, int stage, const unsigned char* stg, int nb, int p,
+                                             float coef) {
+    const IntBlockOffsets o = int_offsets(kD, BITS);
+    unsigned char* W = sm + kWOff + stage * kWBytes;
+    const int g = p >> 6, c = 2 * (p & 63);
+    float2 s = make_float2(0.0f, 0.0f);
+    if (g < nb) {
+        const float4 v = *reinterpret_cast<const float4*>(stg + g * block_bytes<BITS>() + o.km + c * 8);
+        s = make_float2(v.x, v.z);
+    }
+    if (JENSEN == KV_JENSEN_TAYLOR2) {
+        const float w0 = s.x * s.x * coef, w1 = s.y * s.y * coef;
+        const uint32_t hi = pack_bf16(w0, w1);
+        const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+        const uint32_t lo = pack_bf16(w0 - h0, w1 - h1);
+        const int cb = (c & 7) * 2;
+        *reinterpret_cast<uint32_t*>(W + sw_off(g, c >> 3, 16) + cb) = hi;
+        *reinterpret_cast<uint32_t*>(W + sw_off(4 + g, c >> 3, 16) + cb) = lo;
+    } else if (JENSEN == KV_JENSEN_EXACT) {
+        reinterpret_cast<float2*>(W)[(g * kD + c) >> 1] = s;
+    }
 }
 
-// Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T, and
-// the key-validity info.
-__device__ void fill_current_values(unsigned char* sm, int stage, const __nv_bfloat16* Vcur, long long row0,
-                                    int valid, int p) {
+// Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T.
+// Thread p transposes the 8 x 8 block (keys 8 (p >> 4) .., channels 8 (p & 15) ..).
+__device__ __forceinline__ void fill_current_values(unsigned char* sm, int stage, const __nv_bfloat16* Vcur,
+                                                    long long row0, int valid, int p) {
     unsigned char* Vt = sm + kVOff + stage * kTile;
-    TileInfo* info = reinterpret_cast<TileInfo*>(sm + kInfoOff) + stage;
-    if (p < 4) info->nvalid[p] = min(32, max(0, valid - 32 * p));
-    if (p == 0) info->quantised = 0;
     const uint4* Vg = reinterpret_cast<const uint4*>(Vcur + row0 * kD);
-    uint32_t x[2][8][4];                 // both 8x8 blocks' loads in flight before any store
+    const int kc8 = p >> 4, cch = p & 15;
+    uint32_t x[8][4];
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-        const int bi = p + 128 * rep;
-        const int kc8 = bi >> 4, cch = bi & 15;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int key = 8 * kc8 + k;
-            const uint4 v = key < valid ? __ldg(Vg + key * (kD / 8) + cch) : make_uint4(0, 0, 0, 0);
-            x[rep][k][0] = v.x;
-            x[rep][k][1] = v.y;
-            x[rep][k][2] = v.z;
-            x[rep][k][3] = v.w;
-        }
+    for (int k = 0; k < 8; ++k) {
+        const int key = 8 * kc8 + k;
+        const uint4 v = key < valid ? __ldg(Vg + key * (kD / 8) + cch) : make_uint4(0, 0, 0, 0);
+        x[k][0] = v.x;
+        x[k][1] = v.y;
+        x[k][2] = v.z;
+        x[k][3] = v.w;
     }
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-        const int bi = p + 128 * rep;
-        const int kc8 = bi >> 4, cch = bi & 15;
+    for (int i = 0; i < 8; ++i) {
+        // channel 8 cch + i: element i of every key row (word i / 2, half i & 1)
+        const int wi = i >> 1, hf = i & 1;
+        float f[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // channel 8cch+i: element i of every key row (word i/2, half i&1)
-            const int wi = i >> 1, hf = i & 1;
-            uint4 y;
-            y.x = f16_pair_from_bf16(x[rep][0][wi], x[rep][1][wi], hf);
-            y.y = f16_pair_from_bf16(x[rep][2][wi], x[rep][3][wi], hf);
-            y.z = f16_pair_from_bf16(x[rep][4][wi], x[rep][5][wi], hf);
-            y.w = f16_pair_from_bf16(x[rep][6][wi], x[rep][7][wi], hf);
-            *reinterpret_cast<uint4*>(Vt + sw_off(8 * cch + i, kc8)) = y;
-        }
+        for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(hf ? (x[k][wi] & 0xFFFF0000u) : (x[k][wi] << 16));
+        uint4 y;
+        y.x = pack_f16(f[0], f[1]);
+        y.y = pack_f16(f[2], f[3]);
+        y.z = pack_f16(f[4], f[5]);
+        y.w = pack_f16(f[6], f[7]);
+        *reinterpret_cast<uint4*>(Vt + sw_off(8 * cch + i, kc8)) = y;
     }
 }
 
 // Current-chunk keys: bf16 rows copied into the swizzled K_hat buffer.
-__device__ void fill_current_keys(unsigned char* sm, const __nv_bfloat16* Kcur, long long row0, int valid, int p) {
+__device__ __forceinline__ void fill_current_keys(unsigned char* sm, const __nv_bfloat16* Kcur, long long row0,
+                                                  int valid, int p) {
     unsigned char* Kt = sm + kKOff;
     const int jc = p & 15, r0 = p >> 4;
     const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
-    uint4 kv[16];                        // all loads in flight before the first store
+    uint4 kv[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int row = r0 + 8 * i;
+    for (int i = 0; i < 8; ++i) {
+        const int row = r0 + 16 * i;
         kv[i] = row < valid ? __ldg(Kg + row * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 8 * i, jc)) = kv[i];
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 16 * i, jc)) = kv[i];
 }
 
 // --------------------------------------------------------------- kernel -----
-template <int BITS>
+template <int BITS, int JENSEN>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kcur,
-               const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau, int jensen,
+               const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau,
                int n_splits, void* __restrict__ out, int out_f32, float* __restrict__ lse, float* __restrict__ ws_o,
                float2* __restrict__ ws_ml, int* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
@@ -303,7 +310,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     unsigned char* sm =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_qt = (n_q + kM - 1) / kM;
     const int qt = blockIdx.x % n_qt, split = blockIdx.x / n_qt;
     const int hq = blockIdx.y, b = blockIdx.z;
@@ -316,49 +323,84 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     // cache and current-chunk tiles, and its cache tiles still come first.
     const int T = split < n_tiles ? (n_tiles - split + n_splits - 1) / n_splits : 0;
     auto tile_of = [&](int j) { return split + j * n_splits; };
-    auto bar = [&](int i) { return sbase + kBarOff + 8 * i; };
+    auto bar = [&](int i) { return sbase + bar_off<BITS>() + 8 * i; };
+    TileInfo* infos = reinterpret_cast<TileInfo*>(sm + info_off<BITS>());
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bar(BAR_KV_FULL + 0), 128);
-        mbar_init(bar(BAR_KV_FULL + 1), 128);
+        mbar_init(bar(BAR_KV_FULL + 0), kProd);
+        mbar_init(bar(BAR_KV_FULL + 1), kProd);
         mbar_init(bar(BAR_V_EMPTY + 0), 1);
         mbar_init(bar(BAR_V_EMPTY + 1), 1);
         mbar_init(bar(BAR_S_FULL + 0), 1);
         mbar_init(bar(BAR_S_FULL + 1), 1);
-        mbar_init(bar(BAR_P_FULL), 128);
+        mbar_init(bar(BAR_P_FULL), 32 * kSoftWarps);
         mbar_init(bar(BAR_O_DONE), 1);
         mbar_init(bar(BAR_K_EMPTY), 1);
         mbar_init(bar(BAR_STG_FULL + 0), 1);
         mbar_init(bar(BAR_STG_FULL + 1), 1);
-        mbar_init(bar(BAR_STG_EMPTY + 0), 128);
-        mbar_init(bar(BAR_STG_EMPTY + 1), 128);
+        mbar_init(bar(BAR_STG_EMPTY + 0), kProd);
+        mbar_init(bar(BAR_STG_EMPTY + 1), kProd);
         mbar_fence_init();
     }
-    if (warp == 8) tmem_alloc(sbase + kSlotOff, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(sbase + slot_off<BITS>(), kTmemCols);
 
-    // Q tile -> swizzled smem (rows beyond n_q are zero)
-    if (tid < 256) {
-        const uint4* Qg = reinterpret_cast<const uint4*>(Q + (((long long)b * Hq + hq) * n_q) * kD);
-#pragma unroll 4
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + 256 * i;
+    // q^2 of the Q tile (bf16 q, so q^2 has at most 16 significant bits and splits
+    // exactly into bf16 high + low) -> swizzled smem, rows beyond n_q zero; the
+    // Jensen weight tiles start zero (rows 8-15 stay zero)
+    const uint4* Qg = reinterpret_cast<const uint4*>(Q + (((long long)b * Hq + hq) * n_q) * kD);
+    {
+        for (int e = tid; e < kM * kD / 8; e += kThreads) {
             const int row = e >> 4, ch = e & 15;
             const uint4 v =
                 (q0 + row < n_q) ? __ldg(Qg + (long long)(q0 + row) * (kD / 8) + ch) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kQOff + sw_off(row, ch)) = v;
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t hq2[4], lq2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lo = __uint_as_float(wv[k] << 16), hi = __uint_as_float(wv[k] & 0xFFFF0000u);
+                const float a = lo * lo, bq = hi * hi;
+                hq2[k] = pack_bf16(a, bq);
+                lq2[k] = pack_bf16(a - __uint_as_float(hq2[k] << 16), bq - __uint_as_float(hq2[k] & 0xFFFF0000u));
+            }
+            *reinterpret_cast<uint4*>(sm + kQ2hOff + sw_off(row, ch)) = make_uint4(hq2[0], hq2[1], hq2[2], hq2[3]);
+            *reinterpret_cast<uint4*>(sm + kQ2lOff + sw_off(row, ch)) = make_uint4(lq2[0], lq2[1], lq2[2], lq2[3]);
         }
+        for (int e = tid; e < 2 * kWBytes / 16; e += kThreads)
+            reinterpret_cast<uint4*>(sm + kWOff)[e] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async();
     fence_before();
     __syncthreads();
     fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kSlotOff);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + slot_off<BITS>());
+    if (warp < kSoftWarps) {
+        // Q row i -> TMEM lane i, columns kColQ .. kColQ + 63 (two bf16 per column)
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const bool valid = q0 + tid < n_q;
+#pragma unroll
+        for (int hf = 0; hf < 4; ++hf) {
+            uint32_t u[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = valid ? __ldg(Qg + (long long)(q0 + tid) * (kD / 8) + 4 * hf + k) : make_uint4(0, 0, 0, 0);
+                u[4 * k] = v.x;
+                u[4 * k + 1] = v.y;
+                u[4 * k + 2] = v.z;
+                u[4 * k + 3] = v.w;
+            }
+            tmem_st16(tmem + lane_addr + kColQ + 16 * hf, u);
+        }
+        tmem_wait_st();
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
 
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
-        if ((tid & 31) == 0) {
-            const uint32_t sQ = sbase + kQOff, sP = sbase + kPOff;
+        if (lane == 0) {
+            const uint32_t sQ2h = sbase + kQ2hOff, sQ2l = sbase + kQ2lOff, sK = sbase + kKOff;
             auto issue_pv = [&](int jj) -> bool {
                 if (!mbar_wait(bar(BAR_P_FULL), jj & 1, &abort_flag, err, 3)) return false;
                 fence_after();
@@ -366,8 +408,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-                    mma_f16kind(tmem + 256, desc_sw128(sP + off), desc_sw128(sV + off), kIdescPV,
-                                (jj > 0 || kk > 0));
+                    mma_f16kind_ts(tmem + kColO, tmem + kColS + (jj & 1) * kN + 8 * kk, desc_sw128(sV + off), kIdescPV,
+                                   (jj > 0 || kk > 0));
                 }
                 mma_commit(bar(BAR_O_DONE));
                 mma_commit(bar(BAR_V_EMPTY + (jj & 1)));
@@ -378,11 +420,21 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 const int s = j & 1;
                 if (!mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 1)) break;
                 fence_after();
-                const uint32_t sK = sbase + kKOff;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-                    mma_f16kind(tmem + s * kN, desc_sw128(sQ + off), desc_sw128(sK + off), kIdescQK, kk > 0);
+                    mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColQ + 8 * kk, desc_sw128(sK + off), kIdescQK, kk > 0);
+                }
+                if (JENSEN == KV_JENSEN_TAYLOR2 && tile_of(j) < n_cache_tiles) {
+                    const uint32_t sW = sbase + kWOff + s * kWBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 2 * (kD / 16); ++kk) {
+                        const int k = kk & 7;
+                        const uint32_t offa = (k >> 2) * (kM * 128) + (k & 3) * 32;
+                        const uint32_t offb = (k >> 2) * (16 * 128) + (k & 3) * 32;
+                        mma_f16kind(tmem + kColD + 16 * s, desc_sw128((kk < 8 ? sQ2h : sQ2l) + offa),
+                                    desc_sw128(sW + offb), kIdescJ, kk > 0);
+                    }
                 }
                 mma_commit(bar(BAR_S_FULL + s));
                 mma_commit(bar(BAR_K_EMPTY));
@@ -391,11 +443,13 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (ok && T > 0 && !abort_flag) issue_pv(T - 1);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= kSoftWarps) {
         // ----------------------------------------------------------- producers
-        const int p = tid - 128;
+        const int p = tid - 32 * kSoftWarps, pw = p >> 5;
         const int nblk = c.n_blocks[seg];
-        int* stg_len = reinterpret_cast<int*>(sm + kStgLenOff);
+        int* stg_len = reinterpret_cast<int*>(sm + stglen_off<BITS>());
+        const float jcoef = tau * tau * (1.0f / 24.0f) * kLog2e;
+        int issued = 0;   // staging copies issued (by producer thread 0)
         // Bulk-copy cache tile j (if it is one) into staging slot j & 1, with its
         // blocks' valid lengths; run by producer thread 0 two tiles ahead.
         auto stage_copy = [&](int j) {
@@ -403,17 +457,20 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (j >= T || tile >= n_cache_tiles) return;
             const int nb = min(4, nblk - tile * 4);
             for (int q = 0; q < 4; ++q)
-                stg_len[(j & 1) * 4 + q] = q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
-            const uint32_t bytes = (uint32_t)(nb * c.block_bytes[seg]);
+                stg_len[(j & 1) * 4 + q] =
+                    q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
+            const uint32_t bytes = (uint32_t)(nb * block_bytes<BITS>());
             const uint32_t sbar = bar(BAR_STG_FULL + (j & 1));
             mbar_expect_tx(sbar, bytes);
-            bulk_g2s(sbase + kStgOff + (j & 1) * kStage, block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
+            bulk_g2s(sbase + kStgOff + (j & 1) * stage_bytes<BITS>(), block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
+            issued = j + 1;
         };
         if (p == 0) {
             stage_copy(0);
             stage_copy(1);
         }
-        for (int j = 0; j < T; ++j) {
+        int j = 0;
+        for (; j < T; ++j) {
             const int s = j & 1;
             const int tile = tile_of(j);
             const bool cached = tile < n_cache_tiles;
@@ -421,20 +478,25 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (j >= 2) ok = mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
             if (ok && cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
             if (!__all_sync(0xffffffffu, ok)) break;
-            StagedTile st;
-            st.stg = sm + kStgOff + s * kStage;
-            st.len = stg_len + s * 4;
-            st.nb = cached ? min(4, nblk - tile * 4) : 0;
+            unsigned char* stg = sm + kStgOff + s * stage_bytes<BITS>();
+            const int nb = cached ? min(4, nblk - tile * 4) : 0;
             const int t0 = (tile - n_cache_tiles) * kN;
             const long long row0 = ((long long)b * c.Hkv + h) * n_cur + t0;
-            // values first: they only need the V_hat stage, free since PV of tile j - 2
-            if (cached) fill_cache_values<BITS>(sm, s, st, p);
-            else fill_current_values(sm, s, Vcur, row0, min(kN, n_cur - t0), p);
+            const int cvalid = min(kN, n_cur - t0);
+            if (p < 4) infos[s].nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
+            if (p == 0) infos[s].quantised = cached ? 1 : 0;
+            // values first: they only need the V_hat stage, free since P V of tile j - 2
+            if (cached) {
+                fill_cache_values<BITS>(sm, s, stg, nb, pw, lane);
+                if (JENSEN != KV_JENSEN_OFF) fill_weights<BITS, JENSEN>(sm, s, stg, nb, p, jcoef);
+            } else {
+                fill_current_values(sm, s, Vcur, row0, cvalid, p);
+            }
             // keys: the single K_hat buffer is free once Q K_hat^T of tile j - 1 completed
             const bool ok2 = j == 0 || mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
             if (!__all_sync(0xffffffffu, ok2)) break;
-            if (cached) fill_cache_keys<BITS>(sm, s, st, p, jensen);
-            else fill_current_keys(sm, Kcur, row0, min(kN, n_cur - t0), p);
+            if (cached) fill_cache_keys<BITS>(sm, stg, nb, p);
+            else fill_current_keys(sm, Kcur, row0, cvalid, p);
             fence_proxy_async();
             mbar_arrive(bar(BAR_KV_FULL + s));
             if (cached) {
@@ -446,116 +508,116 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     stage_copy(j + 2);
             }
         }
+        if (p == 0) {
+            // copies still in flight after an abort land (bounded wait) before the CTA exits
+            for (int jj = j; jj < issued; ++jj) {
+                if (tile_of(jj) >= n_cache_tiles) continue;
+                const long long t0c = clock64();
+                while (!mbar_try_wait(bar(BAR_STG_FULL + (jj & 1)), (jj >> 1) & 1) && clock64() - t0c < 100000000LL) {
+                }
+            }
+        }
         __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax
         const int i = tid;                          // query row = TMEM lane
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        const float sc = tau * kLog2e;
-        const float jt = jensen == KV_JENSEN_TAYLOR2 ? tau * tau * (1.0f / 24.0f) * kLog2e : 0.5f * tau;
-        // l_run sums the fp16-rounded P that the PV product consumes (so O / l_run
-        // is a properly normalised average); l_ex sums the unrounded p for the lse.
-        float m_ref = -INFINITY, l_run = 0.0f, l_ex = 0.0f;
-        float x[kN];
+        const float c1 = tau * kLog2e;
+        float m_ref = -INFINITY, l_sum = 0.0f;
+        float x[32];
         for (int j = 0; j < T; ++j) {
             const int s = j & 1;
-            // the tile's metadata is ready: compute the Jensen terms while Q K^T runs
             const bool ok0 = mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok0)) break;
-            const TileInfo info = reinterpret_cast<const TileInfo*>(sm + kInfoOff)[s];
-            float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (info.quantised && jensen != KV_JENSEN_OFF) {
-                const float4* W4 = reinterpret_cast<const float4*>(sm + kWOff) + s * kD;   // [4][32] float4
-#pragma unroll 2
-                for (int ch = 0; ch < 16; ++ch) {
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + kQOff + sw_off(i, ch));
-                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                    float qf[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        qf[k] = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const float4 wa = W4[g * 32 + 2 * ch], wb = W4[g * 32 + 2 * ch + 1];
-                        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-                        if (jensen == KV_JENSEN_TAYLOR2) {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) dl[g] = fmaf(qf[k] * qf[k], w[k], dl[g]);
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) dl[g] += log_sinhc(jt * qf[k] * w[k]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < 4; ++g) dl[g] *= (jensen == KV_JENSEN_TAYLOR2 ? jt : kLog2e);
-            }
+            const TileInfo info = infos[s];
             const bool ok1 = mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
             if (!__all_sync(0xffffffffu, ok1)) break;
             fence_after();
+            float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (info.quantised) {
+                if (JENSEN == KV_JENSEN_TAYLOR2) {
+                    float dv[8];
+                    tmem_ld8(tmem + lane_addr + kColD + 16 * s, dv);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) tmem_ld32(tmem + lane_addr + s * kN + 32 * g, x + 32 * g);
+                    for (int g = 0; g < 4; ++g) dl[g] = dv[g] + dv[4 + g];
+                } else if (JENSEN == KV_JENSEN_EXACT) {
+                    const float* SK = reinterpret_cast<const float*>(sm + kWOff + s * kWBytes);
+                    const float jt = 0.5f * tau;
+#pragma unroll 1
+                    for (int ch = 0; ch < 16; ++ch) {
+                        const uint4 qv = q0 + i < n_q ? __ldg(Qg + (long long)(q0 + i) * (kD / 8) + ch)
+                                                      : make_uint4(0, 0, 0, 0);
+                        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float qf = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(jt * qf * SK[g * kD + 8 * ch + k]);
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) dl[g] *= kLog2e;
+                }
+            }
+            // pass 1: the tile's maximum of the corrected logits (log2 units)
             float mt = -INFINITY;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 const int nv = info.nvalid[g];
+                tmem_ld32(tmem + lane_addr + kColS + s * kN + 32 * g, x);
+                float mx = -INFINITY;
+                if (nv == 32) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float v = k < nv ? fmaf(x[32 * g + k], sc, -dl[g]) : -INFINITY;
-                    x[32 * g + k] = v;
-                    mt = fmaxf(mt, v);
+                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, x[k]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, k < nv ? x[k] : -INFINITY);
                 }
+                if (nv > 0) mt = fmaxf(mt, fmaf(mx, c1, -dl[g]));
             }
             const float m_new = fmaxf(m_ref, mt);
             const bool grow = m_new > m_ref + 8.0f;       // also true for the first finite max
-            const bool ok2 = j == 0 || mbar_wait(bar(BAR_O_DONE), (j - 1) & 1, &abort_flag, err, 6);
-            if (!__all_sync(0xffffffffu, ok2)) break;
-            fence_after();
-            // O is rescaled in TMEM when any row of the warp needs it; tcgen05.ld/st
-            // are warp-collective, so the whole warp takes the branch (alpha = 1 for
-            // rows whose running max did not move).
-            const bool resc = grow && j > 0 && m_ref != -INFINITY;
+            // O is rescaled in TMEM when any row of the warp needs it, after P V of
+            // tile j - 1 has completed; tcgen05.ld/st are warp-collective, so the whole
+            // warp takes the branch (alpha = 1 for rows whose running max did not move).
+            const bool resc = grow && j > 0;
             const float alpha = resc ? ex2(m_ref - m_new) : 1.0f;
             if (__any_sync(0xffffffffu, resc)) {
+                const bool ok2 = mbar_wait(bar(BAR_O_DONE), (j - 1) & 1, &abort_flag, err, 6);
+                if (!__all_sync(0xffffffffu, ok2)) break;
+                fence_after();
                 float ob[32];
 #pragma unroll 1
                 for (int g = 0; g < 4; ++g) {
-                    tmem_ld32(tmem + lane_addr + 256 + 32 * g, ob);
+                    tmem_ld32(tmem + lane_addr + kColO + 32 * g, ob);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) ob[k] *= alpha;
-                    tmem_st32(tmem + lane_addr + 256 + 32 * g, ob);
+                    tmem_st32(tmem + lane_addr + kColO + 32 * g, ob);
                 }
             }
-            l_run *= alpha;
-            l_ex *= alpha;
+            l_sum *= alpha;
             if (grow) m_ref = m_new;
             const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-            float psum = 0.0f, rsum = 0.0f;
-            unsigned char* P = sm + kPOff;
+            // pass 2: p = 2^(S c1 - (m + delta_g)), summed in fp32, stored as fp16 over the
+            // S columns already read (group g's 16 columns of P land in columns 16 g ..)
+            float psum = 0.0f;
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                float pv[8];
+            for (int g = 0; g < 4; ++g) {
+                const int nv = info.nvalid[g];
+                tmem_ld32(tmem + lane_addr + kColS + s * kN + 32 * g, x);
+                const float bg = m_use + dl[g];
+                uint32_t u[16];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    pv[k] = ex2(x[ch * 8 + k] - m_use);
-                    psum += pv[k];
+                for (int k = 0; k < 16; ++k) {
+                    const float p0 = 2 * k < nv ? ex2(fmaf(x[2 * k], c1, -bg)) : 0.0f;
+                    const float p1 = 2 * k + 1 < nv ? ex2(fmaf(x[2 * k + 1], c1, -bg)) : 0.0f;
+                    psum += p0 + p1;
+                    u[k] = pack_f16(p0, p1);
                 }
-                uint4 pk;
-                pk.x = pack_f16(pv[0], pv[1]);
-                pk.y = pack_f16(pv[2], pv[3]);
-                pk.z = pack_f16(pv[4], pv[5]);
-                pk.w = pack_f16(pv[6], pv[7]);
-                const uint32_t pw[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pw[k]));
-                    rsum += f.x + f.y;
-                }
-                *reinterpret_cast<uint4*>(P + sw_off(i, ch)) = pk;
+                tmem_st16(tmem + lane_addr + kColS + s * kN + 16 * g, u);
             }
-            l_run += rsum;
-            l_ex += psum;
-            fence_proxy_async();
+            l_sum += psum;
+            tmem_wait_st();
             fence_before();
             mbar_arrive(bar(BAR_P_FULL));
         }
@@ -566,14 +628,14 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         if (have) have = mbar_wait(bar(BAR_O_DONE), (T - 1) & 1, &abort_flag, err, 7);
         have = __all_sync(0xffffffffu, have);
         fence_after();
-        const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+        const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
         const long long rows = (long long)c.B * Hq * n_q;
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) {
             float ob[32];
             __syncwarp();
             if (have) {
-                tmem_ld32(tmem + lane_addr + 256 + 32 * g, ob);
+                tmem_ld32(tmem + lane_addr + kColO + 32 * g, ob);
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k) ob[k] = 0.0f;
@@ -606,16 +668,16 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         }
         if (qi < n_q) {
             if (n_splits == 1) {
-                if (lse) lse[orow] = (m_ref + log2f(l_ex)) * kLn2;
+                if (lse) lse[orow] = l_sum > 0.0f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
             } else {
-                ws_ml[(long long)split * rows + orow] = make_float2(l_run > 0.0f ? m_ref * kLn2 : -INFINITY, l_run);
+                ws_ml[(long long)split * rows + orow] = make_float2(l_sum > 0.0f ? m_ref * kLn2 : -INFINITY, l_sum);
             }
         }
         __syncwarp();
     }
     fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -631,6 +693,27 @@ int num_sms() {
         if (g_num_sms <= 0) g_num_sms = 148;
     }
     return g_num_sms;
+}
+
+template <int BITS, int JENSEN>
+kv_status launch_tc_t(const DevCache& c, const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
+                      float tau, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
+                      int* err, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<BITS, JENSEN>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BITS>());
+        if (e != cudaSuccess)
+            return set_error(KV_ERR_CUDA, "attn_tc_kernel: %d bytes of shared memory: %s", smem_bytes<BITS>(),
+                             cudaGetErrorString(e));
+        attr = true;
+    }
+    const int n_qt = (n_q + kM - 1) / kM;
+    dim3 grid(n_qt * n_splits, Hq, c.B);
+    attn_tc_kernel<BITS, JENSEN><<<grid, kThreads, smem_bytes<BITS>(), st>>>(
+        static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
+        static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, n_splits, out, out_f32, lse, ws_o, ws_ml, err);
+    return check_launch("attn_tc_kernel");
 }
 
 }  // namespace
@@ -683,32 +766,31 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
     float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + 256);
     const long long rows = (long long)c.B * Hq * n_q;
     float2* ws_ml = reinterpret_cast<float2*>(ws_o + (n_splits > 1 ? (long long)n_splits * rows * kD : 0));
-    const int n_qt = (n_q + kM - 1) / kM;
-    dim3 grid(n_qt * n_splits, Hq, c.B);
-    cudaMemsetAsync(err, 0, sizeof(int), st);
-    static bool attr2 = false, attr4 = false;
-    if (c.kind == KV_UNIFORM4) {
-        if (!attr4) {
-            cudaFuncSetAttribute(attn_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            attr4 = true;
-        }
-        attn_tc_kernel<4><<<grid, kThreads, kSmemBytes, st>>>(
-            static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
-            static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, jensen, n_splits, out, out_f32, lse, ws_o,
-            ws_ml, err);
-    } else {
-        if (!attr2) {
-            cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            attr2 = true;
-        }
-        attn_tc_kernel<2><<<grid, kThreads, kSmemBytes, st>>>(
-            static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
-            static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, jensen, n_splits, out, out_f32, lse, ws_o,
-            ws_ml, err);
+    const bool debug = getenv("BITKV_DEBUG_SYNC") != nullptr;
+    if (debug) cudaMemsetAsync(err, 0, sizeof(int), st);
+    kv_status s;
+#define BITKV_TC(BITS)                                                                                        \
+    switch (jensen) {                                                                                         \
+        case KV_JENSEN_TAYLOR2:                                                                               \
+            s = launch_tc_t<BITS, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32, \
+                                                     lse, ws_o, ws_ml, err, st);                              \
+            break;                                                                                            \
+        case KV_JENSEN_EXACT:                                                                                 \
+            s = launch_tc_t<BITS, KV_JENSEN_EXACT>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32,   \
+                                                   lse, ws_o, ws_ml, err, st);                                \
+            break;                                                                                            \
+        default:                                                                                              \
+            s = launch_tc_t<BITS, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32, lse, \
+                                                 ws_o, ws_ml, err, st);                                       \
     }
-    kv_status s = check_launch("attn_tc_kernel");
+    if (c.kind == KV_UNIFORM4) {
+        BITKV_TC(4)
+    } else {
+        BITKV_TC(2)
+    }
+#undef BITKV_TC
     if (s != KV_OK) return s;
-    if (getenv("BITKV_DEBUG_SYNC")) {
+    if (debug) {
         int h_err = 0;
         cudaMemcpyAsync(&h_err, err, sizeof(int), cudaMemcpyDeviceToHost, st);
         cudaStreamSynchronize(st);
