@@ -211,48 +211,73 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
 }
 
 // Merge split partials: m = max m_p, l = sum l_p e^{m_p - m}, o = sum l_p e^{m_p - m} o_p / l.
+// One warp per row: the split weights are reduced across lanes, then each lane
+// combines 4 channels (128-bit loads) per pass over the splits.
+constexpr int kMergeRows = 8;   // rows (warps) per CTA
+
 template <typename T>
-__global__ void lse_merge_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int n_splits,
-                                 long long rows, int d, void* __restrict__ out, int out_f32, float* __restrict__ lse) {
-    const long long row = blockIdx.x;
+__global__ void __launch_bounds__(32 * kMergeRows)
+lse_merge_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int n_splits, long long rows, int d,
+                 void* __restrict__ out, int out_f32, float* __restrict__ lse) {
+    const long long row = (long long)blockIdx.x * kMergeRows + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
     float m = -INFINITY;
-    for (int p = 0; p < n_splits; ++p) {
+    for (int p = lane; p < n_splits; p += 32) {
         const float2 ml = ws_ml[p * rows + row];
         if (ml.y > 0.0f) m = fmaxf(m, ml.x);
     }
+    m = warp_max(m);
     float l = 0.0f;
-    for (int p = 0; p < n_splits; ++p) {
+    for (int p = lane; p < n_splits; p += 32) {
         const float2 ml = ws_ml[p * rows + row];
         if (ml.y > 0.0f) l += ml.y * expf(ml.x - m);
     }
+    l = warp_sum(l);
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    for (int ch = threadIdx.x; ch < d; ch += blockDim.x) {
-        float acc = 0.0f;
+    for (int c4 = lane; c4 < d / 4; c4 += 32) {
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         for (int p = 0; p < n_splits; ++p) {
             const float2 ml = ws_ml[p * rows + row];
-            if (ml.y > 0.0f) acc = fmaf(ml.y * expf(ml.x - m), ws_o[(p * rows + row) * d + ch], acc);
+            if (ml.y > 0.0f) {
+                const float w = ml.y * expf(ml.x - m);
+                const float4 o = reinterpret_cast<const float4*>(ws_o + (p * rows + row) * d)[c4];
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+            }
         }
-        const float v = acc * inv;
-        if (out_f32) static_cast<float*>(out)[row * d + ch] = v;
-        else static_cast<T*>(out)[row * d + ch] = from_f32<T>(v);
+        const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+        if (out_f32) {
+            reinterpret_cast<float4*>(static_cast<float*>(out) + row * d)[c4] = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            T* o = static_cast<T*>(out) + row * d + 4 * c4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = from_f32<T>(v[k]);
+        }
     }
-    if (lse && threadIdx.x == 0) lse[row] = m + logf(l);
+    if (lse && lane == 0) lse[row] = m + logf(l);
 }
 
 }  // namespace
+
+static unsigned merge_grid(long long rows) { return (unsigned)((rows + kMergeRows - 1) / kMergeRows); }
 
 kv_status launch_lse_merge(kv_dtype dt, const float* ws_o, const float2* ws_ml, int n_splits, long long rows, int d,
                            void* out, int out_f32, float* lse, cudaStream_t st) {
     switch (dt) {
         case KV_F32:
-            lse_merge_kernel<float><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out, out_f32, lse);
+            lse_merge_kernel<float><<<merge_grid(rows), 32 * kMergeRows, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out,
+                                                                                 out_f32, lse);
             break;
         case KV_F16:
-            lse_merge_kernel<__half><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out, out_f32, lse);
+            lse_merge_kernel<__half><<<merge_grid(rows), 32 * kMergeRows, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out,
+                                                                                  out_f32, lse);
             break;
         case KV_BF16:
-            lse_merge_kernel<__nv_bfloat16><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, d, out,
-                                                                            out_f32, lse);
+            lse_merge_kernel<__nv_bfloat16><<<merge_grid(rows), 32 * kMergeRows, 0, st>>>(ws_o, ws_ml, n_splits, rows,
+                                                                                         d, out, out_f32, lse);
             break;
     }
     return check_launch("lse_merge_kernel");
@@ -298,7 +323,8 @@ static kv_status launch_simt_t(const void* Q, const void* Kc, const void* Vc, in
     }
     kv_status s = check_launch("attn_simt_kernel");
     if (s != KV_OK || n_splits == 1) return s;
-    lse_merge_kernel<T><<<(unsigned)rows, 128, 0, st>>>(ws_o, ws_ml, n_splits, rows, c.d, out, out_f32, lse);
+    lse_merge_kernel<T><<<merge_grid(rows), 32 * kMergeRows, 0, st>>>(ws_o, ws_ml, n_splits, rows, c.d, out, out_f32,
+                                                                      lse);
     return check_launch("lse_merge_kernel");
 }
 
