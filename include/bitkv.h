@@ -225,14 +225,15 @@ kv_status kv_window_plan(const float* sim, int n_windows, const kv_thresholds* t
                          int32_t* perm_out);
 
 /* Fit CODEBOOK2 key centroids ([QWM] QSAC): per (b, kv head, channel) 1-D
- * Lloyd k-means, 4 centroids, quantile init x_(floor((2k+1)n/8)), `iters`
- * iterations, nearest by fp64 |x - mu| (ties to the lower index), exact fp64
- * member sums, empty clusters keep their centroid.  K (device)
- * [B][Hkv][n_tokens][d] (bf16/f16/f32); writes cache->centroids as fp32.
+ * Lloyd k-means, 4 centroids, quantile init x_(floor((2k+1)n/8)) of the sorted
+ * values, `iters` iterations, nearest by fp64 |x - mu| (ties to the lower index),
+ * fp64 member sums (exact for 16-bit inputs at these sizes), empty clusters
+ * keep their centroid.  K (device) [B][Hkv][n_tokens][d] (bf16/f16/f32),
+ * n_tokens <= 32768; writes cache->centroids as fp32 [B][Hkv][d][4].
  * Qhist (device, nullable) [B][Hkv][n_hist][d] in dtype: if given, the
  * per-channel sensitivity mean q_c^2 is written to weights_out (device,
  * [B][Hkv][d] fp32); it is a per-channel constant and does not change the
- * centroids.  workspace (device) >= kv_codebook_workspace(). */
+ * centroids.  Needs no workspace (kv_codebook_workspace() returns 0). */
 size_t kv_codebook_workspace(const kv_layout* layout, int n_tokens);
 kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, int iters,
                           const void* Qhist, int n_hist, float* weights_out, void* workspace, size_t ws_bytes,
@@ -240,10 +241,13 @@ kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache*
 
 /* PSAC basis ([QWM] principal-subspace compensation): for each (b, kv head) the
  * top-r eigenvectors of the uncentred second moment (1/n) sum q q^T of the
- * historical queries Qhist (device) [B][Hkv][n_hist][d], largest-magnitude
- * entry of each made positive.  Writes cache->psac_u (fp32 [d][r]) and, if
- * eigvals_out (device) is non-null, the r eigenvalues [B][Hkv][r].  Cyclic
- * Jacobi in fp64 on the device; workspace >= kv_psac_workspace(). */
+ * historical queries Qhist (device) [B][Hkv][n_hist][d], eigenvalues
+ * descending (ties to the lower index), the largest-magnitude entry of each
+ * made positive.  Writes cache->psac_u (fp32 [d][r]) and, if eigvals_out
+ * (device) is non-null, the r eigenvalues [B][Hkv][r].  The second moment is
+ * accumulated in fp64 and diagonalised by a cyclic Jacobi method in fp64 on
+ * the device (d even, <= 128); workspace (device) >= kv_psac_workspace() =
+ * 2 B Hkv d^2 doubles. */
 size_t kv_psac_workspace(const kv_layout* layout);
 kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache* cache, float* eigvals_out,
                         void* workspace, size_t ws_bytes, void* stream);
