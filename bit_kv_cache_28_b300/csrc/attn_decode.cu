@@ -129,306 +129,330 @@ __device__ __forceinline__ LaneConst lane_const(int lane) {
     return c;
 }
 
-// Running softmax state of one warp: rows r = 0 (head g) and r = 1 (head g + 8).
-// m in the log2 domain; l and pz are this lane's partial sums (reduced over the
-// lane quad at the end); o is the P V accumulator fragment (c0, c1 row g;
-// c2, c3 row g + 8) over n-tiles of 8 channels.
-template <int D>
+// Running softmax state of one warp in the transposed form: the MMAs compute
+// S^T [keys x heads] and O^T [channels x heads], so a lane owns heads
+// 2 tig, 2 tig + 1 (+ 8 nt) of every accumulator fragment.  m in the log2
+// domain; l and pz are this lane's partial sums (reduced over the 8 lane
+// groups at the end); o[cm][nt] is the O^T fragment of channels 16 cm + g,
+// 16 cm + 8 + g.
+template <int D, int NT>
 struct DecState {
-    float m[2], l[2];
-    float o[D / 8][4];
-    float pz[2][D / 32];
+    float m[NT][2], l[NT][2];
+    float o[D / 16][NT][4];
+    float pz[NT][2][D / 32];
 };
 
-template <int D, bool TWO>
-__device__ __forceinline__ void online_softmax(DecState<D>& st, float (&x)[2][8], float (&p)[2][8]) {
-#pragma unroll
-    for (int r = 0; r < (TWO ? 2 : 1); ++r) {
-        float mx = x[r][0];
-#pragma unroll
-        for (int k = 1; k < 8; ++k) mx = fmaxf(mx, x[r][k]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        if (mx > st.m[r]) {
-            const float alpha = ex2(st.m[r] - mx);   // 0 when the old max is -inf
-            st.l[r] *= alpha;
-#pragma unroll
-            for (int jj = 0; jj < D / 8; ++jj) {
-                st.o[jj][2 * r] *= alpha;
-                st.o[jj][2 * r + 1] *= alpha;
-            }
-#pragma unroll
-            for (int vg = 0; vg < D / 32; ++vg) st.pz[r][vg] *= alpha;
-            st.m[r] = mx;
-        }
-        const float mu = st.m[r] == -INFINITY ? 0.0f : st.m[r];
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            p[r][k] = ex2(x[r][k] - mu);
-            s += p[r][k];
-        }
-        st.l[r] += s;
-    }
-    if (!TWO) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) p[1][k] = 0.0f;
-    }
+__device__ __forceinline__ float group_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
 }
-
+__device__ __forceinline__ float group_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
 __device__ __forceinline__ float quad_sum(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     return v;
 }
 
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// x[nt][mt][e]: logits (log2 units) of keys 16 mt + g (e = 0, 1) and 16 mt + 8 + g
+// (e = 2, 3) for heads 2 tig + (e & 1) (+ 8 nt).  Updates the running max and sum,
+// returns p in the same layout.
+template <int D, int NT>
+__device__ __forceinline__ void online_softmax(DecState<D, NT>& st, float (&x)[NT][2][4], float (&p)[NT][2][4]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            float mx = fmaxf(fmaxf(x[nt][0][hc], x[nt][0][2 + hc]), fmaxf(x[nt][1][hc], x[nt][1][2 + hc]));
+            mx = group_max(mx);
+            if (mx > st.m[nt][hc]) {
+                const float alpha = ex2(st.m[nt][hc] - mx);   // 0 when the old max is -inf
+                st.l[nt][hc] *= alpha;
+#pragma unroll
+                for (int cm = 0; cm < D / 16; ++cm) {
+                    st.o[cm][nt][hc] *= alpha;
+                    st.o[cm][nt][2 + hc] *= alpha;
+                }
+#pragma unroll
+                for (int vg = 0; vg < D / 32; ++vg) st.pz[nt][hc][vg] *= alpha;
+                st.m[nt][hc] = mx;
+            }
+            const float mu = st.m[nt][hc] == -INFINITY ? 0.0f : st.m[nt][hc];
+            float s = 0.0f;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float v = ex2(x[nt][mt][2 * r + hc] - mu);
+                    p[nt][mt][2 * r + hc] = v;
+                    s += v;
+                }
+            st.l[nt][hc] += s;
+        }
+}
+
 // ---- one quantised block ------------------------------------------------------
-// q[r][4 kk + e]: query of row r at channels 16 kk + 2 tig + {0, 1, 8, 9}.
-template <int D, int BITS, bool TWO, int JENSEN>
+// q[nt][4 kk + e]: query of head g + 8 nt at channels 16 kk + 2 tig + {0, 1, 8, 9}.
+template <int D, int BITS, int NT, int JENSEN>
 __device__ __forceinline__ void int_block(const unsigned char* blk, int len, const LaneConst& lc,
-                                          const float (&q)[2][D / 4], float c1, float tau, DecState<D>& st) {
+                                          const float (&q)[NT][D / 4], float c1, float tau, DecState<D, NT>& st) {
     const IntBlockOffsets o = int_offsets(D, BITS);
-    // A = q o s as an fp16 pair hi + lo (hi = fp16(q s), lo = fp16(q s - hi): the
-    // product keeps ~22 bits, enough for outlier channels with large steps), the
-    // zero-point term q.z and the Jensen sum per row
+    // B = (q o s)^T as an fp16 pair hi + lo (hi = fp16(q s), lo = fp16(q s - hi):
+    // the product keeps ~22 bits, enough for outlier channels with large steps),
+    // the zero-point term q.z and the Jensen sum of head g + 8 nt
     const float4* km4 = reinterpret_cast<const float4*>(blk + o.km);
-    uint32_t aqk[D / 16][4], aql[D / 16][4];
-    float qz[2] = {0.0f, 0.0f}, jd[2] = {0.0f, 0.0f};
+    uint32_t bh[NT][D / 16][2], bl[NT][D / 16][2];
+    float qz[NT], jd[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) qz[nt] = jd[nt] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const float4 A = km4[(16 * kk + 2 * lc.tig) >> 1];
         const float4 Bq = km4[(16 * kk + 8 + 2 * lc.tig) >> 1];
         const float s[4] = {A.x, A.z, Bq.x, Bq.z}, z[4] = {A.y, A.w, Bq.y, Bq.w};
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            if (r == 1 && !TWO) {
-                aqk[kk][1] = aqk[kk][3] = aql[kk][1] = aql[kk][3] = 0u;
-                continue;
-            }
+        for (int nt = 0; nt < NT; ++nt) {
             float qs[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                qs[e] = q[r][4 * kk + e] * s[e];
-                qz[r] = fmaf(q[r][4 * kk + e], z[e], qz[r]);
-                if (JENSEN == KV_JENSEN_TAYLOR2) jd[r] = fmaf(qs[e], qs[e], jd[r]);
-                else if (JENSEN == KV_JENSEN_EXACT) jd[r] += log_sinhc(0.5f * tau * qs[e]);
+                qs[e] = q[nt][4 * kk + e] * s[e];
+                qz[nt] = fmaf(q[nt][4 * kk + e], z[e], qz[nt]);
+                if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs[e], qs[e], jd[nt]);
+                else if (JENSEN == KV_JENSEN_EXACT) jd[nt] += log_sinhc(0.5f * tau * qs[e]);
             }
-            aqk[kk][r] = pack_f16(qs[0], qs[1]);
-            aqk[kk][2 + r] = pack_f16(qs[2], qs[3]);
-            const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&aqk[kk][r]));
-            const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&aqk[kk][2 + r]));
-            aql[kk][r] = pack_f16(qs[0] - h01.x, qs[1] - h01.y);
-            aql[kk][2 + r] = pack_f16(qs[2] - h23.x, qs[3] - h23.y);
+            bh[nt][kk][0] = pack_f16(qs[0], qs[1]);
+            bh[nt][kk][1] = pack_f16(qs[2], qs[3]);
+            const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&bh[nt][kk][0]));
+            const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&bh[nt][kk][1]));
+            bl[nt][kk][0] = pack_f16(qs[0] - h01.x, qs[1] - h01.y);
+            bl[nt][kk][1] = pack_f16(qs[2] - h23.x, qs[3] - h23.y);
         }
     }
-    float bias[2];
+    // bias of head g + 8 nt, then gathered for the fragment's heads 2 tig, 2 tig + 1
+    float bias[NT][2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const float z = quad_sum(qz[r]);
+    for (int nt = 0; nt < NT; ++nt) {
         float dl = 0.0f;
         if (JENSEN != KV_JENSEN_OFF) {
-            dl = quad_sum(jd[r]);
+            dl = quad_sum(jd[nt]);
             if (JENSEN == KV_JENSEN_TAYLOR2) dl *= tau * tau * (1.0f / 24.0f);
         }
-        bias[r] = (tau * z - dl) * kLog2e;
+        const float bq = (tau * quad_sum(qz[nt]) - dl) * kLog2e;
+        bias[nt][0] = __shfl_sync(0xffffffffu, bq, (2 * lc.tig) << 2);
+        bias[nt][1] = __shfl_sync(0xffffffffu, bq, (2 * lc.tig + 1) << 2);
     }
 
-    // S = (q o s) codes^T
+    // S^T = codes (q o s)^T: A = key codes [16 keys x 16 channels] per (mt, kk)
     constexpr int KW = D * BITS / 32;   // code words per key row
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
-    float acc[4][4];
+    float acc[2][NT][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-        uint32_t w[KW];
-        const uint4* src = reinterpret_cast<const uint4*>(kc + (8 * j + lc.g) * KW);
+    for (int mt = 0; mt < 2; ++mt) {
+        uint32_t wa[KW], wb[KW];
+        const uint4* sa = reinterpret_cast<const uint4*>(kc + (16 * mt + lc.g) * KW);
+        const uint4* sb = reinterpret_cast<const uint4*>(kc + (16 * mt + 8 + lc.g) * KW);
 #pragma unroll
         for (int i = 0; i < KW / 4; ++i) {
-            const uint4 v = src[i];
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+            const uint4 va = sa[i], vb = sb[i];
+            wa[4 * i] = va.x; wa[4 * i + 1] = va.y; wa[4 * i + 2] = va.z; wa[4 * i + 3] = va.w;
+            wb[4 * i] = vb.x; wb[4 * i + 1] = vb.y; wb[4 * i + 2] = vb.z; wb[4 * i + 3] = vb.w;
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            uint32_t b0, b1;
+            uint32_t a[4];
             if (BITS == 2) {
-                b0 = code_pair(w[kk], lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
-                b1 = code_pair(w[kk], lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[0] = code_pair(wa[kk], lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[1] = code_pair(wb[kk], lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[2] = code_pair(wa[kk], lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[3] = code_pair(wb[kk], lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
             } else {
-                b0 = code_pair(w[2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
-                b1 = code_pair(w[2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[0] = code_pair(wa[2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[1] = code_pair(wb[2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[2] = code_pair(wa[2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[3] = code_pair(wb[2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
             }
-            mma_f16(acc[j], aqk[kk], b0, b1);
-            mma_f16(acc[j], aql[kk], b0, b1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma_f16(acc[mt][nt], a, bh[nt][kk][0], bh[nt][kk][1]);
+                mma_f16(acc[mt][nt], a, bl[nt][kk][0], bl[nt][kk][1]);
+            }
         }
     }
-    float x[2][8], p[2][8];
+    float x[NT][2][4], p[NT][2][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const bool valid = 8 * j + 2 * lc.tig + e < len;
-            x[0][2 * j + e] = valid ? fmaf(acc[j][e], c1, bias[0]) : -INFINITY;
-            x[1][2 * j + e] = valid ? fmaf(acc[j][2 + e], c1, bias[1]) : -INFINITY;
-        }
-    online_softmax<D, TWO>(st, x, p);
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = 16 * mt + 8 * (e >> 1) + lc.g < len;
+                x[nt][mt][e] = valid ? fmaf(acc[mt][nt][e], c1, bias[nt][e & 1]) : -INFINITY;
+            }
+    online_softmax<D, NT>(st, x, p);
 
-    // A = p o s_v (fp16) per value group, and the zero-point term sum p z_v
-    const float4* vm4 = reinterpret_cast<const float4*>(blk + o.vm);
-    uint32_t apv[D / 32][2][4];
+    // B = (p o s_v) per value group, transposed to [keys x heads] by movmatrix,
+    // and the zero-point term sum p z_v
+    const float2* vm = reinterpret_cast<const float2*>(blk + o.vm);
+    uint32_t bpv[D / 32][NT][2][2];
 #pragma unroll
     for (int vg = 0; vg < D / 32; ++vg)
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const float4 SA = vm4[vg * 16 + ((16 * kk + 2 * lc.tig) >> 1)];
-            const float4 SB = vm4[vg * 16 + ((16 * kk + 8 + 2 * lc.tig) >> 1)];
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                if (r == 1 && !TWO) {
-                    apv[vg][kk][1] = apv[vg][kk][3] = 0u;
-                    continue;
+                const float2 sz = vm[vg * 32 + 16 * mt + 8 * r + lc.g];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float p0 = p[nt][mt][2 * r], p1 = p[nt][mt][2 * r + 1];
+                    bpv[vg][nt][mt][r] = movmatrix_t(pack_f16(p0 * sz.x, p1 * sz.x));
+                    st.pz[nt][0][vg] = fmaf(p0, sz.y, st.pz[nt][0][vg]);
+                    st.pz[nt][1][vg] = fmaf(p1, sz.y, st.pz[nt][1][vg]);
                 }
-                const float pa0 = p[r][4 * kk], pa1 = p[r][4 * kk + 1], pb0 = p[r][4 * kk + 2],
-                            pb1 = p[r][4 * kk + 3];
-                apv[vg][kk][r] = pack_f16(pa0 * SA.x, pa1 * SA.z);
-                apv[vg][kk][2 + r] = pack_f16(pb0 * SB.x, pb1 * SB.z);
-                st.pz[r][vg] = fmaf(pa0, SA.y, fmaf(pa1, SA.w, fmaf(pb0, SB.y, fmaf(pb1, SB.w, st.pz[r][vg]))));
             }
-        }
-    // O += (p o s_v) codes
+    // O^T += value codes [16 channels x 16 keys] (p o s_v)
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc);
 #pragma unroll
-    for (int jj = 0; jj < D / 8; ++jj) {
-        const int ch = 8 * jj + lc.g, vg = jj >> 2;
-        if (BITS == 2) {
-            const uint2 w = *reinterpret_cast<const uint2*>(vc + ch * 2);
-            mma_f16(st.o[jj], apv[vg][0], code_pair(w.x, lc.sel2a, lc.mask2, lc.scale2, lc.bias2),
-                    code_pair(w.x, lc.sel2b, lc.mask2, lc.scale2, lc.bias2));
-            mma_f16(st.o[jj], apv[vg][1], code_pair(w.y, lc.sel2a, lc.mask2, lc.scale2, lc.bias2),
-                    code_pair(w.y, lc.sel2b, lc.mask2, lc.scale2, lc.bias2));
-        } else {
-            const uint4 w = *reinterpret_cast<const uint4*>(vc + ch * 4);
-            mma_f16(st.o[jj], apv[vg][0], code_pair(w.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4),
-                    code_pair(w.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4));
-            mma_f16(st.o[jj], apv[vg][1], code_pair(w.z, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4),
-                    code_pair(w.w, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4));
+    for (int cm = 0; cm < D / 16; ++cm) {
+        const int ca = 16 * cm + lc.g, cb = ca + 8, vg = cm >> 1;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t a[4];
+            if (BITS == 2) {
+                const uint32_t wa = vc[ca * 2 + kk], wb = vc[cb * 2 + kk];
+                a[0] = code_pair(wa, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[1] = code_pair(wb, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[2] = code_pair(wa, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[3] = code_pair(wb, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+            } else {
+                const uint2 wa = *reinterpret_cast<const uint2*>(vc + ca * 4 + 2 * kk);
+                const uint2 wb = *reinterpret_cast<const uint2*>(vc + cb * 4 + 2 * kk);
+                a[0] = code_pair(wa.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[1] = code_pair(wb.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[2] = code_pair(wa.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[3] = code_pair(wb.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(st.o[cm][nt], a, bpv[vg][nt][kk][0], bpv[vg][nt][kk][1]);
         }
     }
 }
 
 // ---- one RAW16 block (16-bit K and V kept as given) ------------------------------
-template <typename T, int D, bool TWO>
+template <typename T, int D, int NT>
 __device__ __forceinline__ void raw_block(uint32_t sblk, int len, const LaneConst& lc,
-                                          const uint32_t (&aq)[D / 16][4], float c1, DecState<D>& st) {
+                                          const uint32_t (&aq)[NT][D / 16][2], float c1, DecState<D, NT>& st) {
     const int lane = threadIdx.x & 31, mat = lane >> 3, rr = lane & 7;
-    float acc[4][4];
+    float acc[2][NT][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-        const int key = 8 * j + rr;
+    for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-        for (int cq = 0; cq < D / 32; ++cq) {
-            const int chunk = 4 * cq + mat;
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(sblk + key * (2 * D) + ((chunk ^ rr) << 4), r0, r1, r2, r3);
-            mma_raw<T>(acc[j], aq[2 * cq], r0, r1);
-            mma_raw<T>(acc[j], aq[2 * cq + 1], r2, r3);
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+        const int key = 16 * mt + 8 * (mat & 1) + rr;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = 2 * kk + (mat >> 1);
+            uint32_t a[4];
+            ldsm_x4(sblk + key * (2 * D) + ((chunk ^ rr) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_raw<T>(acc[mt][nt], a, aq[nt][kk][0], aq[nt][kk][1]);
         }
     }
-    float x[2][8], p[2][8];
+    float x[NT][2][4], p[NT][2][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const bool valid = 8 * j + 2 * lc.tig + e < len;
-            x[0][2 * j + e] = valid ? acc[j][e] * c1 : -INFINITY;
-            x[1][2 * j + e] = valid ? acc[j][2 + e] * c1 : -INFINITY;
-        }
-    online_softmax<D, TWO>(st, x, p);
-    uint32_t apv[2][4];
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-        apv[kk][0] = pack_raw<T>(p[0][4 * kk], p[0][4 * kk + 1]);
-        apv[kk][2] = pack_raw<T>(p[0][4 * kk + 2], p[0][4 * kk + 3]);
-        apv[kk][1] = TWO ? pack_raw<T>(p[1][4 * kk], p[1][4 * kk + 1]) : 0u;
-        apv[kk][3] = TWO ? pack_raw<T>(p[1][4 * kk + 2], p[1][4 * kk + 3]) : 0u;
-    }
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = 16 * mt + 8 * (e >> 1) + lc.g < len;
+                x[nt][mt][e] = valid ? acc[mt][nt][e] * c1 : -INFINITY;
+            }
+    online_softmax<D, NT>(st, x, p);
+    uint32_t bpv[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) bpv[nt][mt][r] = movmatrix_t(pack_raw<T>(p[nt][mt][2 * r], p[nt][mt][2 * r + 1]));
     const uint32_t vbase = sblk + kBlockTokens * D * 2;
-    const int key = 8 * mat + rr;
 #pragma unroll
-    for (int jj = 0; jj < D / 8; ++jj) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(vbase + key * (2 * D) + ((jj ^ rr) << 4), r0, r1, r2, r3);
-        mma_raw<T>(st.o[jj], apv[0], r0, r1);
-        mma_raw<T>(st.o[jj], apv[1], r2, r3);
-    }
+    for (int cm = 0; cm < D / 16; ++cm)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const int key = 16 * kk + 8 * (mat >> 1) + rr, chunk = 2 * cm + (mat & 1);
+            uint32_t a[4];
+            ldsm_x4_t(vbase + key * (2 * D) + ((chunk ^ rr) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_raw<T>(st.o[cm][nt], a, bpv[nt][kk][0], bpv[nt][kk][1]);
+        }
 }
 
 // ---- one unquantised current token, on CUDA cores --------------------------------
-template <typename T, int D, bool TWO>
+template <typename T, int D, int NT>
 __device__ __forceinline__ void current_token(const T* kr, const T* vr, const LaneConst& lc,
-                                              const float (&q)[2][D / 4], float c1, DecState<D>& st) {
-    float dot[2] = {0.0f, 0.0f};
+                                              const float (&q)[NT][D / 4], float c1, DecState<D, NT>& st) {
+    float x[NT][2][4], p[NT][2][4];
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const float2 ka = pair_to_f32<T>(*reinterpret_cast<const uint32_t*>(kr + 16 * kk + 2 * lc.tig));
-        const float2 kb = pair_to_f32<T>(*reinterpret_cast<const uint32_t*>(kr + 16 * kk + 8 + 2 * lc.tig));
+    for (int nt = 0; nt < NT; ++nt) {
+        float dot = 0.0f;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            dot[r] = fmaf(q[r][4 * kk], ka.x, dot[r]);
-            dot[r] = fmaf(q[r][4 * kk + 1], ka.y, dot[r]);
-            dot[r] = fmaf(q[r][4 * kk + 2], kb.x, dot[r]);
-            dot[r] = fmaf(q[r][4 * kk + 3], kb.y, dot[r]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const float2 ka = pair_to_f32<T>(*reinterpret_cast<const uint32_t*>(kr + 16 * kk + 2 * lc.tig));
+            const float2 kb = pair_to_f32<T>(*reinterpret_cast<const uint32_t*>(kr + 16 * kk + 8 + 2 * lc.tig));
+            dot = fmaf(q[nt][4 * kk], ka.x, dot);
+            dot = fmaf(q[nt][4 * kk + 1], ka.y, dot);
+            dot = fmaf(q[nt][4 * kk + 2], kb.x, dot);
+            dot = fmaf(q[nt][4 * kk + 3], kb.y, dot);
+        }
+        const float s = quad_sum(dot) * c1;    // head g + 8 nt, in every lane of the quad
+        const float s0 = __shfl_sync(0xffffffffu, s, (2 * lc.tig) << 2);
+        const float s1 = __shfl_sync(0xffffffffu, s, (2 * lc.tig + 1) << 2);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[nt][mt][e] = -INFINITY;
+        if (lc.g == 0) {           // the token sits in key slot 0 of the lane group g = 0
+            x[nt][0][0] = s0;
+            x[nt][0][1] = s1;
         }
     }
-    float x[2][8], p[2][8];
+    online_softmax<D, NT>(st, x, p);
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const float s = quad_sum(dot[r]) * c1;
+    for (int nt = 0; nt < NT; ++nt) {
+        const float p0 = __shfl_sync(0xffffffffu, p[nt][0][0], lc.tig);
+        const float p1 = __shfl_sync(0xffffffffu, p[nt][0][1], lc.tig);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[r][k] = (k == 0 && lc.tig == 0) ? s : -INFINITY;
-    }
-    online_softmax<D, TWO>(st, x, p);
-    float pr[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) pr[r] = __shfl_sync(0xffffffffu, p[r][0], (threadIdx.x & 31) & ~3);
-#pragma unroll
-    for (int jj = 0; jj < D / 8; ++jj) {
-        const float2 v = pair_to_f32<T>(*reinterpret_cast<const uint32_t*>(vr + 8 * jj + 2 * lc.tig));
-        st.o[jj][0] = fmaf(pr[0], v.x, st.o[jj][0]);
-        st.o[jj][1] = fmaf(pr[0], v.y, st.o[jj][1]);
-        if (TWO) {
-            st.o[jj][2] = fmaf(pr[1], v.x, st.o[jj][2]);
-            st.o[jj][3] = fmaf(pr[1], v.y, st.o[jj][3]);
+        for (int cm = 0; cm < D / 16; ++cm) {
+            const float va = to_f32<T>(vr[16 * cm + lc.g]), vb = to_f32<T>(vr[16 * cm + 8 + lc.g]);
+            st.o[cm][nt][0] = fmaf(p0, va, st.o[cm][nt][0]);
+            st.o[cm][nt][1] = fmaf(p1, va, st.o[cm][nt][1]);
+            st.o[cm][nt][2] = fmaf(p0, vb, st.o[cm][nt][2]);
+            st.o[cm][nt][3] = fmaf(p1, vb, st.o[cm][nt][3]);
         }
     }
 }
 
-// First block of split s of a stream whose blocks (segment-major, RAW16, INT4,
-// INT2) are cut into `S` ranges of about equal bytes: the smallest block index
-// i with S * (bytes before i) >= s * (total bytes).
-__device__ int split_begin(const DevCache& c, int s, int S) {
-    long long total = 0;
-#pragma unroll
-    for (int k = 0; k < KV_NUM_SEG; ++k) total += (long long)c.n_blocks[k] * c.block_bytes[k];
-    const long long target = (long long)s * total;
-    long long before = 0;
-    int base = 0;
-#pragma unroll
-    for (int k = 0; k < KV_NUM_SEG; ++k) {
-        const int n = c.n_blocks[k];
-        const long long bb = c.block_bytes[k];
-        if (n > 0 && (long long)S * (before + (long long)(n - 1) * bb) >= target) {
-            const long long num = target - (long long)S * before;
-            const long long j = num <= 0 ? 0 : (num + (long long)S * bb - 1) / ((long long)S * bb);
-            return base + (int)j;
-        }
-        before += (long long)n * bb;
-        base += n;
-    }
-    return base;
+// First block of split s of a stream of nb blocks (segment-major: RAW16, INT4,
+// INT2) cut into S ranges of equal block counts.  A block's cost is about the
+// same in every class once both its bytes and its instructions are counted (an
+// 8 KB RAW16 block streams 4x the bytes of a 2 KB INT2 block but issues about a
+// third of its instructions), so equal counts balance the splits.
+__device__ __forceinline__ int split_begin(const DevCache& c, int s, int S) {
+    const long long nb = (long long)c.n_blocks[0] + c.n_blocks[1] + c.n_blocks[2];
+    return (int)((long long)s * nb / S);
 }
 
 struct DecShape {
@@ -437,8 +461,8 @@ struct DecShape {
     int rows;         // merge rows per warp (8 or 16)
 };
 
-template <typename T, int D, bool TWO, int JENSEN>
-__global__ void __launch_bounds__(kDThreads, D == 64 ? 3 : 1)
+template <typename T, int D, int NT, int JENSEN>
+__global__ void __launch_bounds__(kDThreads, (D == 64 && NT == 1) ? 4 : ((D == 128 && NT == 2) ? 1 : 2))
 attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* __restrict__ Vcur, int n_cur, int Hq,
                    DevCache c, float tau, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
                    float* __restrict__ lse, float* __restrict__ part, int* __restrict__ tickets, int* __restrict__ err) {
@@ -464,36 +488,40 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     mbar_fence_init();
     __syncthreads();
 
-    // queries: fp32 copies for quantised blocks, 16-bit A fragments for RAW16 blocks
-    float q[2][D / 4];
-    uint32_t aq[D / 16][4];
+    // queries of head g + 8 nt: fp32 copies for quantised blocks, 16-bit B fragments
+    // (channel pairs 2 tig, 8 + 2 tig of each k-step) for RAW16 blocks
+    float q[NT][D / 4];
+    uint32_t aq[NT][D / 16][2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int hr = lc.g + 8 * r;
-        const bool ok = hr < G && (r == 0 || TWO);
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hr = lc.g + 8 * nt;
+        const bool ok = hr < G;
         const T* qrow = Q + ((long long)b * Hq + (long long)h * G + (ok ? hr : 0)) * D;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t wa = ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * lc.tig) : 0u;
             const uint32_t wb = ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * lc.tig) : 0u;
             const float2 fa = pair_to_f32<T>(wa), fb = pair_to_f32<T>(wb);
-            q[r][4 * kk] = fa.x;
-            q[r][4 * kk + 1] = fa.y;
-            q[r][4 * kk + 2] = fb.x;
-            q[r][4 * kk + 3] = fb.y;
-            aq[kk][r] = wa;
-            aq[kk][2 + r] = wb;
+            q[nt][4 * kk] = fa.x;
+            q[nt][4 * kk + 1] = fa.y;
+            q[nt][4 * kk + 2] = fb.x;
+            q[nt][4 * kk + 3] = fb.y;
+            aq[nt][kk][0] = wa;
+            aq[nt][kk][1] = wb;
         }
     }
     const float c1 = tau * kLog2e;
 
-    DecState<D> st;
-    st.m[0] = st.m[1] = -INFINITY;
-    st.l[0] = st.l[1] = 0.0f;
+    DecState<D, NT> st;
 #pragma unroll
-    for (int jj = 0; jj < D / 8; ++jj) st.o[jj][0] = st.o[jj][1] = st.o[jj][2] = st.o[jj][3] = 0.0f;
+    for (int nt = 0; nt < NT; ++nt) {
+        st.m[nt][0] = st.m[nt][1] = -INFINITY;
+        st.l[nt][0] = st.l[nt][1] = 0.0f;
 #pragma unroll
-    for (int vg = 0; vg < D / 32; ++vg) st.pz[0][vg] = st.pz[1][vg] = 0.0f;
+        for (int cm = 0; cm < D / 16; ++cm) st.o[cm][nt][0] = st.o[cm][nt][1] = st.o[cm][nt][2] = st.o[cm][nt][3] = 0.0f;
+#pragma unroll
+        for (int vg = 0; vg < D / 32; ++vg) st.pz[nt][0][vg] = st.pz[nt][1][vg] = 0.0f;
+    }
 
     // this warp's blocks: lo + warp, lo + warp + kDW, ... below hi
     const int lo = split_begin(c, split, n_splits), hi = split_begin(c, split + 1, n_splits);
@@ -533,9 +561,9 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
         const int len = __shfl_sync(0xffffffffu, len_next, k & 31);
         const unsigned char* blk = slots + (warp * nsw + k % nsw) * slot_bytes;
         const int cls = seg_class(c.kind, seg);
-        if (cls == CLS_INT2) int_block<D, 2, TWO, JENSEN>(blk, len, lc, q, c1, tau, st);
-        else if (cls == CLS_INT4) int_block<D, 4, TWO, JENSEN>(blk, len, lc, q, c1, tau, st);
-        else raw_block<T, D, TWO>(smem_u32(blk), len, lc, aq, c1, st);
+        if (cls == CLS_INT2) int_block<D, 2, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
+        else if (cls == CLS_INT4) int_block<D, 4, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
+        else raw_block<T, D, NT>(smem_u32(blk), len, lc, aq, c1, st);
         __syncwarp();
         if (lane == 0 && k + nsw < nw) issue(k + nsw);
     }
@@ -553,37 +581,43 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     if (split == n_splits - 1 && !abort_flag) {
         const long long rbase = (long long)stream * n_cur;
         for (int t = warp; t < n_cur; t += kDW)
-            current_token<T, D, TWO>(Kcur + (rbase + t) * D, Vcur + (rbase + t) * D, lc, q, c1, st);
+            current_token<T, D, NT>(Kcur + (rbase + t) * D, Vcur + (rbase + t) * D, lc, q, c1, st);
     }
 
-    // finish the lane partial sums and fold the value zero-point term into o
+    // finish the lane partial sums (over the 8 lane groups) and fold the value
+    // zero-point term into o
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        st.l[r] = quad_sum(st.l[r]);
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int vg = 0; vg < D / 32; ++vg) st.pz[r][vg] = quad_sum(st.pz[r][vg]);
-    }
+        for (int hc = 0; hc < 2; ++hc) {
+            st.l[nt][hc] = group_sum(st.l[nt][hc]);
 #pragma unroll
-    for (int jj = 0; jj < D / 8; ++jj)
+            for (int vg = 0; vg < D / 32; ++vg) st.pz[nt][hc][vg] = group_sum(st.pz[nt][hc][vg]);
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) st.o[jj][e] += st.pz[e >> 1][jj >> 2];
+    for (int cm = 0; cm < D / 16; ++cm)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st.o[cm][nt][e] += st.pz[nt][e & 1][cm >> 1];
 
-    // warps -> CTA through shared memory: row layout [m, l, o[0..D)]
+    // warps -> CTA through shared memory: row (head) layout [m, l, o[0..D)]
     const int rows = sh.rows;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        if (r == 1 && !TWO) break;
-        float* row = mrg + ((warp * rows) + lc.g + 8 * r) * (D + 2);
-        if (lc.tig == 0) {
-            row[0] = st.m[r];
-            row[1] = st.l[r];
-        }
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int jj = 0; jj < D / 8; ++jj) {
-            row[2 + 8 * jj + 2 * lc.tig] = st.o[jj][2 * r];
-            row[2 + 8 * jj + 2 * lc.tig + 1] = st.o[jj][2 * r + 1];
+        for (int hc = 0; hc < 2; ++hc) {
+            float* row = mrg + ((warp * rows) + 2 * lc.tig + hc + 8 * nt) * (D + 2);
+            if (lc.g == 0) {
+                row[0] = st.m[nt][hc];
+                row[1] = st.l[nt][hc];
+            }
+#pragma unroll
+            for (int cm = 0; cm < D / 16; ++cm) {
+                row[2 + 16 * cm + lc.g] = st.o[cm][nt][hc];
+                row[2 + 16 * cm + 8 + lc.g] = st.o[cm][nt][2 + hc];
+            }
         }
-    }
     __syncthreads();
     const long long rows_out = (long long)c.B * Hq;
     for (int e = tid; e < G * D; e += kDThreads) {
@@ -673,7 +707,7 @@ DecShape dec_shape(const kv_cache* cache, int Hq) {
     sh.slot_bytes = (int)((slot + 127) / 128 * 128);
     int nsw = (int)(64 * 1024 / (kDW * (long long)sh.slot_bytes));
     sh.nsw = nsw < 2 ? 2 : (nsw > 8 ? 8 : nsw);
-    sh.rows = Hq / L.Hkv > 8 ? 16 : 8;
+    sh.rows = Hq / L.Hkv > 8 ? 16 : 8;   // heads per warp row block: 8 NT
     return sh;
 }
 
@@ -686,7 +720,7 @@ size_t dec_ticket_bytes(const kv_cache* cache) {
     return ((size_t)cache->layout.B * cache->layout.Hkv * sizeof(int) + 255) / 256 * 256;
 }
 
-template <typename T, int D, bool TWO, int JENSEN>
+template <typename T, int D, int NT, int JENSEN>
 kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur, int Hq, const kv_cache* cache,
                        float tau, int n_splits, void* out, int out_f32, float* lse, void* ws, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
@@ -695,7 +729,7 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     static size_t attr_bytes = 0;
     if (smem > attr_bytes) {
         const cudaError_t e =
-            cudaFuncSetAttribute(attn_decode_kernel<T, D, TWO, JENSEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(attn_decode_kernel<T, D, NT, JENSEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return set_error(KV_ERR_CUDA, "attn_decode_kernel: %zu bytes of shared memory: %s", smem,
                              cudaGetErrorString(e));
@@ -707,7 +741,7 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     float* part = reinterpret_cast<float*>(w + 256 + dec_ticket_bytes(cache));
     cudaMemsetAsync(w, 0, 256 + dec_ticket_bytes(cache), st);
     dim3 grid(n_splits, c.Hkv, c.B);
-    attn_decode_kernel<T, D, TWO, JENSEN><<<grid, kDThreads, smem, st>>>(
+    attn_decode_kernel<T, D, NT, JENSEN><<<grid, kDThreads, smem, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
         sh, out, out_f32, lse, part, tickets, err);
     kv_status s = check_launch("attn_decode_kernel");
@@ -762,23 +796,23 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
     const bool two = Hq / cache->layout.Hkv > 8;
     using F16 = __half;
     using BF16 = __nv_bfloat16;
-#define BITKV_DEC(T, D, TWO)                                                                                    \
+#define BITKV_DEC(T, D, NT)                                                                                    \
     do {                                                                                                        \
         if (jensen == KV_JENSEN_TAYLOR2)                                                                        \
-            return launch_dec_t<T, D, TWO, KV_JENSEN_TAYLOR2>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,  \
+            return launch_dec_t<T, D, NT, KV_JENSEN_TAYLOR2>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,  \
                                                               out_f32, lse, ws, st);                            \
         if (jensen == KV_JENSEN_EXACT)                                                                          \
-            return launch_dec_t<T, D, TWO, KV_JENSEN_EXACT>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
+            return launch_dec_t<T, D, NT, KV_JENSEN_EXACT>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
                                                             out_f32, lse, ws, st);                              \
-        return launch_dec_t<T, D, TWO, KV_JENSEN_OFF>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out, out_f32, \
+        return launch_dec_t<T, D, NT, KV_JENSEN_OFF>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out, out_f32, \
                                                       lse, ws, st);                                             \
     } while (0)
     if (dt == KV_F16) {
-        if (d == 64) { if (two) BITKV_DEC(F16, 64, true); else BITKV_DEC(F16, 64, false); }
-        else { if (two) BITKV_DEC(F16, 128, true); else BITKV_DEC(F16, 128, false); }
+        if (d == 64) { if (two) BITKV_DEC(F16, 64, 2); else BITKV_DEC(F16, 64, 1); }
+        else { if (two) BITKV_DEC(F16, 128, 2); else BITKV_DEC(F16, 128, 1); }
     } else {
-        if (d == 64) { if (two) BITKV_DEC(BF16, 64, true); else BITKV_DEC(BF16, 64, false); }
-        else { if (two) BITKV_DEC(BF16, 128, true); else BITKV_DEC(BF16, 128, false); }
+        if (d == 64) { if (two) BITKV_DEC(BF16, 64, 2); else BITKV_DEC(BF16, 64, 1); }
+        else { if (two) BITKV_DEC(BF16, 128, 2); else BITKV_DEC(BF16, 128, 1); }
     }
 #undef BITKV_DEC
 }
