@@ -112,11 +112,20 @@ __device__ __forceinline__ uint32_t sw_off(int row, int ch, int rows = kM) {
 // 2^e for an integer e in [-126, 127] (exact).
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// The b-bit code at bits [b i, b i + b) of x as the exact float c 2^(b i) (b i + b <= 23).
+// The b-bit code at bits [b i, b i + b) of x as 2^23 + c 2^(b i) (b i + b <= 23): the
+// code or-ed into the mantissa of 2^23.
 template <int BITS>
-__device__ __forceinline__ float code_scaled(uint32_t x, int i) {
-    const uint32_t m = x & (((1u << BITS) - 1u) << (BITS * i));
-    return __uint_as_float(0x4B000000u | m) - 8388608.0f;
+__device__ __forceinline__ float code_magic(uint32_t x, int i) {
+    return __uint_as_float(0x4B000000u | (x & (((1u << BITS) - 1u) << (BITS * i))));
+}
+
+// Two dequantised entries fmaf(c 2^(b i), s 2^(-b i), z) from their magic floats:
+// the subtraction of 2^23 is exact, the FMA rounds once.
+__device__ __forceinline__ void dequant2(float& v0, float& v1, float m0, float m1, float s0, float s1, float z0,
+                                         float z1) {
+    float f0, f1;
+    add2(f0, f1, m0, m1, -8388608.0f, -8388608.0f);
+    fma2(v0, v1, f0, f1, s0, s1, z0, z1);
 }
 
 // ------------------------------------------------------------- producers ----
@@ -137,26 +146,29 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* sm, int stage, 
         const int q = 2 * (pw >> 2) + bb;
         if (q < nb) {
             unsigned char* blk = stg + q * block_bytes<BITS>();
-            float2* vm = reinterpret_cast<float2*>(blk + o.vm) + g * 32;
-            float2 e = vm[lane];
-            e.x *= pow2i(-BITS * (lane % kSlots));
-            vm[lane] = e;
+            float* vm = reinterpret_cast<float*>(blk + o.vm) + g * 64;
+            // token t's (s, z) -> (s 2^(-b slot), z), stored per token pair as
+            // (s'_t, s'_t+1, z_t, z_t+1) so that pairs load into adjacent registers
+            const float2 e = reinterpret_cast<const float2*>(vm)[lane];
+            __syncwarp();
+            vm[4 * (lane >> 1) + (lane & 1)] = e.x * pow2i(-BITS * (lane % kSlots));
+            vm[4 * (lane >> 1) + 2 + (lane & 1)] = e.y;
             __syncwarp();
             const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc) + c * BITS;
             uint32_t w[BITS];
 #pragma unroll
             for (int k = 0; k < BITS; ++k) w[k] = vc[k];
-            const float4* sz = reinterpret_cast<const float4*>(vm);   // (s'_t, z_t, s'_t+1, z_t+1)
+            const float4* sz = reinterpret_cast<const float4*>(vm);
 #pragma unroll
             for (int k8 = 0; k8 < 4; ++k8) {         // tokens 8 k8 .. 8 k8 + 7
                 float v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 8; i += 2) {
                     const int t = 8 * k8 + i;
                     const uint32_t x = BITS == 2 ? (w[t >> 4] >> (16 * ((t >> 3) & 1))) : (w[t >> 3] >> (16 * ((t >> 2) & 1)));
                     const float4 p = sz[t >> 1];
-                    const float sp = (t & 1) ? p.z : p.x, zp = (t & 1) ? p.w : p.y;
-                    v[i] = fmaf(code_scaled<BITS>(x, t % kSlots), sp, zp);
+                    dequant2(v[i], v[i + 1], code_magic<BITS>(x, t % kSlots), code_magic<BITS>(x, (t + 1) % kSlots),
+                             p.x, p.y, p.z, p.w);
                 }
                 uint4 r;
                 r.x = pack_f16(v[0], v[1]);
@@ -207,11 +219,16 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* sm, const unsigne
         if (BITS == 2) {
             const uint32_t x = kc[t * KW + (jc >> 1)] >> (16 * (jc & 1));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = fmaf(code_scaled<2>(x, i), s[i], z[i]);
+            for (int i = 0; i < 8; i += 2)
+                dequant2(v[i], v[i + 1], code_magic<2>(x, i), code_magic<2>(x, i + 1), s[i], s[i + 1], z[i], z[i + 1]);
         } else {
             const uint32_t w = kc[t * KW + jc];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = fmaf(code_scaled<4>(i < 4 ? w : (w >> 16), i & 3), s[i], z[i]);
+            for (int i = 0; i < 8; i += 2) {
+                const uint32_t x = i < 4 ? w : (w >> 16);
+                dequant2(v[i], v[i + 1], code_magic<4>(x, i & 3), code_magic<4>(x, (i + 1) & 3), s[i], s[i + 1], z[i],
+                         z[i + 1]);
+            }
         }
         uint4 rr;
         rr.x = pack_bf16(v[0], v[1]);
@@ -401,24 +418,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t sQ2h = sbase + kQ2hOff, sQ2l = sbase + kQ2lOff, sK = sbase + kKOff;
-            auto issue_pv = [&](int jj) -> bool {
-                if (!mbar_wait(bar(BAR_P_FULL), jj & 1, &abort_flag, err, 3)) return false;
-                fence_after();
-                const uint32_t sV = sbase + kVOff + (jj & 1) * kTile;
-#pragma unroll
-                for (int kk = 0; kk < kN / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-                    mma_f16kind_ts(tmem + kColO, tmem + kColS + (jj & 1) * kN + 8 * kk, desc_sw128(sV + off), kIdescPV,
-                                   (jj > 0 || kk > 0));
-                }
-                mma_commit(bar(BAR_O_DONE));
-                mma_commit(bar(BAR_V_EMPTY + (jj & 1)));
-                return true;
-            };
-            bool ok = true;
-            for (int j = 0; j < T && ok; ++j) {
+            auto issue_qk = [&](int j) {
                 const int s = j & 1;
-                if (!mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 1)) break;
                 fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
@@ -438,9 +439,45 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 }
                 mma_commit(bar(BAR_S_FULL + s));
                 mma_commit(bar(BAR_K_EMPTY));
-                if (j > 0) ok = issue_pv(j - 1);
+            };
+            auto issue_pv = [&](int jj) {
+                fence_after();
+                const uint32_t sV = sbase + kVOff + (jj & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
+                    mma_f16kind_ts(tmem + kColO, tmem + kColS + (jj & 1) * kN + 8 * kk, desc_sw128(sV + off), kIdescPV,
+                                   (jj > 0 || kk > 0));
+                }
+                mma_commit(bar(BAR_O_DONE));
+                mma_commit(bar(BAR_V_EMPTY + (jj & 1)));
+            };
+            // Issue Q K^T of tile j as soon as its operands are staged and P V of
+            // tile i as soon as its P is written, whichever is ready first (P V of a
+            // tile frees the V stage the producers refill next).  Q K^T of tile j
+            // reuses tile j - 2's S columns, so it waits for P V of tile j - 2 to be
+            // issued.  The wait is bounded: no progress for ~2^30 cycles gives up.
+            int nq = 0, np = 0;
+            long long t_prog = clock64();
+            while (np < T) {
+                bool progressed = false;
+                if (np < nq && mbar_try_wait(bar(BAR_P_FULL), np & 1)) {
+                    issue_pv(np++);
+                    progressed = true;
+                } else if (nq < T && nq <= np + 1 && mbar_try_wait(bar(BAR_KV_FULL + (nq & 1)), (nq >> 1) & 1)) {
+                    issue_qk(nq++);
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_prog = clock64();
+                } else if (abort_flag) {
+                    break;
+                } else if (clock64() - t_prog > 1000000000LL) {
+                    abort_flag = 1;
+                    atomicExch(err, 1);
+                    break;
+                }
             }
-            if (ok && T > 0 && !abort_flag) issue_pv(T - 1);
         }
         __syncwarp();
     } else if (warp >= kSoftWarps) {
@@ -568,7 +605,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 float mx = -INFINITY;
                 if (nv == 32) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, x[k]);
+                    for (int k = 0; k < 32; k += 2) mx = fmax3(mx, x[k], x[k + 1]);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) mx = fmaxf(mx, k < nv ? x[k] : -INFINITY);
@@ -607,12 +644,25 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 tmem_ld32(tmem + lane_addr + kColS + s * kN + 32 * g, x);
                 const float bg = m_use + dl[g];
                 uint32_t u[16];
+                if (nv == 32) {
+                    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float p0 = 2 * k < nv ? ex2(fmaf(x[2 * k], c1, -bg)) : 0.0f;
-                    const float p1 = 2 * k + 1 < nv ? ex2(fmaf(x[2 * k + 1], c1, -bg)) : 0.0f;
-                    psum += p0 + p1;
-                    u[k] = pack_f16(p0, p1);
+                    for (int k = 0; k < 16; ++k) {
+                        float e0, e1;
+                        fma2(e0, e1, x[2 * k], x[2 * k + 1], c1, c1, -bg, -bg);
+                        const float p0 = ex2(e0), p1 = ex2(e1);
+                        add2(a0, a1, a0, a1, p0, p1);
+                        u[k] = pack_f16(p0, p1);
+                    }
+                    psum += a0 + a1;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float p0 = 2 * k < nv ? ex2(fmaf(x[2 * k], c1, -bg)) : 0.0f;
+                        const float p1 = 2 * k + 1 < nv ? ex2(fmaf(x[2 * k + 1], c1, -bg)) : 0.0f;
+                        psum += p0 + p1;
+                        u[k] = pack_f16(p0, p1);
+                    }
                 }
                 tmem_st16(tmem + lane_addr + kColS + s * kN + 16 * g, u);
             }
