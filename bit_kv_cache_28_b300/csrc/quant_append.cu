@@ -8,10 +8,10 @@
 // codebook key indices plus PSAC coefficients.
 //
 // One CTA packs one 32-token block of one (batch, kv head): the block's key
-// and value rows are staged in shared memory as fp32, keys are quantised per
-// channel (one thread per channel), values per token and 32-channel group (one
-// warp per group, warp-shuffle min/max), and the codes are packed from a byte
-// scratch array into the block's words.
+// and value rows are staged in shared memory as fp32; each key channel and each
+// (token, 32-channel value group) is reduced by 256/d adjacent threads with
+// shuffle min/max, the codes go to byte scratch arrays, and one thread per
+// output word packs them.
 #include <cstdio>
 
 #include "common.cuh"
@@ -21,6 +21,32 @@ namespace bitkv {
 namespace {
 
 constexpr int kAppendThreads = 256;
+
+// 16 bytes of the input dtype as fp32 values (8 for 16-bit types, 4 for fp32).
+template <typename T> __device__ __forceinline__ void widen16(uint4 v, float* out);
+template <> __device__ __forceinline__ void widen16<float>(uint4 v, float* out) {
+    out[0] = __uint_as_float(v.x);
+    out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z);
+    out[3] = __uint_as_float(v.w);
+}
+template <> __device__ __forceinline__ void widen16<__nv_bfloat16>(uint4 v, float* out) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        out[2 * k] = __uint_as_float(w[k] << 16);
+        out[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+template <> __device__ __forceinline__ void widen16<__half>(uint4 v, float* out) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        out[2 * k] = f.x;
+        out[2 * k + 1] = f.y;
+    }
+}
 
 __device__ __forceinline__ void step_and_zero(float mn, float mx, float qmax, float& s, float& z) {
     z = __fadd_rn(mn, 0.0f);                         // -0.0 -> +0.0
@@ -83,31 +109,100 @@ __device__ void pack_keys(const uint8_t* codes, int d, uint32_t* kcw) {
     }
 }
 
+// Code of d = fl32(x - z) for step s with inverse r = 1/s (rounded): rint(fl32(d / s)),
+// clamped.  fl32(d * r) lies within 3 * 2^-24 |d / s| of fl32(d / s) (both quotients
+// carry at most two roundings of 2^-24), so the two round to the same integer
+// unless one sits within 4e-6 of a half-integer; there the IEEE division decides.
+__device__ __forceinline__ uint32_t code_fast(float x, float s, float r, float z, float qmax) {
+    if (!(s > 0.0f)) return 0u;
+    const float d = __fsub_rn(x, z);
+    float q = __fmul_rn(d, r);
+    const float fr = q - floorf(q);
+    if (fabsf(fr - 0.5f) < 4e-6f || !(r < INFINITY)) q = __fdiv_rn(d, s);
+    return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), qmax));
+}
+
+// One uniform INT block.  Keys: channel c is shared by tpc = 256 / d adjacent
+// threads, each taking 32 / tpc tokens; min / max are combined by shuffles.
+// Values: (token t, 32-channel group g) is shared by tpc threads the same way.
+// Codes go to byte arrays kc8[t][c] and vc8[c][t]; one thread per output word
+// packs them.
 template <int BITS>
-__device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d, int nv, uint8_t* codes,
-                                 unsigned char* blk) {
+__device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d, int nv, uint8_t* kc8,
+                                 uint8_t* vc8, unsigned char* blk) {
     const float qmax = float((1 << BITS) - 1);
     const IntBlockOffsets o = int_offsets(d, BITS);
-    float2* km = reinterpret_cast<float2*>(blk + o.km);
-    for (int ch = threadIdx.x; ch < d; ch += blockDim.x) {
+    const int tid = threadIdx.x;
+    const int tpc = kAppendThreads / d;           // 1, 2, 4 or 8 threads per group
+    const int span = kBlockTokens / tpc;          // elements per thread
+    const int part = tid % tpc;
+    // keys: per channel over the block's valid tokens
+    {
+        const int ch = tid / tpc, t0 = part * span;
         float mn = INFINITY, mx = -INFINITY;
-        for (int t = 0; t < nv; ++t) {
-            const float x = Ks[t * ld + ch];
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
+        for (int i = 0; i < span; ++i) {
+            const int t = t0 + i;
+            if (t < nv) {
+                const float x = Ks[t * ld + ch];
+                mn = fminf(mn, x);
+                mx = fmaxf(mx, x);
+            }
+        }
+        for (int w = 1; w < tpc; w <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, w));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
         }
         float s = 0.0f, z = 0.0f;
         if (nv > 0) step_and_zero(mn, mx, qmax, s, z);
-        km[ch] = make_float2(s, z);
-        for (int t = 0; t < kBlockTokens; ++t)
-            codes[t * d + ch] = t < nv ? static_cast<uint8_t>(code_of(Ks[t * ld + ch], s, z, qmax)) : 0;
+        const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+        if (part == 0) reinterpret_cast<float2*>(blk + o.km)[ch] = make_float2(s, z);
+        for (int i = 0; i < span; ++i) {
+            const int t = t0 + i;
+            kc8[t * d + ch] = t < nv ? static_cast<uint8_t>(code_fast(Ks[t * ld + ch], s, r, z, qmax)) : 0;
+        }
+    }
+    // values: per (token, 32-channel group); pair index = t * (d / 32) + g
+    {
+        const int ng = d / 32, pr = tid / tpc;
+        const int t = pr / ng, g = pr % ng, c0 = g * 32 + part * span;
+        float mn = INFINITY, mx = -INFINITY;
+        if (t < nv)
+            for (int i = 0; i < span; ++i) {
+                const float x = Vs[t * ld + c0 + i];
+                mn = fminf(mn, x);
+                mx = fmaxf(mx, x);
+            }
+        for (int w = 1; w < tpc; w <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, w));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
+        }
+        float s = 0.0f, z = 0.0f;
+        if (t < nv) step_and_zero(mn, mx, qmax, s, z);
+        const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+        if (part == 0) reinterpret_cast<float2*>(blk + o.vm)[g * 32 + t] = make_float2(s, z);
+        for (int i = 0; i < span; ++i)
+            vc8[(c0 + i) * kBlockTokens + t] =
+                t < nv ? static_cast<uint8_t>(code_fast(Vs[t * ld + c0 + i], s, r, z, qmax)) : 0;
     }
     __syncthreads();
-    pack_keys<BITS>(codes, d, reinterpret_cast<uint32_t*>(blk + o.kc));
-    __syncthreads();
-    quantise_values<BITS>(Vs, ld, d, nv, codes, reinterpret_cast<float2*>(blk + o.vm));
-    __syncthreads();
-    pack_values<BITS>(codes, d, reinterpret_cast<uint32_t*>(blk + o.vc));
+    // pack: key word (t, q) holds channels q per .. q per + per - 1 of token t;
+    // value word (c, q) holds tokens q per .. of channel c (per = 32 / BITS)
+    constexpr int per = 32 / BITS;
+    uint32_t* kw = reinterpret_cast<uint32_t*>(blk + o.kc);
+    uint32_t* vw = reinterpret_cast<uint32_t*>(blk + o.vc);
+    const int nwords = kBlockTokens * d / per;    // same count for keys and values
+    for (int w = tid; w < nwords; w += kAppendThreads) {
+        const uint8_t* ksrc = kc8 + w * per;        // token-major bytes: word w covers bytes w per ..
+        const uint8_t* vsrc = vc8 + w * per;        // channel-major bytes, likewise
+        uint32_t a = 0, bq = 0;
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+            a |= uint32_t(ksrc[i]) << (BITS * i);
+            bq |= uint32_t(vsrc[i]) << (BITS * i);
+        }
+        kw[w] = a;
+        vw[w] = bq;
+    }
 }
 
 // Codebook block: nearest fp32 centroid per key entry (fp64 |x - mu|, ties to
@@ -198,16 +293,29 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, De
             rk[kBlockTokens * nch + dst] = t < nv ? Vb[e] : make_uint4(0, 0, 0, 0);
         }
     } else {
-        for (int e = threadIdx.x; e < kBlockTokens * d; e += blockDim.x) {
-            const int t = e / d, ch = e % d;
-            Ks[t * ld + ch] = t < nv ? to_f32<T>(K[row0 + e]) : 0.0f;
-            Vs[t * ld + ch] = t < nv ? to_f32<T>(V[row0 + e]) : 0.0f;
+        // 16-byte vector loads of the block's rows, widened to fp32
+        constexpr int VE = 16 / (int)sizeof(T);
+        for (int e = threadIdx.x; e < kBlockTokens * d / VE; e += blockDim.x) {
+            const int t = (e * VE) / d, ch = (e * VE) % d;
+            float kf[VE], vf[VE];
+            if (t < nv) {
+                widen16<T>(*reinterpret_cast<const uint4*>(K + row0 + (long long)e * VE), kf);
+                widen16<T>(*reinterpret_cast<const uint4*>(V + row0 + (long long)e * VE), vf);
+            } else {
+#pragma unroll
+                for (int i = 0; i < VE; ++i) kf[i] = vf[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < VE; ++i) {
+                Ks[t * ld + ch + i] = kf[i];
+                Vs[t * ld + ch + i] = vf[i];
+            }
         }
         __syncthreads();
         if (cls == CLS_INT4) {
-            encode_int_block<4>(Ks, Vs, ld, d, nv, codes, blk);
+            encode_int_block<4>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk);
         } else if (cls == CLS_INT2) {
-            encode_int_block<2>(Ks, Vs, ld, d, nv, codes, blk);
+            encode_int_block<2>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk);
         } else {
             const long long bh = (long long)b * c.Hkv + h;
             encode_cb_block(Ks, Vs, ld, d, nv, codes, blk, c.centroids + bh * d * 4,
@@ -248,7 +356,7 @@ __global__ void dequant_kernel(DevCache c, int n_tok, float* __restrict__ Kout, 
 }  // namespace
 
 size_t append_smem_bytes(int d) {
-    return 2 * kBlockTokens * (d + 1) * sizeof(float) + kBlockTokens * d;
+    return 2 * kBlockTokens * (d + 1) * sizeof(float) + 2 * kBlockTokens * d;
 }
 
 template <typename T>
