@@ -13,9 +13,14 @@ follow the chunk-wise video-diffusion and video-VLM settings of the pages):
   sequence attends to 19600 cached tokens in 613 windows of FP16 / INT4 / INT2
   (planned by kv_window_plan from a seeded similarity) plus its own token.
   One step = one split-K decode attention.
+* ``codebook``: 24 heads, d 128, bf16; 1560 queries over 8192 cached tokens with
+  codebook keys (4 centroids per channel from a device k-means of the cached keys,
+  weighted by 256 historical queries) and INT2 values, plus the chunk itself, with the
+  rank-8 PSAC logit term; then the chunk is appended.  Calibration runs once, outside
+  the step, and is reported as ``calibration_ms``.
 * ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|codebook|tiny]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 N > 1 runs independent replicas (weak scaling): every rank owns its own
@@ -67,6 +72,17 @@ def workload_spec(name):
                     cache_bytes=cache_bytes, attn_flops=4.0 * n * (n_cache + n) * d,
                     append_bytes=2 * n * d * 4 + 2 * 2048, jensen=1, seed=1,
                     label="tiny: B1 H1 d64 chunk 64 cache 1024 INT2 fp32, Jensen taylor2")
+    if name == "codebook":
+        H, d, n_cache, n, r = 24, 128, 8192, 1560, 8
+        rp = (r + 7) // 8 * 8
+        blk = 24 * d + 32 * rp * 2                      # key indices | value codes | value (s, z) | coefficients
+        cache_bytes = H * (n_cache // 32) * blk
+        flops = 4.0 * n * (n_cache + n) * d * H + 2.0 * n * n_cache * r * H
+        return dict(name=name, kind="chunk", B=1, Hkv=H, Hq=H, d=d, n_q=n, n_cur=n, chunks=[n_cache], r=r,
+                    n_hist=256, dtype="bf16", cache_bytes=cache_bytes, attn_flops=flops,
+                    append_bytes=2 * H * n * d * 2 + H * ((n + 31) // 32) * blk, jensen=0, psac=1, seed=5,
+                    label=f"codebook: B1 H{H} d{d} chunk {n} cache {n_cache} codebook INT2 keys (4 centroids per "
+                          f"channel, device k-means) + INT2 values, PSAC rank {r}")
     if name == "decode":
         B, Hq, Hkv, d, n_cache = 8, 28, 4, 64, 19600
         return dict(name=name, kind="decode", B=B, Hkv=Hkv, Hq=Hq, d=d, n_q=1, n_cur=1, n_cache=n_cache,
@@ -82,6 +98,8 @@ def make_inputs(spec):
         return synth.tiny(spec["seed"])
     if spec["kind"] == "decode":
         return synth.decode_case(spec["seed"])
+    if spec["name"] == "codebook":
+        return synth.codebook_case(spec["seed"])
     return synth.chunk_case(spec["seed"], Hkv=spec["Hkv"], chunks=spec["chunks"], n_cur=spec["n_cur"])
 
 
@@ -227,8 +245,27 @@ class ChunkRunner:
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(tdt)
         nb_cache = sum((n + 31) // 32 for n in spec["chunks"])
         nb_cur = (spec["n_cur"] + 31) // 32
-        self.tc = B.TorchCache(spec["B"], spec["Hkv"], spec["d"], B.KV_UNIFORM2, (0, 0, nb_cache + nb_cur),
-                               device=dev)
+        r = spec.get("r", 0)
+        kind = B.KV_CODEBOOK2 if spec["name"] == "codebook" else B.KV_UNIFORM2
+        self.tc = B.TorchCache(spec["B"], spec["Hkv"], spec["d"], kind, (0, 0, nb_cache + nb_cur),
+                               raw_dtype=B.KV_BF16, psac_rank=r, device=dev)
+        self.calib_ms = None
+        if kind == B.KV_CODEBOOK2:
+            # calibration of the prefill on the device: per-channel centroids of the cached keys,
+            # the PSAC basis of the historical queries
+            K = to(inputs["K_cache"])
+            Qh = to(inputs["Q_hist"][None])
+            ws_b = B.kv_psac_workspace(self.tc.layout)
+            ws = torch.empty(max(ws_b, 16), dtype=torch.uint8, device=dev)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            wts = torch.zeros((1, spec["Hkv"], spec["d"]), dtype=torch.float32, device=dev)
+            B.kv_codebook_fit(K, self.dt, K.shape[2], self.tc.c, 20, Qh, spec["n_hist"], wts)
+            B.kv_psac_basis(Qh, self.dt, spec["n_hist"], self.tc.c, None, ws, ws_b)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            self.calib_ms = e0.elapsed_time(e1)
         t0 = 0
         for n in spec["chunks"]:
             B.kv_quantize_append(to(inputs["K_cache"][:, :, t0:t0 + n]), to(inputs["V_cache"][:, :, t0:t0 + n]),
@@ -237,7 +274,7 @@ class ChunkRunner:
         self.saved = (list(self.tc.c.n_blocks), self.tc.c.n_tokens)
         self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
         self.Q, self.Kc, self.Vc = self.inputs
-        self.opts = B.kv_attn_opts(0.0, spec["jensen"], 0, 0, 0, B.KV_PATH_AUTO)
+        self.opts = B.kv_attn_opts(0.0, spec["jensen"], spec.get("psac", 0), 0, 0, B.KV_PATH_AUTO)
         self.out = torch.empty_like(self.Q)
         self.lse = torch.empty(self.Q.shape[:3], dtype=torch.float32, device=dev)
         self.ws_bytes = B.kv_attention_workspace(self.tc.c, self.dt, spec["n_q"], spec["n_cur"], spec["Hq"],
@@ -414,6 +451,8 @@ def run_own(args, rank, world, dist):
     }
     if spec["kind"] == "chunk":
         line["append_gbs"] = spec["append_bytes"] / t_app / 1e9
+    if getattr(r, "calib_ms", None) is not None:
+        line["calibration_ms"] = r.calib_ms   # once per prefill, outside the step
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, inputs)
     print(json.dumps(line), flush=True)
@@ -463,6 +502,17 @@ def oracle_sample_step(spec, inputs, heads):
                                 "f16", operands="f32")
         return heads * g
     sl = slice(0, heads)
+    if spec["name"] == "codebook":
+        from oracle import codebook as OC, psac as OP
+        cent = np.stack([OC.fit_centroids(inputs["K_cache"][0, h]) for h in range(heads)])[None].astype(np.float32)
+        U = np.stack([OP.psac_basis(inputs["Q_hist"][h], spec["r"])[0] for h in range(heads)])[None].astype(
+            np.float32)
+        nb = inputs["K_cache"].shape[2] // 32
+        oc = OC.build_codebook(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], cent, U, nb)
+        OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
+                                spec["dtype"], psac_U=U)
+        OC.build_codebook(inputs["K_cur"][:, sl], inputs["V_cur"][:, sl], cent, U, (spec["n_cur"] + 31) // 32)
+        return spec["B"] * heads * spec["n_q"]
     oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
                           sum((n + 31) // 32 for n in spec["chunks"]))
     OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
@@ -484,6 +534,9 @@ def sample_text(spec, heads):
     if spec["kind"] == "decode":
         return (f"{heads} kv head of sequence 0 ({heads * spec['Hq'] // spec['Hkv']} query heads): mixed cache "
                 f"build of {spec['n_cache']} tokens + decode attention, fp64 numpy")
+    if spec["name"] == "codebook":
+        return (f"{heads} head of {spec['Hq']}: k-means + PSAC basis + cache build + attention of "
+                f"{spec['n_q']} queries + append, fp64 numpy")
     return (f"{heads} head of {spec['Hq']}: cache build + attention of {spec['n_q']} queries + append, "
             f"fp64 numpy")
 

@@ -33,6 +33,14 @@
 // 384-415, Q 448-511.  Every wait is bounded; every warp-collective tcgen05
 // load/store runs with the whole warp converged.
 //
+// Codebook caches ("QuantWM", Methodology: per-channel 4-centroid INT2 keys plus
+// the rank-r compensation q . U coeff in the logit): K_hat comes from a byte-permute
+// lookup of each key's 2-bit indices in bf16 centroid tables, and the compensation
+// is two more fp16 MMAs into S per 16 ranks -- A = U^T q of the query rows (fp32,
+// split into fp16 high + low parts, TMEM columns 384-415, where the Jensen term
+// lives for INT caches), B = the tile's stored fp16 coefficients.  Codebook keys
+// carry no step sizes, so there is no Jensen term for them.
+//
 // Dequantisation is exact: a code c at bits [b i, b i + b) of a word becomes the
 // float c 2^(b i) by or-ing it into the mantissa of 2^23 and subtracting 2^23,
 // and fmaf(c 2^(b i), s 2^(-b i), z) rounds c s + z once, as fmaf(c, s, z) does.
@@ -67,24 +75,46 @@ constexpr uint32_t kIdescPV = idesc_f16(kM, kD);    // O += P V_hat
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// shared memory map (bytes from a 1024-aligned base)
+// Cache block formats the kernel reads (one template instance each).
+enum { FMT_INT2 = 0, FMT_INT4 = 1, FMT_CB2 = 2 };
+template <int FMT> constexpr int vbits() { return FMT == FMT_INT4 ? 4 : 2; }
+// bytes of one block (CB2: the largest, PSAC rank 32; the actual stride is the layout's)
+template <int FMT> constexpr int max_block_bytes() {
+    return FMT == FMT_CB2 ? 24 * kD + kBlockTokens * 32 * 2 : 8 * kD * vbits<FMT>() + 16 * kD;
+}
+// byte offsets of the value codes and the value (step, zero) pairs inside a block
+template <int FMT> constexpr int voff_codes() { return FMT == FMT_CB2 ? 8 * kD : 4 * kD * vbits<FMT>() + 8 * kD; }
+template <int FMT> constexpr int voff_meta() {
+    return FMT == FMT_CB2 ? 16 * kD : voff_codes<FMT>() + 4 * kD * vbits<FMT>();
+}
+constexpr int kCbCoeffOff = 24 * kD;        // CB2: fp16 PSAC coefficients [32][rp]
+
 constexpr int kTile = kM * kD * 2;          // 32 KB: one 16-bit 128 x 128 operand tile
 constexpr int kWBytes = 16 * kD * 2;        // 4 KB: 16 x 128 bf16 Jensen weights
-constexpr int kQ2hOff = 0;                  // bf16 high part of q^2
-constexpr int kQ2lOff = kQ2hOff + kTile;    // bf16 low part of q^2 (q^2 = high + low exactly)
-constexpr int kKOff = kQ2lOff + kTile;      // 1 buffer
-constexpr int kVOff = kKOff + kTile;        // 2 stages
-constexpr int kWOff = kVOff + 2 * kTile;    // 2 stages
-constexpr int kStgOff = kWOff + 2 * kWBytes;
-
-template <int BITS> constexpr int block_bytes() { return 8 * kD * BITS + 16 * kD; }
-template <int BITS> constexpr int stage_bytes() { return 4 * block_bytes<BITS>(); }
-template <int BITS> constexpr int info_off() { return kStgOff + 2 * stage_bytes<BITS>(); }
-template <int BITS> constexpr int stglen_off() { return info_off<BITS>() + 2 * 32; }
-template <int BITS> constexpr int bar_off() { return stglen_off<BITS>() + 2 * 16; }
+constexpr int kCoefTile = kN * 128;         // 16 KB: 128 keys x 64 fp16 PSAC coefficients (swizzled)
+constexpr int kCentBytes = kD * 8;          // 1 KB: byte-planar bf16 centroid tables
 constexpr int kNumBars = 13;
-template <int BITS> constexpr int slot_off() { return bar_off<BITS>() + kNumBars * 8; }
-template <int BITS> constexpr int smem_bytes() { return slot_off<BITS>() + 16 + 1024; }   // + alignment slack
+
+// Shared memory map (bytes from a 1024-aligned base).  INT formats: the bf16 high
+// and low parts of q^2 for the Jensen MMA; CB2: the PSAC coefficient tile and the
+// centroid tables instead.
+template <int FMT> struct Smem {
+    static constexpr bool cb = FMT == FMT_CB2;
+    static constexpr int q2h = 0;                               // bf16 high part of q^2
+    static constexpr int q2l = q2h + (cb ? 0 : kTile);          // low part (q^2 = high + low exactly)
+    static constexpr int k = q2l + (cb ? 0 : kTile);            // K_hat, 1 buffer
+    static constexpr int coef = k + kTile;                      // CB2: PSAC coefficients, 1 buffer
+    static constexpr int v = coef + (cb ? kCoefTile : 0);       // V_hat^T, 2 stages
+    static constexpr int w = v + 2 * kTile;                     // Jensen weights, 2 stages
+    static constexpr int cent = w + 2 * kWBytes;                // CB2: centroid tables
+    static constexpr int stg = cent + (cb ? kCentBytes : 0);    // staged packed blocks, 2 slots
+    static constexpr int stage = 4 * max_block_bytes<FMT>();
+    static constexpr int info = stg + 2 * stage;
+    static constexpr int stglen = info + 2 * 32;
+    static constexpr int bars = stglen + 2 * 16;
+    static constexpr int slot = bars + kNumBars * 8;
+    static constexpr int total = slot + 16 + 1024;              // + alignment slack
+};
 
 enum {
     BAR_KV_FULL = 0,   // [2] producers -> MMA/softmax: K_hat, V_hat[s], W[s], info[s] ready
@@ -134,19 +164,18 @@ __device__ __forceinline__ void dequant2(float& v0, float& v1, float m0, float m
 // 2 (pw >> 2) + 1 into V_hat^T[stage] (fp16).  The group's per-token steps are
 // first pre-scaled in the staging copy by 2^(-b i), i = the token's slot in its
 // half word.
-template <int BITS>
-__device__ __forceinline__ void fill_cache_values(unsigned char* sm, int stage, unsigned char* stg, int nb, int pw,
+template <int FMT>
+__device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned char* stg, int stride, int nb, int pw,
                                                   int lane) {
-    const IntBlockOffsets o = int_offsets(kD, BITS);
-    unsigned char* Vt = sm + kVOff + stage * kTile;
+    constexpr int BITS = vbits<FMT>();
     const int g = pw & 3, c = 32 * g + lane;
     constexpr int kSlots = 16 / BITS;    // tokens per half word
 #pragma unroll 1
-    for (int bb = 0; bb < 2; ++bb) {
-        const int q = 2 * (pw >> 2) + bb;
+    for (int k2 = 0; k2 < 2; ++k2) {
+        const int q = 2 * (pw >> 2) + k2;
         if (q < nb) {
-            unsigned char* blk = stg + q * block_bytes<BITS>();
-            float* vm = reinterpret_cast<float*>(blk + o.vm) + g * 64;
+            unsigned char* blk = stg + q * stride;
+            float* vm = reinterpret_cast<float*>(blk + voff_meta<FMT>()) + g * 64;
             // token t's (s, z) -> (s 2^(-b slot), z), stored per token pair as
             // (s'_t, s'_t+1, z_t, z_t+1) so that pairs load into adjacent registers
             const float2 e = reinterpret_cast<const float2*>(vm)[lane];
@@ -154,7 +183,7 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* sm, int stage, 
             vm[4 * (lane >> 1) + (lane & 1)] = e.x * pow2i(-BITS * (lane % kSlots));
             vm[4 * (lane >> 1) + 2 + (lane & 1)] = e.y;
             __syncwarp();
-            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc) + c * BITS;
+            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + voff_codes<FMT>()) + c * BITS;
             uint32_t w[BITS];
 #pragma unroll
             for (int k = 0; k < BITS; ++k) w[k] = vc[k];
@@ -187,16 +216,15 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* sm, int stage, 
 // Keys of a staged cache tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
 // 8 kg .. 8 kg + 7 (one block) into K_hat (bf16).
 template <int BITS>
-__device__ __forceinline__ void fill_cache_keys(unsigned char* sm, const unsigned char* stg, int nb, int p) {
+__device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigned char* stg, int nb, int p) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    unsigned char* Kt = sm + kKOff;
     const int jc = p & 15, kg = p >> 4, q = kg >> 2, t0 = 8 * (kg & 3);
     if (q >= nb) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(8 * kg + r, jc)) = make_uint4(0, 0, 0, 0);
         return;
     }
-    const unsigned char* blk = stg + q * block_bytes<BITS>();
+    const unsigned char* blk = stg + q * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>();
     constexpr int kSlots = 16 / BITS;
     const float4* km4 = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
     float s[8], z[8];
@@ -239,18 +267,91 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* sm, const unsigne
     }
 }
 
+// Centroid tables of one (batch, kv head) for the codebook key lookup: channel c's
+// four centroids rounded to bf16, stored byte-planar as two words -- the four low
+// bytes, then the four high bytes -- so that one byte permute with selector
+// nibbles (k, 4 + k) returns centroid k as a bf16.
+__device__ __forceinline__ void fill_centroid_tables(uint32_t* tab, const float* cent, int tid) {
+    for (int ch = tid; ch < kD; ch += kThreads) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(cent) + ch);
+        const uint32_t c01 = pack_bf16(v.x, v.y), c23 = pack_bf16(v.z, v.w);
+        tab[2 * ch] = __byte_perm(c01, c23, 0x6420);
+        tab[2 * ch + 1] = __byte_perm(c01, c23, 0x7531);
+    }
+}
+
+// Keys of a staged codebook tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
+// 8 kg .. 8 kg + 7 (one block) into K_hat (bf16) by looking the 2-bit centroid
+// indices up in its channels' tables, two keys at a time.  For the channel pair
+// (2 i, 2 i + 1) the four index bits n = k0 + 4 k1 of a key become the selector
+// bytes (17 k0 + 0x40, 17 k1 + 0x40), i.e. nibbles (k0, 4 + k0, k1, 4 + k1):
+// 17 n + 1071 (n & 12) + 0x4040 = 17 k0 + 4352 k1 + 0x4040.
+__device__ __forceinline__ void fill_cb_keys(unsigned char* Kt, const unsigned char* stg, int stride, int nb,
+                                             const uint32_t* tab, int p) {
+    const int jc = p & 15, kg = p >> 4, q = kg >> 2, t0 = 8 * (kg & 3);
+    if (q >= nb) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(8 * kg + r, jc)) = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 v = reinterpret_cast<const uint4*>(tab)[4 * jc + k];
+        lo[2 * k] = v.x;
+        hi[2 * k] = v.y;
+        lo[2 * k + 1] = v.z;
+        hi[2 * k + 1] = v.w;
+    }
+    constexpr int KW = kD / 16;   // code words per key
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(stg + q * stride);
+    const uint32_t half = (jc & 1) ? 0x7632u : 0x5410u;
+#pragma unroll
+    for (int r = 0; r < 8; r += 2) {
+        const int t = t0 + r;
+        // key t's 8 indices in the low half, key t + 1's in the high half
+        const uint32_t x = __byte_perm(kc[t * KW + (jc >> 1)], kc[(t + 1) * KW + (jc >> 1)], half);
+        uint32_t o0[4], o1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t y = x >> (4 * i);
+            const uint32_t sel = (y & 0x000F000Fu) * 17u + (y & 0x000C000Cu) * 1071u + 0x40404040u;
+            const uint32_t sel1 = sel >> 16;
+            o0[i] = __byte_perm(__byte_perm(lo[2 * i], hi[2 * i], sel), __byte_perm(lo[2 * i + 1], hi[2 * i + 1], sel),
+                                0x7610);
+            o1[i] = __byte_perm(__byte_perm(lo[2 * i], hi[2 * i], sel1),
+                                __byte_perm(lo[2 * i + 1], hi[2 * i + 1], sel1), 0x7610);
+        }
+        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t, jc)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t + 1, jc)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    }
+}
+
+// PSAC coefficients of a staged codebook tile -> the K-major swizzled B operand
+// [128 keys x nch 8-element chunks] (fp16); chunks at or beyond the stored rp and
+// rows of missing blocks are zero.
+__device__ __forceinline__ void fill_coeff(unsigned char* Ct, const unsigned char* stg, int stride, int nb, int rp,
+                                           int nch, int p) {
+    for (int e = p; e < kN * nch; e += kProd) {
+        const int row = e / nch, ch = e - (e / nch) * nch, q = row >> 5, t = row & 31;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (q < nb && 8 * ch < rp)
+            v = *reinterpret_cast<const uint4*>(stg + q * stride + kCbCoeffOff + (t * rp + 8 * ch) * 2);
+        *reinterpret_cast<uint4*>(Ct + sw_off(row, ch)) = v;
+    }
+}
+
 // Jensen weights of a staged tile.  TAYLOR2: W rows g and 4 + g hold the bf16
 // high and low parts of w_c = s_c^2 tau^2 / 24 log2(e) of block g (zero for
 // missing blocks); rows 8-15 stay zero.  EXACT: the block steps s_c as fp32 [4][128].
 template <int BITS, int JENSEN>
-__device__ __forceinline__ void fill_weights(unsigned char* sm, int stage, const unsigned char* stg, int nb, int p,
-                                             float coef) {
+__device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned char* stg, int nb, int p, float coef) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    unsigned char* W = sm + kWOff + stage * kWBytes;
     const int g = p >> 6, c = 2 * (p & 63);
     float2 s = make_float2(0.0f, 0.0f);
     if (g < nb) {
-        const float4 v = *reinterpret_cast<const float4*>(stg + g * block_bytes<BITS>() + o.km + c * 8);
+        const float4 v = *reinterpret_cast<const float4*>(stg + g * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>() +
+                                                          o.km + c * 8);
         s = make_float2(v.x, v.z);
     }
     if (JENSEN == KV_JENSEN_TAYLOR2) {
@@ -268,9 +369,8 @@ __device__ __forceinline__ void fill_weights(unsigned char* sm, int stage, const
 
 // Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T.
 // Thread p transposes the 8 x 8 block (keys 8 (p >> 4) .., channels 8 (p & 15) ..).
-__device__ __forceinline__ void fill_current_values(unsigned char* sm, int stage, const __nv_bfloat16* Vcur,
-                                                    long long row0, int valid, int p) {
-    unsigned char* Vt = sm + kVOff + stage * kTile;
+__device__ __forceinline__ void fill_current_values(unsigned char* Vt, const __nv_bfloat16* Vcur, long long row0,
+                                                    int valid, int p) {
     const uint4* Vg = reinterpret_cast<const uint4*>(Vcur + row0 * kD);
     const int kc8 = p >> 4, cch = p & 15;
     uint32_t x[8][4];
@@ -300,9 +400,8 @@ __device__ __forceinline__ void fill_current_values(unsigned char* sm, int stage
 }
 
 // Current-chunk keys: bf16 rows copied into the swizzled K_hat buffer.
-__device__ __forceinline__ void fill_current_keys(unsigned char* sm, const __nv_bfloat16* Kcur, long long row0,
+__device__ __forceinline__ void fill_current_keys(unsigned char* Kt, const __nv_bfloat16* Kcur, long long row0,
                                                   int valid, int p) {
-    unsigned char* Kt = sm + kKOff;
     const int jc = p & 15, r0 = p >> 4;
     const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
     uint4 kv[8];
@@ -316,12 +415,14 @@ __device__ __forceinline__ void fill_current_keys(unsigned char* sm, const __nv_
 }
 
 // --------------------------------------------------------------- kernel -----
-template <int BITS, int JENSEN>
+template <int FMT, int JENSEN>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kcur,
-               const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau,
+               const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau, int r16,
                int n_splits, void* __restrict__ out, int out_f32, float* __restrict__ lse, float* __restrict__ ws_o,
                float2* __restrict__ ws_ml, int* __restrict__ err) {
+    using M = Smem<FMT>;
+    constexpr bool kCb = FMT == FMT_CB2;
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
     unsigned char* sm =
@@ -333,15 +434,17 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     const int hq = blockIdx.y, b = blockIdx.z;
     const int h = hq / (Hq / c.Hkv);
     const int q0 = qt * kM;
-    const int seg = BITS == 4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    // staging stride of one block (a CB2 block's size depends on the PSAC rank)
+    const int bb = kCb ? (int)c.block_bytes[seg] : max_block_bytes<FMT>();
     const int n_cache_tiles = (c.n_blocks[seg] + 3) / 4;
     const int n_tiles = n_cache_tiles + (n_cur + kN - 1) / kN;
     // split s takes tiles s, s + n_splits, ...: every split gets an even share of
     // cache and current-chunk tiles, and its cache tiles still come first.
     const int T = split < n_tiles ? (n_tiles - split + n_splits - 1) / n_splits : 0;
     auto tile_of = [&](int j) { return split + j * n_splits; };
-    auto bar = [&](int i) { return sbase + bar_off<BITS>() + 8 * i; };
-    TileInfo* infos = reinterpret_cast<TileInfo*>(sm + info_off<BITS>());
+    auto bar = [&](int i) { return sbase + M::bars + 8 * i; };
+    TileInfo* infos = reinterpret_cast<TileInfo*>(sm + M::info);
 
     if (tid == 0) {
         abort_flag = 0;
@@ -360,13 +463,26 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         mbar_init(bar(BAR_STG_EMPTY + 1), kProd);
         mbar_fence_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(sbase + slot_off<BITS>(), kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(sbase + M::slot, kTmemCols);
 
-    // q^2 of the Q tile (bf16 q, so q^2 has at most 16 significant bits and splits
-    // exactly into bf16 high + low) -> swizzled smem, rows beyond n_q zero; the
-    // Jensen weight tiles start zero (rows 8-15 stay zero)
     const uint4* Qg = reinterpret_cast<const uint4*>(Q + (((long long)b * Hq + hq) * n_q) * kD);
-    {
+    // PSAC basis U of this head, zero-padded to [d][r16] fp32, staged in the second
+    // V_hat stage (written by the producers only after the second barrier below)
+    float* Us = reinterpret_cast<float*>(sm + M::v + kTile);
+    if (kCb) {
+        fill_centroid_tables(reinterpret_cast<uint32_t*>(sm + M::cent),
+                             c.centroids + ((long long)b * c.Hkv + h) * kD * 4, tid);
+        if (r16 > 0) {
+            const float* U = c.psac_u + ((long long)b * c.Hkv + h) * kD * c.r;
+            for (int e = tid; e < kD * r16; e += kThreads) {
+                const int ch = e / r16, jj = e - (e / r16) * r16;
+                Us[e] = jj < c.r ? __ldg(U + ch * c.r + jj) : 0.0f;
+            }
+        }
+    } else {
+        // q^2 of the Q tile (bf16 q, so q^2 has at most 16 significant bits and splits
+        // exactly into bf16 high + low) -> swizzled smem, rows beyond n_q zero; the
+        // Jensen weight tiles start zero (rows 8-15 stay zero)
         for (int e = tid; e < kM * kD / 8; e += kThreads) {
             const int row = e >> 4, ch = e & 15;
             const uint4 v =
@@ -380,17 +496,17 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 hq2[k] = pack_bf16(a, bq);
                 lq2[k] = pack_bf16(a - __uint_as_float(hq2[k] << 16), bq - __uint_as_float(hq2[k] & 0xFFFF0000u));
             }
-            *reinterpret_cast<uint4*>(sm + kQ2hOff + sw_off(row, ch)) = make_uint4(hq2[0], hq2[1], hq2[2], hq2[3]);
-            *reinterpret_cast<uint4*>(sm + kQ2lOff + sw_off(row, ch)) = make_uint4(lq2[0], lq2[1], lq2[2], lq2[3]);
+            *reinterpret_cast<uint4*>(sm + M::q2h + sw_off(row, ch)) = make_uint4(hq2[0], hq2[1], hq2[2], hq2[3]);
+            *reinterpret_cast<uint4*>(sm + M::q2l + sw_off(row, ch)) = make_uint4(lq2[0], lq2[1], lq2[2], lq2[3]);
         }
         for (int e = tid; e < 2 * kWBytes / 16; e += kThreads)
-            reinterpret_cast<uint4*>(sm + kWOff)[e] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(sm + M::w)[e] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async();
     fence_before();
     __syncthreads();
     fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + slot_off<BITS>());
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M::slot);
     if (warp < kSoftWarps) {
         // Q row i -> TMEM lane i, columns kColQ .. kColQ + 63 (two bf16 per column)
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
@@ -408,6 +524,44 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             }
             tmem_st16(tmem + lane_addr + kColQ + 16 * hf, u);
         }
+        if (kCb && r16 > 0) {
+            // u = U^T q of row i in fp32, split into fp16 high + low parts (u = hi + lo up
+            // to 2^-22 |u|): the A operand of the PSAC MMAs, TMEM columns kColD + 8 ks
+            // (high) and kColD + 16 + 8 ks (low) for the 16-wide rank chunk ks
+#pragma unroll 1
+            for (int ks = 0; ks < r16 / 16; ++ks) {
+                float u[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) u[jj] = 0.0f;
+#pragma unroll 1
+                for (int c8 = 0; c8 < kD / 8; ++c8) {
+                    const uint4 v = valid ? __ldg(Qg + (long long)(q0 + tid) * (kD / 8) + c8) : make_uint4(0, 0, 0, 0);
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float qf = __uint_as_float(k & 1 ? (wv[k >> 1] & 0xFFFF0000u) : (wv[k >> 1] << 16));
+                        const float4* ur = reinterpret_cast<const float4*>(Us + (8 * c8 + k) * r16 + 16 * ks);
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const float4 w4 = ur[j4];
+                            u[4 * j4] = fmaf(w4.x, qf, u[4 * j4]);
+                            u[4 * j4 + 1] = fmaf(w4.y, qf, u[4 * j4 + 1]);
+                            u[4 * j4 + 2] = fmaf(w4.z, qf, u[4 * j4 + 2]);
+                            u[4 * j4 + 3] = fmaf(w4.w, qf, u[4 * j4 + 3]);
+                        }
+                    }
+                }
+                uint32_t uh[8], ul[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uh[k] = pack_f16(u[2 * k], u[2 * k + 1]);
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&uh[k]));
+                    ul[k] = pack_f16(u[2 * k] - hf.x, u[2 * k + 1] - hf.y);
+                }
+                tmem_st8(tmem + lane_addr + kColD + 8 * ks, uh);
+                tmem_st8(tmem + lane_addr + kColD + 16 + 8 * ks, ul);
+            }
+        }
         tmem_wait_st();
     }
     fence_before();
@@ -417,7 +571,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t sQ2h = sbase + kQ2hOff, sQ2l = sbase + kQ2lOff, sK = sbase + kKOff;
+            const uint32_t sQ2h = sbase + M::q2h, sQ2l = sbase + M::q2l, sK = sbase + M::k;
             auto issue_qk = [&](int j) {
                 const int s = j & 1;
                 fence_after();
@@ -426,8 +580,19 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
                     mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColQ + 8 * kk, desc_sw128(sK + off), kIdescQK, kk > 0);
                 }
+                if (kCb && r16 > 0 && tile_of(j) < n_cache_tiles) {
+                    // S += (U^T q) coeff^T: fp16, K = the rank padded to 16, high and low
+                    // parts of U^T q against the same coefficients
+                    const uint32_t sC = sbase + M::coef;
+                    for (int ks = 0; ks < r16 / 16; ++ks) {
+                        mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColD + 8 * ks, desc_sw128(sC + 32 * ks),
+                                       kIdescPV, 1);
+                        mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColD + 16 + 8 * ks, desc_sw128(sC + 32 * ks),
+                                       kIdescPV, 1);
+                    }
+                }
                 if (JENSEN == KV_JENSEN_TAYLOR2 && tile_of(j) < n_cache_tiles) {
-                    const uint32_t sW = sbase + kWOff + s * kWBytes;
+                    const uint32_t sW = sbase + M::w + s * kWBytes;
 #pragma unroll
                     for (int kk = 0; kk < 2 * (kD / 16); ++kk) {
                         const int k = kk & 7;
@@ -442,7 +607,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             };
             auto issue_pv = [&](int jj) {
                 fence_after();
-                const uint32_t sV = sbase + kVOff + (jj & 1) * kTile;
+                const uint32_t sV = sbase + M::v + (jj & 1) * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
@@ -484,7 +649,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         // ----------------------------------------------------------- producers
         const int p = tid - 32 * kSoftWarps, pw = p >> 5;
         const int nblk = c.n_blocks[seg];
-        int* stg_len = reinterpret_cast<int*>(sm + stglen_off<BITS>());
+        int* stg_len = reinterpret_cast<int*>(sm + M::stglen);
         const float jcoef = tau * tau * (1.0f / 24.0f) * kLog2e;
         int issued = 0;   // staging copies issued (by producer thread 0)
         // Bulk-copy cache tile j (if it is one) into staging slot j & 1, with its
@@ -496,10 +661,10 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             for (int q = 0; q < 4; ++q)
                 stg_len[(j & 1) * 4 + q] =
                     q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
-            const uint32_t bytes = (uint32_t)(nb * block_bytes<BITS>());
+            const uint32_t bytes = (uint32_t)(nb * bb);
             const uint32_t sbar = bar(BAR_STG_FULL + (j & 1));
             mbar_expect_tx(sbar, bytes);
-            bulk_g2s(sbase + kStgOff + (j & 1) * stage_bytes<BITS>(), block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
+            bulk_g2s(sbase + M::stg + (j & 1) * M::stage, block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
             issued = j + 1;
         };
         if (p == 0) {
@@ -515,25 +680,33 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (j >= 2) ok = mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
             if (ok && cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
             if (!__all_sync(0xffffffffu, ok)) break;
-            unsigned char* stg = sm + kStgOff + s * stage_bytes<BITS>();
+            unsigned char* stg = sm + M::stg + s * M::stage;
             const int nb = cached ? min(4, nblk - tile * 4) : 0;
             const int t0 = (tile - n_cache_tiles) * kN;
             const long long row0 = ((long long)b * c.Hkv + h) * n_cur + t0;
             const int cvalid = min(kN, n_cur - t0);
             if (p < 4) infos[s].nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
-            if (p == 0) infos[s].quantised = cached ? 1 : 0;
+            if (p == 0) infos[s].quantised = cached && !kCb ? 1 : 0;
             // values first: they only need the V_hat stage, free since P V of tile j - 2
+            unsigned char* Vt = sm + M::v + s * kTile;
             if (cached) {
-                fill_cache_values<BITS>(sm, s, stg, nb, pw, lane);
-                if (JENSEN != KV_JENSEN_OFF) fill_weights<BITS, JENSEN>(sm, s, stg, nb, p, jcoef);
+                fill_cache_values<FMT>(Vt, stg, bb, nb, pw, lane);
+                if (!kCb && JENSEN != KV_JENSEN_OFF)
+                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef);
             } else {
-                fill_current_values(sm, s, Vcur, row0, cvalid, p);
+                fill_current_values(Vt, Vcur, row0, cvalid, p);
             }
             // keys: the single K_hat buffer is free once Q K_hat^T of tile j - 1 completed
             const bool ok2 = j == 0 || mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
             if (!__all_sync(0xffffffffu, ok2)) break;
-            if (cached) fill_cache_keys<BITS>(sm, stg, nb, p);
-            else fill_current_keys(sm, Kcur, row0, cvalid, p);
+            if (cached && kCb) {
+                fill_cb_keys(sm + M::k, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
+                if (r16 > 0) fill_coeff(sm + M::coef, stg, bb, nb, c.rp, r16 / 8, p);
+            } else if (cached) {
+                fill_cache_keys<vbits<FMT>()>(sm + M::k, stg, nb, p);
+            } else {
+                fill_current_keys(sm + M::k, Kcur, row0, cvalid, p);
+            }
             fence_proxy_async();
             mbar_arrive(bar(BAR_KV_FULL + s));
             if (cached) {
@@ -578,7 +751,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
 #pragma unroll
                     for (int g = 0; g < 4; ++g) dl[g] = dv[g] + dv[4 + g];
                 } else if (JENSEN == KV_JENSEN_EXACT) {
-                    const float* SK = reinterpret_cast<const float*>(sm + kWOff + s * kWBytes);
+                    const float* SK = reinterpret_cast<const float*>(sm + M::w + s * kWBytes);
                     const float jt = 0.5f * tau;
 #pragma unroll 1
                     for (int ch = 0; ch < 16; ++ch) {
@@ -745,24 +918,26 @@ int num_sms() {
     return g_num_sms;
 }
 
-template <int BITS, int JENSEN>
+template <int FMT, int JENSEN>
 kv_status launch_tc_t(const DevCache& c, const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
-                      float tau, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
+                      float tau, int r16, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
                       int* err, cudaStream_t st) {
+    constexpr int kSmem = Smem<FMT>::total;
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<BITS, JENSEN>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BITS>());
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, JENSEN>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess)
-            return set_error(KV_ERR_CUDA, "attn_tc_kernel: %d bytes of shared memory: %s", smem_bytes<BITS>(),
+            return set_error(KV_ERR_CUDA, "attn_tc_kernel: %d bytes of shared memory: %s", kSmem,
                              cudaGetErrorString(e));
         attr = true;
     }
     const int n_qt = (n_q + kM - 1) / kM;
     dim3 grid(n_qt * n_splits, Hq, c.B);
-    attn_tc_kernel<BITS, JENSEN><<<grid, kThreads, smem_bytes<BITS>(), st>>>(
+    attn_tc_kernel<FMT, JENSEN><<<grid, kThreads, kSmem, st>>>(
         static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
-        static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, n_splits, out, out_f32, lse, ws_o, ws_ml, err);
+        static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, r16, n_splits, out, out_f32, lse, ws_o, ws_ml,
+        err);
     return check_launch("attn_tc_kernel");
 }
 
@@ -773,7 +948,10 @@ bool tc_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const cha
     (void)Hq;
     if (dt != KV_BF16) { *why = "needs bf16 I/O"; return false; }
     if (L.d != kD) { *why = "needs head dim 128"; return false; }
-    if (L.kind != KV_UNIFORM2 && L.kind != KV_UNIFORM4) { *why = "needs a UNIFORM2 or UNIFORM4 cache"; return false; }
+    if (L.kind != KV_UNIFORM2 && L.kind != KV_UNIFORM4 && L.kind != KV_CODEBOOK2) {
+        *why = "needs a UNIFORM2, UNIFORM4 or CODEBOOK2 cache";
+        return false;
+    }
     if (n_q < 16) { *why = "needs at least 16 queries"; return false; }
     return true;
 }
@@ -810,7 +988,6 @@ size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits) {
 kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
                          const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out, int out_f32,
                          float* lse, void* ws, cudaStream_t st) {
-    (void)psac;
     const DevCache c = make_dev_cache(cache);
     int* err = static_cast<int*>(ws);
     float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + 256);
@@ -819,24 +996,29 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
     const bool debug = getenv("BITKV_DEBUG_SYNC") != nullptr;
     if (debug) cudaMemsetAsync(err, 0, sizeof(int), st);
     kv_status s;
-#define BITKV_TC(BITS)                                                                                        \
+#define BITKV_TC(FMT)                                                                                         \
     switch (jensen) {                                                                                         \
         case KV_JENSEN_TAYLOR2:                                                                               \
-            s = launch_tc_t<BITS, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32, \
-                                                     lse, ws_o, ws_ml, err, st);                              \
+            s = launch_tc_t<FMT, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out,      \
+                                                    out_f32, lse, ws_o, ws_ml, err, st);                      \
             break;                                                                                            \
         case KV_JENSEN_EXACT:                                                                                 \
-            s = launch_tc_t<BITS, KV_JENSEN_EXACT>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32,   \
-                                                   lse, ws_o, ws_ml, err, st);                                \
+            s = launch_tc_t<FMT, KV_JENSEN_EXACT>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32, \
+                                                  lse, ws_o, ws_ml, err, st);                                 \
             break;                                                                                            \
         default:                                                                                              \
-            s = launch_tc_t<BITS, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, n_splits, out, out_f32, lse, \
-                                                 ws_o, ws_ml, err, st);                                       \
+            s = launch_tc_t<FMT, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32,   \
+                                                lse, ws_o, ws_ml, err, st);                                   \
     }
-    if (c.kind == KV_UNIFORM4) {
-        BITKV_TC(4)
+    if (c.kind == KV_CODEBOOK2) {
+        // codebook keys carry no step sizes: no Jensen term
+        const int r16 = psac ? (c.r + 15) / 16 * 16 : 0;
+        s = launch_tc_t<FMT_CB2, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32, lse,
+                                                ws_o, ws_ml, err, st);
+    } else if (c.kind == KV_UNIFORM4) {
+        BITKV_TC(FMT_INT4)
     } else {
-        BITKV_TC(2)
+        BITKV_TC(FMT_INT2)
     }
 #undef BITKV_TC
     if (s != KV_OK) return s;
