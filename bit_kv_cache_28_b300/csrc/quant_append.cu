@@ -53,62 +53,6 @@ __device__ __forceinline__ void step_and_zero(float mn, float mx, float qmax, fl
     s = __fadd_rn(__fdiv_rn(__fsub_rn(mx, z), qmax), 0.0f);
 }
 
-__device__ __forceinline__ uint32_t code_of(float x, float s, float z, float qmax) {
-    if (!(s > 0.0f)) return 0u;
-    float t = rintf(__fdiv_rn(__fsub_rn(x, z), s));  // ties to even
-    t = fminf(fmaxf(t, 0.0f), qmax);
-    return static_cast<uint32_t>(t);
-}
-
-// Values of one block: per (token, 32-channel group) with a warp per group.
-// Writes Vm[g][t] and the value codes into codes[t][ch].
-template <int BITS>
-__device__ void quantise_values(const float* Vs, int ld, int d, int nv, uint8_t* codes, float2* vm) {
-    const float qmax = float((1 << BITS) - 1);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const int ng = d / 32;
-    for (int p = warp; p < kBlockTokens * ng; p += nwarps) {
-        const int t = p / ng, g = p % ng;
-        const float x = Vs[t * ld + g * 32 + lane];
-        float s = 0.0f, z = 0.0f;
-        uint32_t q = 0;
-        if (t < nv) {                                  // warp-uniform
-            const float mn = warp_min(x), mx = warp_max(x);
-            step_and_zero(mn, mx, qmax, s, z);
-            q = code_of(x, s, z, qmax);
-        }
-        codes[t * d + g * 32 + lane] = static_cast<uint8_t>(q);
-        if (lane == 0) vm[g * 32 + t] = make_float2(s, z);
-    }
-}
-
-// Pack codes[t][ch] channel-major: word (ch, q) holds tokens q*per .. q*per+per-1.
-template <int BITS>
-__device__ void pack_values(const uint8_t* codes, int d, uint32_t* vcw) {
-    constexpr int per = 32 / BITS;
-    for (int w = threadIdx.x; w < d * BITS; w += blockDim.x) {
-        const int ch = w / BITS, q = w % BITS;
-        uint32_t v = 0;
-#pragma unroll
-        for (int i = 0; i < per; ++i) v |= uint32_t(codes[(q * per + i) * d + ch]) << (BITS * i);
-        vcw[w] = v;
-    }
-}
-
-// Pack codes[t][ch] token-major: word (t, q) holds channels q*per .. q*per+per-1.
-template <int BITS>
-__device__ void pack_keys(const uint8_t* codes, int d, uint32_t* kcw) {
-    constexpr int per = 32 / BITS;
-    const int wpr = d / per;
-    for (int w = threadIdx.x; w < kBlockTokens * wpr; w += blockDim.x) {
-        const int t = w / wpr, q = w % wpr;
-        uint32_t v = 0;
-#pragma unroll
-        for (int i = 0; i < per; ++i) v |= uint32_t(codes[t * d + q * per + i]) << (BITS * i);
-        kcw[w] = v;
-    }
-}
-
 // Code of d = fl32(x - z) for step s with inverse r = 1/s (rounded): rint(fl32(d / s)),
 // clamped.  fl32(d * r) lies within 3 * 2^-24 |d / s| of fl32(d / s) (both quotients
 // carry at most two roundings of 2^-24), so the two round to the same integer
@@ -122,11 +66,60 @@ __device__ __forceinline__ uint32_t code_fast(float x, float s, float r, float z
     return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), qmax));
 }
 
+// Values of one block, INT layout: (token t, 32-channel group g) is shared by
+// tpc = 256 / d adjacent threads, each taking 32 / tpc channels; min / max are
+// combined by shuffles.  Writes Vm[g][t] and the codes into vc8[c][t].
+template <int BITS>
+__device__ void encode_values(const float* Vs, int ld, int d, int nv, uint8_t* vc8, float2* vm) {
+    const float qmax = float((1 << BITS) - 1);
+    const int tid = threadIdx.x;
+    const int tpc = kAppendThreads / d, span = kBlockTokens / tpc, part = tid % tpc;
+    const int ng = d / 32, pr = tid / tpc;
+    const int t = pr / ng, g = pr % ng, c0 = g * 32 + part * span;
+    float mn = INFINITY, mx = -INFINITY;
+    if (t < nv)
+        for (int i = 0; i < span; ++i) {
+            const float x = Vs[t * ld + c0 + i];
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+        }
+    for (int w = 1; w < tpc; w <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, w));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
+    }
+    float s = 0.0f, z = 0.0f;
+    if (t < nv) step_and_zero(mn, mx, qmax, s, z);
+    const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    if (part == 0) vm[g * 32 + t] = make_float2(s, z);
+    for (int i = 0; i < span; ++i)
+        vc8[(c0 + i) * kBlockTokens + t] =
+            t < nv ? static_cast<uint8_t>(code_fast(Vs[t * ld + c0 + i], s, r, z, qmax)) : 0;
+}
+
+// Pack byte codes into b-bit words: word w holds bytes w per .. w per + per - 1
+// (per = 32 / b), byte i at bits [b i, b i + b).  The key bytes are token-major
+// and the value bytes channel-major, so the same rule gives both layouts.
+template <int BITS>
+__device__ void pack_words(const uint8_t* kc8, const uint8_t* vc8, int nwords, uint32_t* kw, uint32_t* vw) {
+    constexpr int per = 32 / BITS;
+    for (int w = threadIdx.x; w < nwords; w += kAppendThreads) {
+        const uint8_t* ksrc = kc8 + w * per;
+        const uint8_t* vsrc = vc8 + w * per;
+        uint32_t a = 0, bq = 0;
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+            a |= uint32_t(ksrc[i]) << (BITS * i);
+            bq |= uint32_t(vsrc[i]) << (BITS * i);
+        }
+        kw[w] = a;
+        vw[w] = bq;
+    }
+}
+
 // One uniform INT block.  Keys: channel c is shared by tpc = 256 / d adjacent
 // threads, each taking 32 / tpc tokens; min / max are combined by shuffles.
-// Values: (token t, 32-channel group g) is shared by tpc threads the same way.
-// Codes go to byte arrays kc8[t][c] and vc8[c][t]; one thread per output word
-// packs them.
+// Values as encode_values.  Codes go to byte arrays kc8[t][c] and vc8[c][t];
+// one thread per output word packs them.
 template <int BITS>
 __device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d, int nv, uint8_t* kc8,
                                  uint8_t* vc8, unsigned char* blk) {
@@ -161,89 +154,243 @@ __device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d
             kc8[t * d + ch] = t < nv ? static_cast<uint8_t>(code_fast(Ks[t * ld + ch], s, r, z, qmax)) : 0;
         }
     }
-    // values: per (token, 32-channel group); pair index = t * (d / 32) + g
-    {
-        const int ng = d / 32, pr = tid / tpc;
-        const int t = pr / ng, g = pr % ng, c0 = g * 32 + part * span;
-        float mn = INFINITY, mx = -INFINITY;
-        if (t < nv)
-            for (int i = 0; i < span; ++i) {
-                const float x = Vs[t * ld + c0 + i];
-                mn = fminf(mn, x);
-                mx = fmaxf(mx, x);
-            }
-        for (int w = 1; w < tpc; w <<= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, w));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, w));
-        }
-        float s = 0.0f, z = 0.0f;
-        if (t < nv) step_and_zero(mn, mx, qmax, s, z);
-        const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
-        if (part == 0) reinterpret_cast<float2*>(blk + o.vm)[g * 32 + t] = make_float2(s, z);
-        for (int i = 0; i < span; ++i)
-            vc8[(c0 + i) * kBlockTokens + t] =
-                t < nv ? static_cast<uint8_t>(code_fast(Vs[t * ld + c0 + i], s, r, z, qmax)) : 0;
-    }
+    encode_values<BITS>(Vs, ld, d, nv, vc8, reinterpret_cast<float2*>(blk + o.vm));
     __syncthreads();
-    // pack: key word (t, q) holds channels q per .. q per + per - 1 of token t;
-    // value word (c, q) holds tokens q per .. of channel c (per = 32 / BITS)
-    constexpr int per = 32 / BITS;
-    uint32_t* kw = reinterpret_cast<uint32_t*>(blk + o.kc);
-    uint32_t* vw = reinterpret_cast<uint32_t*>(blk + o.vc);
-    const int nwords = kBlockTokens * d / per;    // same count for keys and values
-    for (int w = tid; w < nwords; w += kAppendThreads) {
-        const uint8_t* ksrc = kc8 + w * per;        // token-major bytes: word w covers bytes w per ..
-        const uint8_t* vsrc = vc8 + w * per;        // channel-major bytes, likewise
-        uint32_t a = 0, bq = 0;
-#pragma unroll
-        for (int i = 0; i < per; ++i) {
-            a |= uint32_t(ksrc[i]) << (BITS * i);
-            bq |= uint32_t(vsrc[i]) << (BITS * i);
-        }
-        kw[w] = a;
-        vw[w] = bq;
-    }
+    pack_words<BITS>(kc8, vc8, kBlockTokens * d * BITS / 32, reinterpret_cast<uint32_t*>(blk + o.kc),
+                     reinterpret_cast<uint32_t*>(blk + o.vc));
 }
 
-// Codebook block: nearest fp32 centroid per key entry (fp64 |x - mu|, ties to
-// the lower index), INT2 values, fp16 PSAC coefficients U^T (k - k_hat) in fp64.
-__device__ void encode_cb_block(const float* Ks, const float* Vs, int ld, int d, int nv, uint8_t* codes,
-                                unsigned char* blk, const float* cent, const float* U, int r, int rp) {
+// Exact sum s + e = a + b of two floats (Knuth's TwoSum; no FMA contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 instructions: one instruction, two lanes of work).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 x2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 x2_split(f32x2 v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f32x2 x2_add(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 x2_sub(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 x2_mul(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 x2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// One compensated dot-product step for two ranks: (s, cc) += u (eh + el), with the
+// product u eh split exactly by FMA and the sum split exactly by TwoSum.
+__device__ __forceinline__ void dot2_step(f32x2& s, f32x2& cc, f32x2 u, f32x2 eh, f32x2 el) {
+    const f32x2 p = x2_mul(u, eh);
+    const f32x2 pe = x2_fma(u, el, x2_fma(u, eh, p ^ 0x8000000080000000ull));
+    const f32x2 s2 = x2_add(s, p);
+    const f32x2 bp = x2_sub(s2, s);
+    const f32x2 err = x2_add(x2_sub(s, x2_sub(s2, bp)), x2_sub(p, bp));
+    s = s2;
+    cc = x2_add(cc, x2_add(err, pe));
+}
+// (s, cc) += (s', cc') for two ranks, the high parts added exactly by TwoSum.
+__device__ __forceinline__ void dot2_merge(f32x2& s, f32x2& cc, f32x2 so, f32x2 co) {
+    const f32x2 s2 = x2_add(s, so);
+    const f32x2 bp = x2_sub(s2, s);
+    const f32x2 err = x2_add(x2_sub(s, x2_sub(s2, bp)), x2_sub(so, bp));
+    s = s2;
+    cc = x2_add(x2_add(cc, co), err);
+}
+
+// Nearest-centroid rule of one channel as fp32 comparisons.  The centroids
+// sorted ascending by (value, index), v_0 <= .. <= v_3, each position carrying
+// the lowest index that holds its value (rep), split the line at the midpoints
+// M_i = (v_i + v_{i+1}) / 2: x is nearest to v_c with c = #{i : x > M_i}, and
+// x == M_c is a tie between v_c and v_{c+1} that goes to the lower index (equal
+// neighbours share rep, so their midpoint changes nothing).  For an fp32 x,
+// x > M exactly when x > RD32(M), and x == M only if M is an fp32 value; M comes
+// exactly from the TwoSum a + b = s + e as s / 2 + e / 2 (RD32(M) = s / 2 if
+// e >= 0, else the float below it; an fp32 value iff e == 0).  Centroids must be
+// finite, with pairwise sums of magnitude >= 2^-125 or zero (s / 2 exact).
+//
+// The rule is the exact nearest centroid; fp64 |x - mu| is exact too unless x and
+// a nonzero mu differ by more than 2^29 in magnitude.  There (|x| below 2^-28 of
+// the largest |mu| or above 2^28 of the smallest nonzero |mu|) the fp64 distances
+// are compared directly, first minimum winning, so that both agree everywhere.
+struct CentroidRule {
+    float thr[3];     // RD32(M_i)
+    float teq[3];     // M_i when it is an fp32 value, else NaN
+    uint32_t rep;     // byte c: index of v_c (lowest index of its value)
+    uint32_t tie;     // byte c: min(rep_c, rep_{c+1})
+    float tiny, huge; // |x| < tiny or |x| > huge: fp64 comparison
+};
+
+__device__ __forceinline__ CentroidRule centroid_rule(float4 mu) {
+    float v[4] = {mu.x, mu.y, mu.z, mu.w};
+    int id[4] = {0, 1, 2, 3};
+    // sort (value, index) ascending: 5 compare-exchanges
+    auto cx = [&](int i, int j) {
+        if (v[i] > v[j] || (v[i] == v[j] && id[i] > id[j])) {
+            const float tv = v[i];
+            v[i] = v[j];
+            v[j] = tv;
+            const int ti = id[i];
+            id[i] = id[j];
+            id[j] = ti;
+        }
+    };
+    cx(0, 1);
+    cx(2, 3);
+    cx(0, 2);
+    cx(1, 3);
+    cx(1, 2);
+    int rp[4];
+    rp[0] = id[0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) rp[k] = v[k] == v[k - 1] ? rp[k - 1] : id[k];
+    CentroidRule R;
+    float amax = 0.0f, amin = INFINITY;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float a = fabsf(v[k]);
+        amax = fmaxf(amax, a);
+        if (a > 0.0f) amin = fminf(amin, a);
+    }
+    R.tiny = amax * 3.7252902984619141e-09f;     // 2^-28
+    R.huge = amin * 268435456.0f;                // 2^28 (inf when every mu is 0)
+    R.rep = (uint32_t)rp[0] | ((uint32_t)rp[1] << 8) | ((uint32_t)rp[2] << 16) | ((uint32_t)rp[3] << 24);
+    R.tie = 0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        float s, e;
+        two_sum(v[i], v[i + 1], s, e);
+        const float h = __fmul_rn(s, 0.5f);
+        // the float below h (h != 0 when e != 0: a nonzero exact sum never rounds to 0)
+        const float below = __int_as_float(__float_as_int(h) + (h > 0.0f ? -1 : 1));
+        R.thr[i] = e >= 0.0f ? h : below;
+        R.teq[i] = e == 0.0f ? h : __int_as_float(0x7FC00000);
+        R.tie |= (uint32_t)min(rp[i], rp[i + 1]) << (8 * i);
+    }
+    return R;
+}
+
+__device__ __noinline__ uint32_t nearest_centroid_f64(float4 mu, float x) {
+    const double xd = x;
+    const double d0 = fabs(xd - (double)mu.x), d1 = fabs(xd - (double)mu.y), d2 = fabs(xd - (double)mu.z),
+                 d3 = fabs(xd - (double)mu.w);
+    uint32_t k = 0;
+    double best = d0;
+    if (d1 < best) { best = d1; k = 1; }
+    if (d2 < best) { best = d2; k = 2; }
+    if (d3 < best) k = 3;
+    return k;
+}
+
+__device__ __forceinline__ uint32_t nearest_centroid(const CentroidRule& R, float4 mu, float x) {
+    const float ax = fabsf(x);
+    if (!(ax < INFINITY)) return 0u;                 // NaN / inf: every distance ties -> index 0
+    if (ax != 0.0f && (ax < R.tiny || ax > R.huge)) return nearest_centroid_f64(mu, x);
+    const int c = (x > R.thr[0]) + (x > R.thr[1]) + (x > R.thr[2]);
+    const float q = c == 0 ? R.teq[0] : (c == 1 ? R.teq[1] : R.teq[2]);
+    const uint32_t w = (c < 3 && x == q) ? R.tie : R.rep;
+    return (w >> (8 * c)) & 3u;
+}
+
+// Codebook block: the nearest fp32 centroid per key entry (ties to the lower
+// index), INT2 values, fp16 PSAC coefficients U^T (k - k_hat).  The residual
+// k - k_hat is kept exactly as a float pair and each coefficient is a
+// compensated dot product (TwoProduct by FMA, TwoSum accumulation: the result
+// of twice-fp32 precision), added in fp64 and rounded once to fp16.
+__device__ void encode_cb_block(float* Ks, float* Vs, int ld, int d, int nv, uint8_t* kc8, uint8_t* vc8,
+                                float* Us, unsigned char* blk, const float* cent, const float* U, int r, int rp) {
     const CbBlockOffsets o = cb_offsets(d);
-    for (int ch = threadIdx.x; ch < d; ch += blockDim.x) {
-        const double mu0 = cent[ch * 4 + 0], mu1 = cent[ch * 4 + 1], mu2 = cent[ch * 4 + 2], mu3 = cent[ch * 4 + 3];
-        for (int t = 0; t < kBlockTokens; ++t) {
-            uint8_t k = 0;
-            if (t < nv) {
-                const double x = Ks[t * ld + ch];
-                double best = fabs(x - mu0);
-                const double d1 = fabs(x - mu1), d2 = fabs(x - mu2), d3 = fabs(x - mu3);
-                if (d1 < best) { best = d1; k = 1; }
-                if (d2 < best) { best = d2; k = 2; }
-                if (d3 < best) { best = d3; k = 3; }
-            }
-            codes[t * d + ch] = k;
-        }
+    const int tid = threadIdx.x;
+    for (int e = tid; e < d * rp; e += kAppendThreads) {
+        const int c = e / rp, j = e - (e / rp) * rp;
+        Us[e] = j < r ? __ldg(U + c * r + j) : 0.0f;
+    }
+    encode_values<2>(Vs, ld, d, nv, vc8, reinterpret_cast<float2*>(blk + o.vm));
+    __syncthreads();     // V is free for the low parts of the residual
+    // keys: channel ch by tpc adjacent threads; the residual pair (high, low)
+    // overwrites (K, V) in place
+    const int tpc = kAppendThreads / d, span = kBlockTokens / tpc, part = tid % tpc;
+    const int ch = tid / tpc, t0 = part * span;
+    const float4 mu = __ldg(reinterpret_cast<const float4*>(cent) + ch);
+    const CentroidRule R = centroid_rule(mu);
+    for (int i = 0; i < span; ++i) {
+        const int t = t0 + i;
+        const float x = Ks[t * ld + ch];
+        const uint32_t k = t < nv ? nearest_centroid(R, mu, x) : 0u;
+        kc8[t * d + ch] = static_cast<uint8_t>(k);
+        float eh = 0.0f, el = 0.0f;
+        const float kh = k == 0 ? mu.x : (k == 1 ? mu.y : (k == 2 ? mu.z : mu.w));
+        if (t < nv) two_sum(x, -kh, eh, el);
+        Ks[t * ld + ch] = eh;
+        Vs[t * ld + ch] = el;
     }
     __syncthreads();
-    pack_keys<2>(codes, d, reinterpret_cast<uint32_t*>(blk + o.kc));
-    // PSAC coefficients before the scratch is reused for values
+    pack_words<2>(kc8, vc8, kBlockTokens * d / 16, reinterpret_cast<uint32_t*>(blk + o.kc),
+                  reinterpret_cast<uint32_t*>(blk + o.vc));
+    if (rp == 0) return;
+    // coefficients: thread (token t, part) sums channels part, part + 8, .. for 8
+    // ranks at a time from U staged as [d][rp] (zero past r); the 8 parts of a token
+    // are adjacent lanes, merged by a TwoSum butterfly that leaves the same pair in
+    // each of them
+    const float4* Us4 = reinterpret_cast<const float4*>(Us);
     __half* kq = reinterpret_cast<__half*>(blk + o.kq);
-    for (int e = threadIdx.x; e < kBlockTokens * rp; e += blockDim.x) {
-        const int t = e / rp, j = e % rp;
-        double acc = 0.0;
-        if (t < nv && j < r) {
-            for (int ch = 0; ch < d; ++ch) {
-                const double khat = cent[ch * 4 + codes[t * d + ch]];
-                acc += (double)U[ch * r + j] * ((double)Ks[t * ld + ch] - khat);
+    const int t = tid >> 3, prt = tid & 7;
+    const float* ehr = Ks + t * ld;
+    const float* elr = Vs + t * ld;
+    for (int j0 = 0; j0 < rp; j0 += 8) {
+        f32x2 sa[4], ca[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sa[k] = ca[k] = 0ull;
+        if (t < nv) {
+#pragma unroll 4
+            for (int c = prt; c < d; c += 8) {
+                const float eh = ehr[c], el = elr[c];
+                const f32x2 eh2 = x2(eh, eh), el2 = x2(el, el);
+                const float4 u0 = Us4[(c * rp + j0) >> 2], u1 = Us4[((c * rp + j0) >> 2) + 1];
+                dot2_step(sa[0], ca[0], x2(u0.x, u0.y), eh2, el2);
+                dot2_step(sa[1], ca[1], x2(u0.z, u0.w), eh2, el2);
+                dot2_step(sa[2], ca[2], x2(u1.x, u1.y), eh2, el2);
+                dot2_step(sa[3], ca[3], x2(u1.z, u1.w), eh2, el2);
             }
         }
-        kq[e] = __double2half(acc);
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dot2_merge(sa[k], ca[k], __shfl_xor_sync(0xffffffffu, sa[k], m),
+                           __shfl_xor_sync(0xffffffffu, ca[k], m));
+        // lane part writes rank j0 + part
+        float sv = 0.0f, cv = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 a2 = x2_split(sa[k]), c2 = x2_split(ca[k]);
+            if (prt == 2 * k) { sv = a2.x; cv = c2.x; }
+            if (prt == 2 * k + 1) { sv = a2.y; cv = c2.y; }
+        }
+        const int j = j0 + prt;
+        kq[t * rp + j] = (t < nv && j < r) ? __double2half((double)sv + (double)cv) : __float2half_rn(0.0f);
     }
-    __syncthreads();
-    quantise_values<2>(Vs, ld, d, nv, codes, reinterpret_cast<float2*>(blk + o.vm));
-    __syncthreads();
-    pack_values<2>(codes, d, reinterpret_cast<uint32_t*>(blk + o.vc));
 }
 
 // mode 0: uniform (segment `uni_seg`), 1: mixed (class per window), 2: codebook.
@@ -318,7 +465,8 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, De
             encode_int_block<2>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk);
         } else {
             const long long bh = (long long)b * c.Hkv + h;
-            encode_cb_block(Ks, Vs, ld, d, nv, codes, blk, c.centroids + bh * d * 4,
+            encode_cb_block(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d,
+                            reinterpret_cast<float*>(codes + 2 * kBlockTokens * d), blk, c.centroids + bh * d * 4,
                             c.r > 0 ? c.psac_u + bh * d * c.r : nullptr, c.r, c.rp);
         }
     }
@@ -355,15 +503,17 @@ __global__ void dequant_kernel(DevCache c, int n_tok, float* __restrict__ Kout, 
 
 }  // namespace
 
-size_t append_smem_bytes(int d) {
-    return 2 * kBlockTokens * (d + 1) * sizeof(float) + 2 * kBlockTokens * d;
+// K and V rows (fp32, padded), key and value code bytes, and for codebook blocks the
+// PSAC basis [d][rp] (fp32)
+size_t append_smem_bytes(int d, int rp) {
+    return 2 * kBlockTokens * (d + 1) * sizeof(float) + 2 * kBlockTokens * d + (size_t)d * rp * sizeof(float);
 }
 
 template <typename T>
 static kv_status launch_append_t(const void* K, const void* V, int n_tokens, const kv_cache* cache, int mode,
                                  int uni_seg, const int8_t* win_bits, int n_win, int grid_x, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
-    const size_t sm = append_smem_bytes(c.d);
+    const size_t sm = append_smem_bytes(c.d, c.kind == KV_CODEBOOK2 ? c.rp : 0);
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(append_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024);

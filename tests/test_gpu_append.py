@@ -127,3 +127,42 @@ def test_codebook_append_with_oracle_calibration():
     # only where the oracle's value sits on an fp16 rounding boundary (none expected)
     assert (data == oc.data).all()
     assert (blen == oc.blk_len).all() and (bpos == oc.blk_pos).all()
+
+
+@pytest.mark.parametrize("r", [0, 24])
+def test_codebook_append_adversarial_keys(r):
+    """Nearest-centroid decisions at their edges, bit-exact against the oracle: duplicated
+    centroids, keys exactly on midpoints (ties go to the lower index), keys next to midpoints,
+    and keys far smaller than symmetric centroids (where fp64 |x - mu| rounds to a tie)."""
+    import torch
+    rng = np.random.default_rng(7)
+    H, d, n = 1, 128, 96
+    cent = rng.normal(size=(d, 4)).astype(np.float32)
+    dup = rng.normal(size=(32, 2)).astype(np.float32)
+    cent[32:64] = dup[:, [1, 0, 1, 0]]                                    # duplicates, higher index first
+    cent[64:96] = rng.integers(-8, 8, size=(32, 4)) * 0.25                # bf16-exact midpoints
+    b = np.abs(rng.normal(size=(32, 2))).astype(np.float32)
+    cent[96:128] = np.stack([b[:, 0], -b[:, 0], -b[:, 1], b[:, 1]], 1)   # symmetric pairs
+    K = synth.to_bf16_values(rng.normal(size=(1, H, n, d)).astype(np.float32))
+    for c in range(64, 96):                                               # keys on and next to midpoints
+        mids = (cent[c][:, None].astype(np.float64) + cent[c][None, :]) / 2
+        pick = rng.choice(mids.reshape(-1), n)
+        K[0, 0, :, c] = synth.to_bf16_values(pick.astype(np.float32))
+        K[0, 0, ::3, c] = synth.to_bf16_values(np.nextafter(pick[::3].astype(np.float32), np.float32(9)))
+    tiny = np.array([0.0, -0.0, 1e-30, -1e-30, 1e-38, -1e-38, 3e-39, 1e-20], np.float32)
+    K[0, 0, :, 96:] = synth.to_bf16_values(rng.choice(tiny, (n, 32)))
+    V = synth.to_bf16_values(rng.normal(size=(1, H, n, d)).astype(np.float32))
+    nb = n // 32
+    U = None
+    if r:
+        Qh = synth.to_bf16_values(rng.normal(size=(64, d)).astype(np.float32))
+        U = OP.psac_basis(Qh, r)[0].astype(np.float32)[None, None]
+    tc = B.TorchCache(1, H, d, B.KV_CODEBOOK2, (0, 0, nb), raw_dtype=B.KV_BF16, psac_rank=r)
+    tc.centroids.copy_(torch.from_numpy(cent.reshape(-1)).cuda())
+    if r:
+        tc.psac_u.copy_(torch.from_numpy(U.reshape(-1)).cuda())
+    B.kv_quantize_append(to_dev(K, "bf16"), to_dev(V, "bf16"), B.KV_BF16, n, tc.c)
+    oc = OC.build_codebook(K, V, cent[None, None], U, nb)
+    data, blen, _ = cache_bytes(tc)
+    assert (data == oc.data).all(), np.argwhere(data != oc.data)[:8]
+    assert (blen == oc.blk_len).all()
