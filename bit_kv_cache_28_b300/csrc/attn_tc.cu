@@ -12,7 +12,7 @@
 //   warps 0-3   softmax: thread i owns query row i = TMEM lane i.  Two passes
 //               over the S row in TMEM (row maximum per 32-key group, then
 //               p = 2^(S c1 - (m + delta_g))), a lazily rescaled running max (O is
-//               rescaled only when the max grows by more than 2^8), P written
+//               rescaled only when the max grows by more than 2^15), P written
 //               back to TMEM as fp16.
 //   warps 4-11  producers: thread 0 bulk-copies (TMA engine) each packed cache
 //               tile -- 4 contiguous blocks -- into a double-buffered staging
@@ -91,9 +91,10 @@ constexpr int kCbCoeffOff = 24 * kD;        // CB2: fp16 PSAC coefficients [32][
 
 constexpr int kTile = kM * kD * 2;          // 32 KB: one 16-bit 128 x 128 operand tile
 constexpr int kWBytes = 16 * kD * 2;        // 4 KB: 16 x 128 bf16 Jensen weights
+constexpr int kExactW = 4 * kD * 4;         // 2 KB: fp32 steps [4 blocks][128] (EXACT Jensen)
 constexpr int kCoefTile = kN * 128;         // 16 KB: 128 keys x 64 fp16 PSAC coefficients (swizzled)
 constexpr int kCentBytes = kD * 8;          // 1 KB: byte-planar bf16 centroid tables
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 16;
 
 // Shared memory map (bytes from a 1024-aligned base).  INT formats: the bf16 high
 // and low parts of q^2 for the Jensen MMA; CB2: the PSAC coefficient tile and the
@@ -110,21 +111,22 @@ template <int FMT> struct Smem {
     static constexpr int stg = cent + (cb ? kCentBytes : 0);    // staged packed blocks, 2 slots
     static constexpr int stage = 4 * max_block_bytes<FMT>();
     static constexpr int info = stg + 2 * stage;
-    static constexpr int stglen = info + 2 * 32;
+    static constexpr int stglen = info + 4 * 32;            // info: a ring of 4 tiles
     static constexpr int bars = stglen + 2 * 16;
     static constexpr int slot = bars + kNumBars * 8;
     static constexpr int total = slot + 16 + 1024;              // + alignment slack
 };
 
 enum {
-    BAR_KV_FULL = 0,   // [2] producers -> MMA/softmax: K_hat, V_hat[s], W[s], info[s] ready
+    BAR_K_FULL = 0,    // [2] producers -> MMA/softmax: K_hat (+ W[s] / PSAC coefficients), info[s] ready
     BAR_V_EMPTY = 2,   // [2] P V of the stage's tile completed
     BAR_S_FULL = 4,    // [2] S and Delta of the tile in TMEM
-    BAR_P_FULL = 6,    // softmax -> MMA: P written
-    BAR_O_DONE = 7,    // P V completed
-    BAR_K_EMPTY = 8,   // Q K_hat^T completed (K_hat may be overwritten)
-    BAR_STG_FULL = 9,  // [2] staging slot filled by the bulk copy
-    BAR_STG_EMPTY = 11,  // [2] all producers finished reading the staging slot
+    BAR_P_FULL = 6,    // [2] softmax -> MMA: P of the stage's tile written
+    BAR_O_DONE = 8,    // P V completed
+    BAR_K_EMPTY = 9,   // Q K_hat^T completed (K_hat may be overwritten)
+    BAR_STG_FULL = 10,   // [2] staging slot filled by the bulk copy
+    BAR_STG_EMPTY = 12,  // [2] all producers finished reading the staging slot
+    BAR_V_FULL = 14,   // [2] producers -> MMA: V_hat[s] ready
 };
 
 struct TileInfo {
@@ -445,16 +447,35 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     auto tile_of = [&](int j) { return split + j * n_splits; };
     auto bar = [&](int i) { return sbase + M::bars + 8 * i; };
     TileInfo* infos = reinterpret_cast<TileInfo*>(sm + M::info);
+    const int nblk = c.n_blocks[seg];
+    int* stg_len = reinterpret_cast<int*>(sm + M::stglen);
+    // Bulk-copy cache tile j (if it is one) into staging slot j & 1, with its
+    // blocks' valid lengths: tiles 0 and 1 by thread 0 after the barriers are
+    // initialised, later ones by producer thread 0 two tiles ahead.
+    auto stage_copy = [&](int j) {
+        const int tile = tile_of(j);
+        if (j >= T || tile >= n_cache_tiles) return;
+        const int nb = min(4, nblk - tile * 4);
+        for (int q = 0; q < 4; ++q)
+            stg_len[(j & 1) * 4 + q] = q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
+        const uint32_t bytes = (uint32_t)(nb * bb);
+        const uint32_t sbar = bar(BAR_STG_FULL + (j & 1));
+        mbar_expect_tx(sbar, bytes);
+        bulk_g2s(sbase + M::stg + (j & 1) * M::stage, block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
+    };
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bar(BAR_KV_FULL + 0), kProd);
-        mbar_init(bar(BAR_KV_FULL + 1), kProd);
+        mbar_init(bar(BAR_K_FULL + 0), kProd);
+        mbar_init(bar(BAR_K_FULL + 1), kProd);
+        mbar_init(bar(BAR_V_FULL + 0), kProd);
+        mbar_init(bar(BAR_V_FULL + 1), kProd);
         mbar_init(bar(BAR_V_EMPTY + 0), 1);
         mbar_init(bar(BAR_V_EMPTY + 1), 1);
         mbar_init(bar(BAR_S_FULL + 0), 1);
         mbar_init(bar(BAR_S_FULL + 1), 1);
-        mbar_init(bar(BAR_P_FULL), 32 * kSoftWarps);
+        mbar_init(bar(BAR_P_FULL + 0), 32 * kSoftWarps);
+        mbar_init(bar(BAR_P_FULL + 1), 32 * kSoftWarps);
         mbar_init(bar(BAR_O_DONE), 1);
         mbar_init(bar(BAR_K_EMPTY), 1);
         mbar_init(bar(BAR_STG_FULL + 0), 1);
@@ -462,6 +483,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         mbar_init(bar(BAR_STG_EMPTY + 0), kProd);
         mbar_init(bar(BAR_STG_EMPTY + 1), kProd);
         mbar_fence_init();
+        // the first two cache tiles' copies start now, under the prologue
+        stage_copy(0);
+        stage_copy(1);
     }
     if (warp == kMmaWarp) tmem_alloc(sbase + M::slot, kTmemCols);
 
@@ -626,10 +650,11 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             long long t_prog = clock64();
             while (np < T) {
                 bool progressed = false;
-                if (np < nq && mbar_try_wait(bar(BAR_P_FULL), np & 1)) {
+                if (np < nq && mbar_test_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1) &&
+                    mbar_test_wait(bar(BAR_V_FULL + (np & 1)), (np >> 1) & 1)) {
                     issue_pv(np++);
                     progressed = true;
-                } else if (nq < T && nq <= np + 1 && mbar_try_wait(bar(BAR_KV_FULL + (nq & 1)), (nq >> 1) & 1)) {
+                } else if (nq < T && nq <= np + 1 && mbar_test_wait(bar(BAR_K_FULL + (nq & 1)), (nq >> 1) & 1)) {
                     issue_qk(nq++);
                     progressed = true;
                 }
@@ -648,74 +673,64 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     } else if (warp >= kSoftWarps) {
         // ----------------------------------------------------------- producers
         const int p = tid - 32 * kSoftWarps, pw = p >> 5;
-        const int nblk = c.n_blocks[seg];
-        int* stg_len = reinterpret_cast<int*>(sm + M::stglen);
         const float jcoef = tau * tau * (1.0f / 24.0f) * kLog2e;
-        int issued = 0;   // staging copies issued (by producer thread 0)
-        // Bulk-copy cache tile j (if it is one) into staging slot j & 1, with its
-        // blocks' valid lengths; run by producer thread 0 two tiles ahead.
-        auto stage_copy = [&](int j) {
-            const int tile = tile_of(j);
-            if (j >= T || tile >= n_cache_tiles) return;
-            const int nb = min(4, nblk - tile * 4);
-            for (int q = 0; q < 4; ++q)
-                stg_len[(j & 1) * 4 + q] =
-                    q < nb ? c.blk_len[(long long)b * c.cap_total + c.seg_base[seg] + tile * 4 + q] : 0;
-            const uint32_t bytes = (uint32_t)(nb * bb);
-            const uint32_t sbar = bar(BAR_STG_FULL + (j & 1));
-            mbar_expect_tx(sbar, bytes);
-            bulk_g2s(sbase + M::stg + (j & 1) * M::stage, block_ptr(c, b, h, seg, tile * 4), bytes, sbar);
-            issued = j + 1;
-        };
-        if (p == 0) {
-            stage_copy(0);
-            stage_copy(1);
-        }
+        int issued = min(T, 2);   // staging copies issued so far (tiles 0 and 1 by thread 0)
         int j = 0;
         for (; j < T; ++j) {
             const int s = j & 1;
             const int tile = tile_of(j);
             const bool cached = tile < n_cache_tiles;
+            // keys first: the single K_hat buffer (and W[s], the PSAC coefficients) is
+            // free once Q K_hat^T of tile j - 1 completed
             bool ok = true;
-            if (j >= 2) ok = mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
-            if (ok && cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
+            if (cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
+            if (ok && j > 0) ok = mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
             if (!__all_sync(0xffffffffu, ok)) break;
             unsigned char* stg = sm + M::stg + s * M::stage;
             const int nb = cached ? min(4, nblk - tile * 4) : 0;
             const int t0 = (tile - n_cache_tiles) * kN;
             const long long row0 = ((long long)b * c.Hkv + h) * n_cur + t0;
             const int cvalid = min(kN, n_cur - t0);
-            if (p < 4) infos[s].nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
-            if (p == 0) infos[s].quantised = cached && !kCb ? 1 : 0;
-            // values first: they only need the V_hat stage, free since P V of tile j - 2
-            unsigned char* Vt = sm + M::v + s * kTile;
-            if (cached) {
-                fill_cache_values<FMT>(Vt, stg, bb, nb, pw, lane);
-                if (!kCb && JENSEN != KV_JENSEN_OFF)
-                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef);
-            } else {
-                fill_current_values(Vt, Vcur, row0, cvalid, p);
-            }
-            // keys: the single K_hat buffer is free once Q K_hat^T of tile j - 1 completed
-            const bool ok2 = j == 0 || mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
-            if (!__all_sync(0xffffffffu, ok2)) break;
+            // tile info in a ring of 4: the softmax read tile j - 4's copy before P V of
+            // tile j - 3 was issued, which Q K^T of tile j - 1 waited for
+            TileInfo& inf = infos[j & 3];
+            if (p < 4) inf.nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
+            if (p == 0) inf.quantised = cached && !kCb ? 1 : 0;
             if (cached && kCb) {
                 fill_cb_keys(sm + M::k, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
                 if (r16 > 0) fill_coeff(sm + M::coef, stg, bb, nb, c.rp, r16 / 8, p);
             } else if (cached) {
                 fill_cache_keys<vbits<FMT>()>(sm + M::k, stg, nb, p);
+                // TAYLOR2: bf16 weights read by the Jensen MMA with Q K^T (stage s, free
+                // since Q K^T of tile j - 2 completed); EXACT: fp32 steps read by the
+                // softmax, in a ring of 4 like the tile info
+                if (JENSEN == KV_JENSEN_TAYLOR2)
+                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef);
+                else if (JENSEN == KV_JENSEN_EXACT)
+                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef);
             } else {
                 fill_current_keys(sm + M::k, Kcur, row0, cvalid, p);
             }
             fence_proxy_async();
-            mbar_arrive(bar(BAR_KV_FULL + s));
+            mbar_arrive(bar(BAR_K_FULL + s));
+            // values: the V_hat stage is free once P V of tile j - 2 completed; Q K^T and
+            // the softmax of this tile proceed meanwhile
+            const bool ok2 = j < 2 || mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
+            if (!__all_sync(0xffffffffu, ok2)) break;
+            unsigned char* Vt = sm + M::v + s * kTile;
+            if (cached) fill_cache_values<FMT>(Vt, stg, bb, nb, pw, lane);
+            else fill_current_values(Vt, Vcur, row0, cvalid, p);
+            fence_proxy_async();
+            mbar_arrive(bar(BAR_V_FULL + s));
             if (cached) {
                 // staging slot s is consumed; thread 0 refills it with tile j + 2 once
                 // every producer has arrived (a bounded wait, like all others)
                 mbar_arrive(bar(BAR_STG_EMPTY + s));
                 if (p == 0 && j + 2 < T && tile_of(j + 2) < n_cache_tiles &&
-                    mbar_wait(bar(BAR_STG_EMPTY + s), (j >> 1) & 1, &abort_flag, err, 10))
+                    mbar_wait(bar(BAR_STG_EMPTY + s), (j >> 1) & 1, &abort_flag, err, 10)) {
                     stage_copy(j + 2);
+                    issued = j + 3;
+                }
             }
         }
         if (p == 0) {
@@ -737,9 +752,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         float x[32];
         for (int j = 0; j < T; ++j) {
             const int s = j & 1;
-            const bool ok0 = mbar_wait(bar(BAR_KV_FULL + s), (j >> 1) & 1, &abort_flag, err, 4);
+            const bool ok0 = mbar_wait(bar(BAR_K_FULL + s), (j >> 1) & 1, &abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok0)) break;
-            const TileInfo info = infos[s];
+            const TileInfo info = infos[j & 3];
             const bool ok1 = mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
             if (!__all_sync(0xffffffffu, ok1)) break;
             fence_after();
@@ -751,7 +766,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
 #pragma unroll
                     for (int g = 0; g < 4; ++g) dl[g] = dv[g] + dv[4 + g];
                 } else if (JENSEN == KV_JENSEN_EXACT) {
-                    const float* SK = reinterpret_cast<const float*>(sm + M::w + s * kWBytes);
+                    const float* SK = reinterpret_cast<const float*>(sm + M::w + (j & 3) * kExactW);
                     const float jt = 0.5f * tau;
 #pragma unroll 1
                     for (int ch = 0; ch < 16; ++ch) {
@@ -786,7 +801,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 if (nv > 0) mt = fmaxf(mt, fmaf(mx, c1, -dl[g]));
             }
             const float m_new = fmaxf(m_ref, mt);
-            const bool grow = m_new > m_ref + 8.0f;       // also true for the first finite max
+            // rescale only when the max grows by more than 2^15: p <= 2^15 stays inside
+            // fp16 (max 65504) and its relative precision does not depend on the scale
+            const bool grow = m_new > m_ref + 15.0f;      // also true for the first finite max
             // O is rescaled in TMEM when any row of the warp needs it, after P V of
             // tile j - 1 has completed; tcgen05.ld/st are warp-collective, so the whole
             // warp takes the branch (alpha = 1 for rows whose running max did not move).
@@ -842,7 +859,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             l_sum += psum;
             tmem_wait_st();
             fence_before();
-            mbar_arrive(bar(BAR_P_FULL));
+            mbar_arrive(bar(BAR_P_FULL + s));
         }
         // ---- epilogue
         const int qi = q0 + i;

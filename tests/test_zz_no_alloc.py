@@ -15,6 +15,7 @@ import pytest
 from bit_kv_cache_28_b300 import bitkv as B
 from bit_kv_cache_28_b300 import synth
 from helpers import DT, gpu_uniform, out_tol, run_attention, to_dev
+from oracle import layout as OL, attention as OA
 
 pytestmark = pytest.mark.gpu
 
@@ -59,16 +60,27 @@ def test_noalloc_matches_kv_attention_on_consecutive_calls():
 
 def test_noalloc_fits_automatic_splits_into_the_array():
     """The 24-head chunk workload's automatic split count needs more scratch than the
-    array holds; the call takes fewer splits and still matches kv_attention."""
+    array holds; the call takes fewer splits.  Consecutive calls agree bit for bit, and
+    sampled rows match the oracle (the split count changes the rounding of the fp16
+    attention weights, so the two entry points are compared through the oracle rather
+    than with each other)."""
     case = synth.chunk()
     tc = gpu_uniform(case, 2)
     n = case["Q"].shape[2]
     _, splits = B.kv_attention_plan(tc.c, B.KV_BF16, n, n, 24, B.kv_attn_opts(0.0, 1, 0, 1, 0, 0))
-    ro, rl = run_attention(tc, case, jensen=1, out_f32=True)
-    for _ in range(2):
-        o, l = run_noalloc(tc, case, jensen=1, out_f32=True)
-        assert_close(o, l, ro, rl, "bf16", True)
     assert splits >= 1
+    o1, l1 = run_noalloc(tc, case, jensen=1, out_f32=True)
+    o2, l2 = run_noalloc(tc, case, jensen=1, out_f32=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    oc = OL.build_uniform(case["K_cache"], case["V_cache"], 2, case["chunks"],
+                          sum((m + 31) // 32 for m in case["chunks"]))
+    rows = np.random.default_rng(3).choice(n, 24, replace=False)
+    for h in [2, 17]:
+        view = OL.Cache(1, 1, 128, oc.classes, oc.caps)
+        view.blocks = [[oc.blocks[0][h]]]
+        ro, rl = OA.attention_over_cache(view, case["Q"][:, h:h + 1], case["K_cur"][:, h:h + 1],
+                                         case["V_cur"][:, h:h + 1], "bf16", jensen=1, rows=rows)
+        assert_close(o1[:, h:h + 1, rows], l1[:, h:h + 1, rows], ro, rl, "bf16", True)
 
 
 def test_noalloc_rejects_scratch_beyond_the_array():
