@@ -641,47 +641,162 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
             else static_cast<T*>(out)[orow * D + ch] = from_f32<T>(v);
             if (lse && ch == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         } else {
-            float* pr = part + (((long long)stream * n_splits + split) * G + gi) * (D + 2);
+            float* pr = part + (((long long)stream * n_splits + split) * G + gi) * (D + 4);
             if (ch == 0) {
                 pr[0] = M;
                 pr[1] = L;
             }
-            pr[2 + ch] = O;
+            pr[4 + ch] = O;
         }
     }
     (void)rows_out;
     if (n_splits == 1) return;
 
-    // the last CTA of this stream merges every split's partial
+    // the last CTA of this stream merges every split's partial.  All (m, l) pairs come
+    // in with one round of loads into shared memory (the warp-merge area, free now),
+    // the per-split weights are formed once per head, and each output element's
+    // partials are loaded together, so the merge costs a few L2 round trips
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(&tickets[stream], 1) == n_splits - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int e = tid; e < G * D; e += kDThreads) {
-        const int gi = e / D, ch = e % D;
-        const float* base = part + ((long long)stream * n_splits * G + gi) * (D + 2);
-        const long long sstride = (long long)G * (D + 2);
-        float M = -INFINITY;
-        for (int s = 0; s < n_splits; ++s) {
-            const float ls = __ldcg(base + s * sstride + 1);
-            if (ls > 0.0f) M = fmaxf(M, __ldcg(base + s * sstride));
-        }
-        float L = 0.0f, O = 0.0f;
-        for (int s = 0; s < n_splits; ++s) {
-            const float ls = __ldcg(base + s * sstride + 1);
-            if (ls > 0.0f) {
-                const float f = ex2(__ldcg(base + s * sstride) - M);
-                L = fmaf(ls, f, L);
-                O = fmaf(__ldcg(base + s * sstride + 2 + ch), f, O);
+    // partial rows are (m, l, -, -, o[D]): D + 4 floats, o 16-byte aligned
+    const float* pbase = part + (long long)stream * n_splits * G * (D + 4);
+    float* mls = mrg;                          // [n_splits * G] (m, l)
+    float* fws = mls + 2 * n_splits * G;       // [n_splits * G] weights 2^(m_s - m)
+    float* hml = fws + n_splits * G;           // [G] (m, l) of the merged rows
+    constexpr int kC4 = D / 4;
+    const long long sstride4 = (long long)G * (D + 4) / 4;
+    if (n_splits <= 16) {
+        // each thread takes (head, 4-channel group) slots; every split's (m, l) and the
+        // first 8 splits' 16-byte partials load together, the other 8 in a second round;
+        // the thread forms the weights itself
+        for (int e = tid; e < G * kC4; e += kDThreads) {
+            const int gi = e / kC4, c4 = e % kC4;
+            const float* row0 = pbase + (long long)gi * (D + 4);
+            const float4* o0 = reinterpret_cast<const float4*>(row0 + 4) + c4;
+            float2 ml[16];
+            float4 o[8];
+#pragma unroll
+            for (int sp = 0; sp < 16; ++sp)
+                ml[sp] = sp < n_splits ? __ldcg(reinterpret_cast<const float2*>(row0 + sp * sstride4 * 4))
+                                       : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+            for (int sp = 0; sp < 8; ++sp)
+                o[sp] = sp < n_splits ? __ldcg(o0 + sp * sstride4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float M = -INFINITY;
+#pragma unroll
+            for (int sp = 0; sp < 16; ++sp)
+                if (ml[sp].y > 0.0f) M = fmaxf(M, ml[sp].x);
+            float L = 0.0f;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                if (half == 1) {
+#pragma unroll
+                    for (int sp = 0; sp < 8; ++sp)
+                        o[sp] = 8 + sp < n_splits ? __ldcg(o0 + (8 + sp) * sstride4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp) {
+                    const float2 w = ml[8 * half + sp];
+                    const float f = w.y > 0.0f ? ex2(w.x - M) : 0.0f;
+                    L = fmaf(w.y, f, L);
+                    acc.x = fmaf(o[sp].x, f, acc.x);
+                    acc.y = fmaf(o[sp].y, f, acc.y);
+                    acc.z = fmaf(o[sp].z, f, acc.z);
+                    acc.w = fmaf(o[sp].w, f, acc.w);
+                }
             }
+            const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+            const long long orow = (long long)b * Hq + (long long)h * G + gi;
+            const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+            if (out_f32) {
+                reinterpret_cast<float4*>(static_cast<float*>(out) + orow * D)[c4] = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                T* dst = static_cast<T*>(out) + orow * D + 4 * c4;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = from_f32<T>(v[k]);
+            }
+            if (lse && c4 == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        const long long orow = (long long)b * Hq + (long long)h * G + gi;
-        const float v = L > 0.0f ? O / L : 0.0f;
-        if (out_f32) static_cast<float*>(out)[orow * D + ch] = v;
-        else static_cast<T*>(out)[orow * D + ch] = from_f32<T>(v);
-        if (lse && ch == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    } else if (3 * n_splits * G + 2 * G <= kDW * rows * (D + 2)) {
+        for (int e = tid; e < n_splits * G; e += kDThreads) {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(pbase + (long long)e * (D + 4)));
+            mls[2 * e] = v.x;
+            mls[2 * e + 1] = v.y;
+        }
+        __syncthreads();
+        for (int gi = tid; gi < G; gi += kDThreads) {
+            float M = -INFINITY;
+            for (int sp = 0; sp < n_splits; ++sp)
+                if (mls[2 * (sp * G + gi) + 1] > 0.0f) M = fmaxf(M, mls[2 * (sp * G + gi)]);
+            float L = 0.0f;
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float ls = mls[2 * (sp * G + gi) + 1];
+                const float f = ls > 0.0f ? ex2(mls[2 * (sp * G + gi)] - M) : 0.0f;
+                fws[sp * G + gi] = f;
+                L = fmaf(ls, f, L);
+            }
+            hml[2 * gi] = M;
+            hml[2 * gi + 1] = L;
+        }
+        __syncthreads();
+        // thread -> (head, 4-channel group), weights from shared memory; empty splits
+        // carry f = 0 and o = 0
+        for (int e = tid; e < G * kC4; e += kDThreads) {
+            const int gi = e / kC4, c4 = e % kC4;
+            const float4* src = reinterpret_cast<const float4*>(pbase + (long long)gi * (D + 4) + 4) + c4;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 16
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float4 o = __ldcg(src + sp * sstride4);
+                const float f = fws[sp * G + gi];
+                acc.x = fmaf(o.x, f, acc.x);
+                acc.y = fmaf(o.y, f, acc.y);
+                acc.z = fmaf(o.z, f, acc.z);
+                acc.w = fmaf(o.w, f, acc.w);
+            }
+            const float M = hml[2 * gi], L = hml[2 * gi + 1];
+            const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+            const long long orow = (long long)b * Hq + (long long)h * G + gi;
+            const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+            if (out_f32) {
+                reinterpret_cast<float4*>(static_cast<float*>(out) + orow * D)[c4] = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                T* dst = static_cast<T*>(out) + orow * D + 4 * c4;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dst[k] = from_f32<T>(v[k]);
+            }
+            if (lse && c4 == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+    } else {
+        for (int e = tid; e < G * D; e += kDThreads) {
+            const int gi = e / D, ch = e % D;
+            const float* base = pbase + (long long)gi * (D + 4);
+            const long long sstride = (long long)G * (D + 4);
+            float M = -INFINITY;
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float ls = __ldcg(base + sp * sstride + 1);
+                if (ls > 0.0f) M = fmaxf(M, __ldcg(base + sp * sstride));
+            }
+            float L = 0.0f, O = 0.0f;
+            for (int sp = 0; sp < n_splits; ++sp) {
+                const float ls = __ldcg(base + sp * sstride + 1);
+                if (ls > 0.0f) {
+                    const float f = ex2(__ldcg(base + sp * sstride) - M);
+                    L = fmaf(ls, f, L);
+                    O = fmaf(__ldcg(base + sp * sstride + 4 + ch), f, O);
+                }
+            }
+            const long long orow = (long long)b * Hq + (long long)h * G + gi;
+            const float v = L > 0.0f ? O / L : 0.0f;
+            if (out_f32) static_cast<float*>(out)[orow * D + ch] = v;
+            else static_cast<T*>(out)[orow * D + ch] = from_f32<T>(v);
+            if (lse && ch == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
     }
     if (tid == 0) tickets[stream] = 0;
 }
@@ -785,7 +900,7 @@ size_t decode_workspace(const kv_cache* cache, int Hq, int n_splits) {
     const kv_layout& L = cache->layout;
     const int G = Hq / L.Hkv;
     size_t ws = 256 + dec_ticket_bytes(cache);
-    if (n_splits > 1) ws += (size_t)L.B * L.Hkv * n_splits * G * (L.d + 2) * sizeof(float);
+    if (n_splits > 1) ws += (size_t)L.B * L.Hkv * n_splits * G * (L.d + 4) * sizeof(float);
     return ws;
 }
 
