@@ -18,9 +18,12 @@ follow the chunk-wise video-diffusion and video-VLM settings of the pages):
   weighted by 256 historical queries) and INT2 values, plus the chunk itself, with the
   rank-8 PSAC logit term; then the chunk is appended.  Calibration runs once, outside
   the step, and is reported as ``calibration_ms``.
+* ``rollout_decode``: the rollout cache (40 heads, d 128, 21 INT2 chunks = 32760 tokens)
+  read by one decode query per head plus its own token, Jensen on: the streaming path
+  over a video-diffusion cache.  One step = one split-K decode attention.
 * ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|codebook|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|codebook|rollout_decode|tiny]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 N > 1 runs independent replicas (weak scaling): every rank owns its own
@@ -83,6 +86,16 @@ def workload_spec(name):
                     append_bytes=2 * H * n * d * 2 + H * ((n + 31) // 32) * blk, jensen=0, psac=1, seed=5,
                     label=f"codebook: B1 H{H} d{d} chunk {n} cache {n_cache} codebook INT2 keys (4 centroids per "
                           f"channel, device k-means) + INT2 values, PSAC rank {r}")
+    if name == "rollout_decode":
+        H, n, d, n_chunks = 40, 1560, 128, 21
+        n_cache = n * n_chunks
+        groups = n_chunks * ((n + 31) // 32)
+        cache_bytes = H * n_cache * d * 2 * 2 / 8 + H * groups * d * 8 + H * n_cache * (d // 32) * 8
+        return dict(name=name, kind="chunkdecode", B=1, Hkv=H, Hq=H, d=d, n_q=1, n_cur=1, chunks=[n] * n_chunks,
+                    dtype="bf16", cache_bytes=cache_bytes, attn_flops=4.0 * H * (n_cache + 1) * d,
+                    append_bytes=0, jensen=1, seed=3,
+                    label=f"rollout_decode: B1 H{H} d{d}, one query per head over {n_cache} INT2 cached tokens "
+                          "(21 chunks) + its own token, Jensen taylor2, split-K")
     if name == "decode":
         B, Hq, Hkv, d, n_cache = 8, 28, 4, 64, 19600
         return dict(name=name, kind="decode", B=B, Hkv=Hkv, Hq=Hq, d=d, n_q=1, n_cur=1, n_cache=n_cache,
@@ -100,6 +113,8 @@ def make_inputs(spec):
         return synth.decode_case(spec["seed"])
     if spec["name"] == "codebook":
         return synth.codebook_case(spec["seed"])
+    if spec["kind"] == "chunkdecode":
+        return synth.chunk_case(spec["seed"], Hkv=spec["Hkv"], chunks=spec["chunks"], n_cur=1, n_q=1)
     return synth.chunk_case(spec["seed"], Hkv=spec["Hkv"], chunks=spec["chunks"], n_cur=spec["n_cur"])
 
 
@@ -359,6 +374,9 @@ def run_own(args, rank, world, dist):
     spec = workload_spec(args.workload)
     inputs = make_inputs(spec)
     r = (DecodeRunner if spec["kind"] == "decode" else ChunkRunner)(spec, inputs, dev)
+    if spec["kind"] == "chunkdecode":
+        r.launches_per_step = 1     # the decode kernel only (no append in the step)
+        r.append = lambda stream: None
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -422,7 +440,7 @@ def run_own(args, rank, world, dist):
     peaks = load_peaks()
     kernel = {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_decode_kernel"}.get(r.path)
     cache_gbs = r.cache_bytes / t_attn / 1e9
-    if spec["kind"] == "decode":
+    if spec["kind"] in ("decode", "chunkdecode"):
         roof = {"bound": "hbm", "achieved": cache_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": cache_gbs / peaks["hbm_gbs"]}
     else:
@@ -432,7 +450,8 @@ def run_own(args, rank, world, dist):
     roof.update({"traffic": traffic_for(kernel, spec["name"]), "kernel": kernel, "splits": r.splits,
                  "peak_source": peaks["source"],
                  "algorithmic": ("cache bytes (codes of valid tokens + all metadata) per launch"
-                                 if spec["kind"] == "decode" else "4 n_q (n_cache + n_cur) d FLOPs per head"),
+                                 if spec["kind"] in ("decode", "chunkdecode")
+                                 else "4 n_q (n_cache + n_cur) d FLOPs per head"),
                  "roofline_time_frac_of_step": max(r.cache_bytes / (peaks["hbm_gbs"] * 1e9),
                                                    spec["attn_flops"] / (peaks["bf16_tflops"] * 1e12)) / t_step})
     line = {
@@ -451,6 +470,8 @@ def run_own(args, rank, world, dist):
     }
     if spec["kind"] == "chunk":
         line["append_gbs"] = spec["append_bytes"] / t_app / 1e9
+    if spec["kind"] == "chunkdecode":
+        line.pop("append_ms", None)
     if getattr(r, "calib_ms", None) is not None:
         line["calibration_ms"] = r.calib_ms   # once per prefill, outside the step
     if world == 1 and not args.no_cpu_baseline:
@@ -502,6 +523,12 @@ def oracle_sample_step(spec, inputs, heads):
                                 "f16", operands="f32")
         return heads * g
     sl = slice(0, heads)
+    if spec["kind"] == "chunkdecode":
+        oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
+                              sum((n + 31) // 32 for n in spec["chunks"]))
+        OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
+                                spec["dtype"], jensen=spec["jensen"], operands="f32")
+        return spec["B"] * heads
     if spec["name"] == "codebook":
         from oracle import codebook as OC, psac as OP
         cent = np.stack([OC.fit_centroids(inputs["K_cache"][0, h]) for h in range(heads)])[None].astype(np.float32)
@@ -534,6 +561,9 @@ def sample_text(spec, heads):
     if spec["kind"] == "decode":
         return (f"{heads} kv head of sequence 0 ({heads * spec['Hq'] // spec['Hkv']} query heads): mixed cache "
                 f"build of {spec['n_cache']} tokens + decode attention, fp64 numpy")
+    if spec["kind"] == "chunkdecode":
+        return (f"{heads} head of {spec['Hq']}: cache build of {sum(spec['chunks'])} tokens + decode attention, "
+                f"fp64 numpy")
     if spec["name"] == "codebook":
         return (f"{heads} head of {spec['Hq']}: k-means + PSAC basis + cache build + attention of "
                 f"{spec['n_q']} queries + append, fp64 numpy")

@@ -114,3 +114,22 @@ def test_decode_matches_simt_path():
     o_d, l_d = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_DECODE)
     o_s, l_s = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_SIMT)
     assert np.abs(o_d - o_s).max() < 2e-3 and np.abs(l_d - l_s).max() < 2e-3
+
+
+def test_decode_over_rollout_cache_sampled():
+    """The streaming path over a video-diffusion cache at full size: one query per head over
+    the rollout cache (40 heads, 21 INT2 chunks = 32760 tokens, d 128, bf16) plus its own
+    token, Jensen TAYLOR2, automatic split-K; sampled heads against the oracle."""
+    chunks = [1560] * 21
+    case = synth.chunk_case(3, Hkv=40, chunks=chunks, n_cur=1, n_q=1)
+    tc = gpu_uniform(case, 2)
+    path, splits = B.kv_attention_plan(tc.c, B.KV_BF16, 1, 1, 40, B.kv_attn_opts(0.0, 1, 0, 1, 0, B.KV_PATH_AUTO))
+    assert path == B.KV_PATH_DECODE and splits > 1
+    o, l = run_attention(tc, case, jensen=1, out_f32=True)
+    nb = sum((n + 31) // 32 for n in chunks)
+    for h in [0, 17, 39]:
+        sl = slice(h, h + 1)
+        oc = OL.build_uniform(case["K_cache"][:, sl], case["V_cache"][:, sl], 2, chunks, nb)
+        ro, rl = OA.attention_over_cache(oc, case["Q"][:, sl], case["K_cur"][:, sl], case["V_cur"][:, sl], "bf16",
+                                         jensen=1, operands="f32")
+        check(o[:, sl], l[:, sl], ro, rl, "bf16", True)
