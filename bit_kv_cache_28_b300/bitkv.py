@@ -21,7 +21,7 @@ KV_F32, KV_F16, KV_BF16 = 0, 1, 2
 KV_UNIFORM2, KV_UNIFORM4, KV_MIXED, KV_CODEBOOK2 = 0, 1, 2, 3
 KV_SEG_RAW16, KV_SEG_INT4, KV_SEG_INT2 = 0, 1, 2
 KV_REGION_DATA, KV_REGION_BLK_LEN, KV_REGION_BLK_POS, KV_REGION_CENTROIDS, KV_REGION_PSAC_U = 0, 1, 2, 3, 4
-KV_JENSEN_OFF, KV_JENSEN_TAYLOR2, KV_JENSEN_EXACT = 0, 1, 2
+KV_JENSEN_OFF, KV_JENSEN_TAYLOR2, KV_JENSEN_EXACT, KV_JENSEN_ISOTROPIC = 0, 1, 2, 3
 KV_PATH_AUTO, KV_PATH_SIMT, KV_PATH_TC, KV_PATH_DECODE = 0, 1, 2, 3
 
 STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3: "KV_ERR_CAPACITY",

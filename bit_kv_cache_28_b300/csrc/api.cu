@@ -317,7 +317,7 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
         return set_error(KV_ERR_UNSUPPORTED, "MIXED cache: I/O dtype must equal raw_dtype");
     const kv_attn_opts dflt = {0.0f, KV_JENSEN_OFF, 0, 0, 0, KV_PATH_AUTO};
     const kv_attn_opts* o = opts ? opts : &dflt;
-    if (o->jensen < KV_JENSEN_OFF || o->jensen > KV_JENSEN_EXACT) return set_error(KV_ERR_INVALID_ARG, "bad jensen mode");
+    if (o->jensen < KV_JENSEN_OFF || o->jensen > KV_JENSEN_ISOTROPIC) return set_error(KV_ERR_INVALID_ARG, "bad jensen mode");
     if (o->psac && (L.kind != KV_CODEBOOK2 || L.psac_rank == 0 || !cache->psac_u))
         return set_error(KV_ERR_INVALID_ARG, "psac needs a CODEBOOK2 cache with psac_rank > 0 and a basis");
     const float tau = o->scale != 0.0f ? o->scale : 1.0f / sqrtf((float)L.d);

@@ -213,6 +213,7 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
     const float4* km4 = reinterpret_cast<const float4*>(blk + o.km);
     uint32_t bh[NT][D / 16][2], bl[NT][D / 16][2];
     float qz[NT], jd[NT];
+    float ss2 = 0.0f;   // ISOTROPIC: sum_c s_c^2 (jd then holds |q|^2)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) qz[nt] = jd[nt] = 0.0f;
 #pragma unroll
@@ -220,6 +221,10 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
         const float4 A = km4[(16 * kk + 2 * lc.tig) >> 1];
         const float4 Bq = km4[(16 * kk + 8 + 2 * lc.tig) >> 1];
         const float s[4] = {A.x, A.z, Bq.x, Bq.z}, z[4] = {A.y, A.w, Bq.y, Bq.w};
+        if (JENSEN == KV_JENSEN_ISOTROPIC) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ss2 = fmaf(s[e], s[e], ss2);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             float qs[4];
@@ -229,6 +234,7 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
                 qz[nt] = fmaf(q[nt][4 * kk + e], z[e], qz[nt]);
                 if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs[e], qs[e], jd[nt]);
                 else if (JENSEN == KV_JENSEN_EXACT) jd[nt] += log_sinhc(0.5f * tau * qs[e]);
+                else if (JENSEN == KV_JENSEN_ISOTROPIC) jd[nt] = fmaf(q[nt][4 * kk + e], q[nt][4 * kk + e], jd[nt]);
             }
             bh[nt][kk][0] = pack_f16(qs[0], qs[1]);
             bh[nt][kk][1] = pack_f16(qs[2], qs[3]);
@@ -240,12 +246,14 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
     }
     // bias of head g + 8 nt, then gathered for the fragment's heads 2 tig, 2 tig + 1
     float bias[NT][2];
+    const float ms2 = JENSEN == KV_JENSEN_ISOTROPIC ? quad_sum(ss2) * (1.0f / D) : 0.0f;   // mean_c s_c^2
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         float dl = 0.0f;
         if (JENSEN != KV_JENSEN_OFF) {
             dl = quad_sum(jd[nt]);
             if (JENSEN == KV_JENSEN_TAYLOR2) dl *= tau * tau * (1.0f / 24.0f);
+            else if (JENSEN == KV_JENSEN_ISOTROPIC) dl = tau * tau * (1.0f / 24.0f) * dl * ms2;
         }
         const float bq = (tau * quad_sum(qz[nt]) - dl) * kLog2e;
         bias[nt][0] = __shfl_sync(0xffffffffu, bq, (2 * lc.tig) << 2);
@@ -919,6 +927,9 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
         if (jensen == KV_JENSEN_EXACT)                                                                          \
             return launch_dec_t<T, D, NT, KV_JENSEN_EXACT>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
                                                             out_f32, lse, ws, st);                              \
+        if (jensen == KV_JENSEN_ISOTROPIC)                                                                      \
+            return launch_dec_t<T, D, NT, KV_JENSEN_ISOTROPIC>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits,     \
+                                                                out, out_f32, lse, ws, st);                     \
         return launch_dec_t<T, D, NT, KV_JENSEN_OFF>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out, out_f32, \
                                                       lse, ws, st);                                             \
     } while (0)

@@ -137,14 +137,26 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
         // Jensen correction of this block for this row
         float delta = 0.0f;
         if (quantised && jensen != KV_JENSEN_OFF) {
+            float qn2 = 0.0f, ss2 = 0.0f;    // ISOTROPIC: |q|^2 and sum_c s_c^2
             for (int ch = part; ch < D; ch += 4) {
                 const float q = Qs[row * ld + ch], s = Sk[ch];
                 if (jensen == KV_JENSEN_TAYLOR2) delta = fmaf(q * q, s * s, delta);
-                else delta += log_sinhc(0.5f * tau * q * s);
+                else if (jensen == KV_JENSEN_ISOTROPIC) {
+                    qn2 = fmaf(q, q, qn2);
+                    ss2 = fmaf(s, s, ss2);
+                } else delta += log_sinhc(0.5f * tau * q * s);
             }
-            delta += __shfl_xor_sync(0xffffffffu, delta, 1);
-            delta += __shfl_xor_sync(0xffffffffu, delta, 2);
-            if (jensen == KV_JENSEN_TAYLOR2) delta *= tau * tau * (1.0f / 24.0f);
+            if (jensen == KV_JENSEN_ISOTROPIC) {
+                qn2 += __shfl_xor_sync(0xffffffffu, qn2, 1);
+                qn2 += __shfl_xor_sync(0xffffffffu, qn2, 2);
+                ss2 += __shfl_xor_sync(0xffffffffu, ss2, 1);
+                ss2 += __shfl_xor_sync(0xffffffffu, ss2, 2);
+                delta = tau * tau * (1.0f / 24.0f) * qn2 * (ss2 * (1.0f / D));
+            } else {
+                delta += __shfl_xor_sync(0xffffffffu, delta, 1);
+                delta += __shfl_xor_sync(0xffffffffu, delta, 2);
+                if (jensen == KV_JENSEN_TAYLOR2) delta *= tau * tau * (1.0f / 24.0f);
+            }
         }
         float lg[kSK / 4];
         float tmax = -INFINITY;

@@ -96,6 +96,13 @@ constexpr int kCoefTile = kN * 128;         // 16 KB: 128 keys x 64 fp16 PSAC co
 constexpr int kCentBytes = kD * 8;          // 1 KB: byte-planar bf16 centroid tables
 constexpr int kNumBars = 16;
 
+struct TileInfo {
+    int nvalid[4];
+    int quantised;
+    int pad[3];
+    float ss2[4][2];   // ISOTROPIC: sum of s_c^2 of block g over channels 0-63 and 64-127
+};
+
 // Shared memory map (bytes from a 1024-aligned base).  INT formats: the bf16 high
 // and low parts of q^2 for the Jensen MMA; CB2: the PSAC coefficient tile and the
 // centroid tables instead.
@@ -111,7 +118,7 @@ template <int FMT> struct Smem {
     static constexpr int stg = cent + (cb ? kCentBytes : 0);    // staged packed blocks, 2 slots
     static constexpr int stage = 4 * max_block_bytes<FMT>();
     static constexpr int info = stg + 2 * stage;
-    static constexpr int stglen = info + 4 * 32;            // info: a ring of 4 tiles
+    static constexpr int stglen = info + 4 * (int)sizeof(TileInfo);   // info: a ring of 4 tiles
     static constexpr int bars = stglen + 2 * 16;
     static constexpr int slot = bars + kNumBars * 8;
     static constexpr int total = slot + 16 + 1024;              // + alignment slack
@@ -127,12 +134,6 @@ enum {
     BAR_STG_FULL = 10,   // [2] staging slot filled by the bulk copy
     BAR_STG_EMPTY = 12,  // [2] all producers finished reading the staging slot
     BAR_V_FULL = 14,   // [2] producers -> MMA: V_hat[s] ready
-};
-
-struct TileInfo {
-    int nvalid[4];
-    int quantised;
-    int pad[3];
 };
 
 // Byte offset of 16-byte chunk `ch` of row `row` in a `rows`-row x 128-column
@@ -346,8 +347,11 @@ __device__ __forceinline__ void fill_coeff(unsigned char* Ct, const unsigned cha
 // Jensen weights of a staged tile.  TAYLOR2: W rows g and 4 + g hold the bf16
 // high and low parts of w_c = s_c^2 tau^2 / 24 log2(e) of block g (zero for
 // missing blocks); rows 8-15 stay zero.  EXACT: the block steps s_c as fp32 [4][128].
+// ISOTROPIC: the two warps of block g each sum s_c^2 over their 64 channels into
+// ss2[g][w] (the softmax adds the two in a fixed order).
 template <int BITS, int JENSEN>
-__device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned char* stg, int nb, int p, float coef) {
+__device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned char* stg, int nb, int p, float coef,
+                                             float (*ss2)[2] = nullptr) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
     const int g = p >> 6, c = 2 * (p & 63);
     float2 s = make_float2(0.0f, 0.0f);
@@ -366,6 +370,9 @@ __device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned ch
         *reinterpret_cast<uint32_t*>(W + sw_off(4 + g, c >> 3, 16) + cb) = lo;
     } else if (JENSEN == KV_JENSEN_EXACT) {
         reinterpret_cast<float2*>(W)[(g * kD + c) >> 1] = s;
+    } else if (JENSEN == KV_JENSEN_ISOTROPIC) {
+        const float v = warp_sum(fmaf(s.x, s.x, s.y * s.y));
+        if ((p & 31) == 0) ss2[g][(p >> 5) & 1] = v;
     }
 }
 
@@ -708,6 +715,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef);
                 else if (JENSEN == KV_JENSEN_EXACT)
                     fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef);
+                else if (JENSEN == KV_JENSEN_ISOTROPIC)
+                    fill_weights<vbits<FMT>(), JENSEN>(nullptr, stg, nb, p, jcoef, inf.ss2);
             } else {
                 fill_current_keys(sm + M::k, Kcur, row0, cvalid, p);
             }
@@ -748,6 +757,21 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         const int i = tid;                          // query row = TMEM lane
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const float c1 = tau * kLog2e;
+        // ISOTROPIC: (tau^2 / 24) log2(e) |q|^2 / d of this row, times a block's sum of s_c^2
+        float iso_c = 0.0f;
+        if (JENSEN == KV_JENSEN_ISOTROPIC) {
+            float qn2 = 0.0f;
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint4 qv = q0 + i < n_q ? __ldg(Qg + (long long)(q0 + i) * (kD / 8) + ch) : make_uint4(0, 0, 0, 0);
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float lo = __uint_as_float(qw[k] << 16), hi = __uint_as_float(qw[k] & 0xFFFF0000u);
+                    qn2 = fmaf(lo, lo, fmaf(hi, hi, qn2));
+                }
+            }
+            iso_c = tau * tau * (1.0f / 24.0f) * kLog2e * qn2 * (1.0f / kD);
+        }
         float m_ref = -INFINITY, l_sum = 0.0f;
         float x[32];
         for (int j = 0; j < T; ++j) {
@@ -782,6 +806,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     }
 #pragma unroll
                     for (int g = 0; g < 4; ++g) dl[g] *= kLog2e;
+                } else if (JENSEN == KV_JENSEN_ISOTROPIC) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) dl[g] = iso_c * (info.ss2[g][0] + info.ss2[g][1]);
                 }
             }
             // pass 1: the tile's maximum of the corrected logits (log2 units)
@@ -1022,6 +1049,10 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
         case KV_JENSEN_EXACT:                                                                                 \
             s = launch_tc_t<FMT, KV_JENSEN_EXACT>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32, \
                                                   lse, ws_o, ws_ml, err, st);                                 \
+            break;                                                                                            \
+        case KV_JENSEN_ISOTROPIC:                                                                             \
+            s = launch_tc_t<FMT, KV_JENSEN_ISOTROPIC>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out,    \
+                                                      out_f32, lse, ws_o, ws_ml, err, st);                    \
             break;                                                                                            \
         default:                                                                                              \
             s = launch_tc_t<FMT, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32,   \

@@ -115,7 +115,7 @@ typedef struct {
     const int8_t* window_bits_dev;
 } kv_append_opts;
 
-typedef enum { KV_JENSEN_OFF = 0, KV_JENSEN_TAYLOR2 = 1, KV_JENSEN_EXACT = 2 } kv_jensen;
+typedef enum { KV_JENSEN_OFF = 0, KV_JENSEN_TAYLOR2 = 1, KV_JENSEN_EXACT = 2, KV_JENSEN_ISOTROPIC = 3 } kv_jensen;
 
 typedef enum {
     KV_PATH_AUTO = 0,   /* decode kernel for n_q == 1, tensor-core kernel for bf16 d=128 chunks, else SIMT */
@@ -177,7 +177,9 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
  * unquantised and bidirectional).  l_ij = tau q_i.k_hat_j - delta_ij (+ PSAC)
  * for cached keys, tau q_i.k_j for current keys.  Jensen delta ([JB]):
  * TAYLOR2 (tau^2/24) sum_c q_c^2 s_c^2, EXACT sum_c log(sinh x_c / x_c) with
- * x_c = tau q_c s_c / 2, using the step sizes of the key's group; zero for
+ * x_c = tau q_c s_c / 2, ISOTROPIC (tau^2/24) |q|^2 mean_c s_c^2 (the query-norm
+ * form; equal to TAYLOR2 when a group's steps are equal), using the step sizes
+ * of the key's group; zero for
  * RAW16 windows and codebook keys.  Dequantised cache entries are rounded to
  * the I/O dtype before the products.
  *   Q (device) [B][Hq][n_q][d]; Kcur, Vcur (device) [B][Hkv][n_cur][d] (may be

@@ -17,6 +17,13 @@ so the corrected cached logit is  tau q.k_hat - delta  with
     delta_exact   = sum_c log(sinh(x_c) / x_c)
     delta_taylor2 = sum_c x_c^2 / 6 = (tau^2 / 24) sum_c q_c^2 s_c^2
 
+and, in the abstract's "query norm" form that treats the noise as isotropic (one
+step for every channel, the group's mean square step),
+
+    delta_isotropic = (tau^2 / 24) |q|^2 mean_c s_c^2,
+
+which equals delta_taylor2 whenever a group's steps are all equal.
+
 applied to quantised cached keys only (zero for RAW16 windows and the current
 chunk).  All sums and the softmax are fp64; the output is returned in fp64.
 """
@@ -29,7 +36,7 @@ from .quant import round_to
 
 F64 = np.float64
 
-JENSEN_OFF, JENSEN_TAYLOR2, JENSEN_EXACT = 0, 1, 2
+JENSEN_OFF, JENSEN_TAYLOR2, JENSEN_EXACT, JENSEN_ISOTROPIC = 0, 1, 2, 3
 
 
 def log_sinhc(x):
@@ -59,6 +66,10 @@ def jensen_delta(Q, s_groups, tau, mode):
     if mode == JENSEN_EXACT:
         x = 0.5 * tau * Q[:, None, :] * S[None, :, :]
         return log_sinhc(x).sum(-1)
+    if mode == JENSEN_ISOTROPIC:
+        qn2 = (Q * Q).sum(-1)                      # |q|^2
+        ms2 = (S * S).mean(-1)                     # mean_c s_c^2 of each group
+        return (tau * tau / 24.0) * qn2[:, None] * ms2[None, :]
     raise ValueError(mode)
 
 

@@ -28,7 +28,7 @@ def oracle_uniform(case, bits):
                             sum((n + 31) // 32 for n in case["chunks"]))
 
 
-@pytest.mark.parametrize("jensen", [0, 1, 2])
+@pytest.mark.parametrize("jensen", [0, 1, 2, 3])
 def test_tiny_workload(jensen):
     case = synth.tiny()
     tc = gpu_uniform(case, 2)
@@ -40,7 +40,7 @@ def test_tiny_workload(jensen):
 
 
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("jensen", [0, 1, 2])
+@pytest.mark.parametrize("jensen", [0, 1, 2, 3])
 @pytest.mark.parametrize("out_f32", [True, False])
 def test_chunk_small_simt(bits, jensen, out_f32):
     case = synth.chunk_case(51, B=2, Hkv=2, Hq=4, d=128, chunks=[100, 77], n_cur=45, dtype="bf16")
@@ -135,7 +135,7 @@ def test_chunk_workload_simt_sampled():
 # ------------------------------------------------------ tensor-core path -----
 
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("jensen", [0, 1, 2])
+@pytest.mark.parametrize("jensen", [0, 1, 2, 3])
 def test_chunk_small_tc(bits, jensen):
     """tcgen05 kernel: ragged cache blocks, ragged current tile, partial query tile, GQA."""
     case = synth.chunk_case(61, B=2, Hkv=2, Hq=4, d=128, chunks=[300, 77], n_cur=150, n_q=150, dtype="bf16")

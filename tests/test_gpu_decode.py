@@ -43,7 +43,7 @@ def test_decode_workload_full():
     tc, oc = mixed_case(case)
     path, splits = B.kv_attention_plan(tc.c, B.KV_F16, 1, 1, 28)
     assert path == B.KV_PATH_DECODE and splits > 1
-    for jensen in (0, 1):
+    for jensen in (0, 1, 3):
         ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=jensen, operands="f32")
         o, l = run_attention(tc, case, jensen=jensen, out_f32=True)
         check(o, l, ro, rl, "f16", True)
@@ -61,7 +61,7 @@ def test_decode_mixed_ragged(dtype, n_cur):
         case["K_cur"] = synth.to_dtype_values(rng.standard_normal((3, 2, n_cur, 64)), dtype)
         case["V_cur"] = synth.to_dtype_values(rng.standard_normal((3, 2, n_cur, 64)), dtype)
     tc, oc = mixed_case(case)
-    for jensen in (0, 1, 2):
+    for jensen in (0, 1, 2, 3):
         ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], dtype, jensen=jensen, operands="f32")
         for splits in (1, 3, 7):
             o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
@@ -76,7 +76,7 @@ def test_decode_uniform(bits, d, Hq, Hkv):
     tc = gpu_uniform(case, bits)
     oc = OL.build_uniform(case["K_cache"], case["V_cache"], bits, case["chunks"],
                           sum((n + 31) // 32 for n in case["chunks"]))
-    for jensen in (0, 1):
+    for jensen in (0, 1, 3):
         ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen, operands="f32")
         for splits in (0, 2):
             o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)

@@ -133,10 +133,29 @@ def test_taylor2_is_second_order_of_exact():
     assert abs(t2[1, 2] - tau * tau / 24 * np.sum(Q[1] ** 2 * S[2] ** 2)) < 1e-15
 
 
+def test_isotropic_jensen_pins():
+    """The query-norm form (tau^2/24)|q|^2 mean_c s_c^2: a hand value, equality with TAYLOR2
+    whenever a group's steps are equal, and a difference from it when they are not."""
+    # hand value: q = (1, 2, 0, 0), s = (2, 0, 4, 2), tau = 1/2: |q|^2 = 5, mean s^2 = 24/4 = 6,
+    # delta = (1/4)/24 * 30 = 0.3125
+    d = A.jensen_delta(np.array([[1.0, 2.0, 0.0, 0.0]]), np.array([[2.0, 0.0, 4.0, 2.0]]), 0.5,
+                       A.JENSEN_ISOTROPIC)
+    assert abs(d[0, 0] - 0.3125) < 1e-15
+    rng = np.random.default_rng(7)
+    Q = rng.standard_normal((5, 32))
+    S = np.repeat(rng.uniform(0.1, 2.0, (6, 1)), 32, axis=1)     # equal steps within each group
+    tau = 1 / np.sqrt(32)
+    iso = A.jensen_delta(Q, S, tau, A.JENSEN_ISOTROPIC)
+    t2 = A.jensen_delta(Q, S, tau, A.JENSEN_TAYLOR2)
+    assert np.abs(iso - t2).max() < 1e-12 * np.abs(t2).max()
+    S2 = rng.uniform(0.1, 2.0, (6, 32))
+    assert np.abs(A.jensen_delta(Q, S2, tau, A.JENSEN_ISOTROPIC) - A.jensen_delta(Q, S2, tau, A.JENSEN_TAYLOR2)).max() > 1e-3
+
+
 def test_jensen_special_cases():
     Q = np.zeros((2, 8))
     S = np.ones((3, 8))
-    for mode in (A.JENSEN_TAYLOR2, A.JENSEN_EXACT):
+    for mode in (A.JENSEN_TAYLOR2, A.JENSEN_EXACT, A.JENSEN_ISOTROPIC):
         assert np.abs(A.jensen_delta(Q, S, 0.3, mode)).max() == 0
         assert np.abs(A.jensen_delta(np.ones((2, 8)), np.zeros((3, 8)), 0.3, mode)).max() == 0
         assert (A.jensen_delta(np.ones((1, 8)), S, 0.3, mode) > 0).all()
