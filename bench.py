@@ -24,6 +24,7 @@ follow the chunk-wise video-diffusion and video-VLM settings of the pages):
 * ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|codebook|rollout_decode|tiny]
+                    [--jensen 0|1|2|3]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 N > 1 runs independent replicas (weak scaling): every rank owns its own
@@ -366,12 +367,24 @@ class DecodeRunner:
         pass
 
 
+def with_jensen(spec, jensen):
+    """The workload with its Jensen mode overridden (None keeps the workload's own)."""
+    if jensen is None or jensen == spec["jensen"]:
+        return spec
+    names = {0: "off", 1: "taylor2", 2: "exact", 3: "isotropic"}
+    spec = dict(spec, jensen=jensen)
+    spec["label"] = spec["label"].replace("Jensen taylor2", f"Jensen {names[jensen]}")
+    if "Jensen" not in spec["label"]:
+        spec["label"] += f", Jensen {names[jensen]}"
+    return spec
+
+
 def run_own(args, rank, world, dist):
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = workload_spec(args.workload)
+    spec = with_jensen(workload_spec(args.workload), args.jensen)
     inputs = make_inputs(spec)
     r = (DecodeRunner if spec["kind"] == "decode" else ChunkRunner)(spec, inputs, dev)
     if spec["kind"] == "chunkdecode":
@@ -589,7 +602,7 @@ def cpu_baseline(spec, inputs):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    spec = workload_spec(args.workload)
+    spec = with_jensen(workload_spec(args.workload), args.jensen)
     inputs = make_inputs(spec)
     heads = 1
     for _ in range(args.warmup):
@@ -619,6 +632,8 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--workload", default="chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--jensen", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="override the workload's Jensen mode (0 off, 1 TAYLOR2, 2 EXACT, 3 ISOTROPIC)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "own" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
