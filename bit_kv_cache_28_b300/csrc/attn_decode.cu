@@ -473,7 +473,8 @@ template <typename T, int D, int NT, int JENSEN>
 __global__ void __launch_bounds__(kDThreads, (D == 64 && NT == 1) ? 4 : ((D == 128 && NT == 2) ? 1 : 2))
 attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* __restrict__ Vcur, int n_cur, int Hq,
                    DevCache c, float tau, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
-                   float* __restrict__ lse, float* __restrict__ part, int* __restrict__ tickets, int* __restrict__ err) {
+                   float* __restrict__ lse, float* __restrict__ part, int* __restrict__ tickets, int* __restrict__ err,
+                   int stall) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
     __shared__ int s_last;
@@ -490,7 +491,12 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     const uint32_t bar0 = smem_u32(mrg + kDW * sh.rows * (D + 2));
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)(warp * nsw + i); };
 
-    if (tid == 0) abort_flag = 0;
+    // bar0 + 8 kDW nsw: a barrier nothing arrives on, the target of the injected stall
+    // (failure tests)
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar0 + 8u * (uint32_t)(kDW * nsw), 1);
+    }
     if (lane == 0)
         for (int i = 0; i < nsw; ++i) mbar_init(bar(i), 1);
     mbar_fence_init();
@@ -562,7 +568,11 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
                 len_next = c.blk_len[(long long)b * c.cap_total + c.seg_base[sg] + ix];
             }
         }
-        const bool ok = mbar_wait(bar(k % nsw), (k / nsw) & 1, &abort_flag, err, 1);
+        // (failure tests: with `stall` the first wait targets a barrier nothing arrives on,
+        // with a short limit, so the bounded-wait abort path runs)
+        const bool ok = stall && k == 0
+                            ? mbar_wait(bar0 + 8u * (uint32_t)(kDW * nsw), 0, &abort_flag, err, 12, 1LL << 21)
+                            : mbar_wait(bar(k % nsw), (k / nsw) & 1, &abort_flag, err, 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         int seg, idx;
         locate(lo + warp + kDW * k, seg, idx);
@@ -836,7 +846,7 @@ DecShape dec_shape(const kv_cache* cache, int Hq) {
 
 size_t dec_smem_bytes(const DecShape& sh, int d) {
     return 1024 + (size_t)kDW * sh.nsw * sh.slot_bytes + (size_t)kDW * sh.rows * (d + 2) * sizeof(float) +
-           (size_t)kDW * sh.nsw * 8;
+           (size_t)kDW * sh.nsw * 8 + 8;
 }
 
 size_t dec_ticket_bytes(const kv_cache* cache) {
@@ -866,7 +876,7 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     dim3 grid(n_splits, c.Hkv, c.B);
     attn_decode_kernel<T, D, NT, JENSEN><<<grid, kDThreads, smem, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
-        sh, out, out_f32, lse, part, tickets, err);
+        sh, out, out_f32, lse, part, tickets, err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
     kv_status s = check_launch("attn_decode_kernel");
     if (s != KV_OK) return s;
     if (getenv("BITKV_DEBUG_SYNC")) {

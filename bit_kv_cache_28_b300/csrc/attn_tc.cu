@@ -94,7 +94,7 @@ constexpr int kWBytes = 16 * kD * 2;        // 4 KB: 16 x 128 bf16 Jensen weight
 constexpr int kExactW = 4 * kD * 4;         // 2 KB: fp32 steps [4 blocks][128] (EXACT Jensen)
 constexpr int kCoefTile = kN * 128;         // 16 KB: 128 keys x 64 fp16 PSAC coefficients (swizzled)
 constexpr int kCentBytes = kD * 8;          // 1 KB: byte-planar bf16 centroid tables
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;
 
 struct TileInfo {
     int nvalid[4];
@@ -134,6 +134,8 @@ enum {
     BAR_STG_FULL = 10,   // [2] staging slot filled by the bulk copy
     BAR_STG_EMPTY = 12,  // [2] all producers finished reading the staging slot
     BAR_V_FULL = 14,   // [2] producers -> MMA: V_hat[s] ready
+    BAR_MMA_DONE = 16, // every MMA the issuer started has completed (before TMEM is freed)
+    BAR_NEVER = 17,    // never arrived on: the target of the injected stall (failure tests)
 };
 
 // Byte offset of 16-byte chunk `ch` of row `row` in a `rows`-row x 128-column
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kcur,
                const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau, int r16,
                int n_splits, void* __restrict__ out, int out_f32, float* __restrict__ lse, float* __restrict__ ws_o,
-               float2* __restrict__ ws_ml, int* __restrict__ err) {
+               float2* __restrict__ ws_ml, int* __restrict__ err, int stall) {
     using M = Smem<FMT>;
     constexpr bool kCb = FMT == FMT_CB2;
     extern __shared__ unsigned char smem_raw[];
@@ -477,6 +479,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         mbar_init(bar(BAR_K_FULL + 1), kProd);
         mbar_init(bar(BAR_V_FULL + 0), kProd);
         mbar_init(bar(BAR_V_FULL + 1), kProd);
+        mbar_init(bar(BAR_MMA_DONE), 1);
+        mbar_init(bar(BAR_NEVER), 1);
         mbar_init(bar(BAR_V_EMPTY + 0), 1);
         mbar_init(bar(BAR_V_EMPTY + 1), 1);
         mbar_init(bar(BAR_S_FULL + 0), 1);
@@ -675,6 +679,11 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     break;
                 }
             }
+            // every MMA issued so far completes before TMEM is freed (also after an abort)
+            mma_commit(bar(BAR_MMA_DONE));
+            const long long t_done = clock64();
+            while (!mbar_try_wait(bar(BAR_MMA_DONE), 0) && clock64() - t_done < 100000000LL) {
+            }
         }
         __syncwarp();
     } else if (warp >= kSoftWarps) {
@@ -779,7 +788,10 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             const bool ok0 = mbar_wait(bar(BAR_K_FULL + s), (j >> 1) & 1, &abort_flag, err, 4);
             if (!__all_sync(0xffffffffu, ok0)) break;
             const TileInfo info = infos[j & 3];
-            const bool ok1 = mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
+            // (failure tests: with `stall` the first wait targets a barrier nothing arrives
+            // on, with a short limit, so the bounded-wait abort path runs)
+            const bool ok1 = stall && j == 0 ? mbar_wait(bar(BAR_NEVER), 0, &abort_flag, err, 12, 1LL << 21)
+                                             : mbar_wait(bar(BAR_S_FULL + s), (j >> 1) & 1, &abort_flag, err, 5);
             if (!__all_sync(0xffffffffu, ok1)) break;
             fence_after();
             float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -981,7 +993,7 @@ kv_status launch_tc_t(const DevCache& c, const void* Q, const void* Kc, const vo
     attn_tc_kernel<FMT, JENSEN><<<grid, kThreads, kSmem, st>>>(
         static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
         static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, r16, n_splits, out, out_f32, lse, ws_o, ws_ml,
-        err);
+        err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
     return check_launch("attn_tc_kernel");
 }
 

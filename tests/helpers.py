@@ -76,12 +76,22 @@ def run_attention(tc, case, jensen=0, out_f32=False, path=B.KV_PATH_AUTO, splits
     kc = to_dev(Kcur, dt) if n_cur else None
     vc = to_dev(Vcur, dt) if n_cur else None
     opts = B.kv_attn_opts(0.0, jensen, psac, 1 if out_f32 else 0, splits, path)
-    out = torch.empty((Bn, Hq, nq, d), dtype=torch.float32 if out_f32 else torch_dtype(dt), device="cuda")
-    lse = torch.empty((Bn, Hq, nq), dtype=torch.float32, device="cuda")
+    # out and lse sit between canary guard bands (16 KB of a fixed byte pattern on each
+    # side), checked after the call: a kernel writing outside its outputs fails the test
+    odt = torch.float32 if out_f32 else torch_dtype(dt)
+    n_out, n_lse = Bn * Hq * nq * d, Bn * Hq * nq
+    G = 16384
+    ob = torch.full((2 * G + n_out * torch.empty((), dtype=odt).element_size(),), 0x5A, dtype=torch.uint8,
+                    device="cuda")
+    lb = torch.full((2 * G + 4 * n_lse,), 0x5A, dtype=torch.uint8, device="cuda")
+    out = ob[G:G + n_out * torch.empty((), dtype=odt).element_size()].view(odt).view(Bn, Hq, nq, d)
+    lse = lb[G:G + 4 * n_lse].view(torch.float32).view(Bn, Hq, nq)
     ws_bytes = B.kv_attention_workspace(tc.c, DT[dt], nq, n_cur, Hq, opts)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
     B.kv_attention(q, kc, vc, DT[dt], nq, n_cur, Hq, tc.c, opts, out, lse, ws, ws_bytes)
     torch.cuda.synchronize()
+    for buf, n in ((ob, ob.numel()), (lb, lb.numel())):
+        assert bool((buf[:G] == 0x5A).all()) and bool((buf[n - G:] == 0x5A).all()), "write outside the output"
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
