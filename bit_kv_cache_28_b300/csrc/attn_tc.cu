@@ -29,7 +29,8 @@
 //               of group g's weights), and O += P V_hat with P read from tensor
 //               memory (fp16).
 // TMEM columns: S double buffer 0-255 (a tile's P overwrites the first 64
-// columns of its S once they are read), O 256-383, Delta double buffer
+// columns of its S once they are read; Q K^T of the tile two later is issued
+// only after P V of this one has completed), O 256-383, Delta double buffer
 // 384-415, Q 448-511.  Every wait is bounded; every warp-collective tcgen05
 // load/store runs with the whole warp converged.
 //
@@ -655,8 +656,11 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             // Issue Q K^T of tile j as soon as its operands are staged and P V of
             // tile i as soon as its P is written, whichever is ready first (P V of a
             // tile frees the V stage the producers refill next).  Q K^T of tile j
-            // reuses tile j - 2's S columns, so it waits for P V of tile j - 2 to be
-            // issued.  The wait is bounded: no progress for ~2^30 cycles gives up.
+            // writes the S columns that P V of tile j - 2 reads its P from.  MMAs into
+            // different accumulators are not ordered with one another, so Q K^T of
+            // tile j waits until P V of tile j - 2 has completed (its V stage's empty
+            // barrier, which nothing else can have advanced past it yet).  The wait is
+            // bounded: no progress for ~2^30 cycles gives up.
             int nq = 0, np = 0;
             long long t_prog = clock64();
             while (np < T) {
@@ -665,7 +669,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     mbar_test_wait(bar(BAR_V_FULL + (np & 1)), (np >> 1) & 1)) {
                     issue_pv(np++);
                     progressed = true;
-                } else if (nq < T && nq <= np + 1 && mbar_test_wait(bar(BAR_K_FULL + (nq & 1)), (nq >> 1) & 1)) {
+                } else if (nq < T && nq <= np + 1 && mbar_test_wait(bar(BAR_K_FULL + (nq & 1)), (nq >> 1) & 1) &&
+                           (nq < 2 || mbar_test_wait(bar(BAR_V_EMPTY + (nq & 1)), ((nq - 2) >> 1) & 1))) {
                     issue_qk(nq++);
                     progressed = true;
                 }
