@@ -134,6 +134,27 @@ def test_chunk_workload_simt_sampled():
 
 # ------------------------------------------------------ tensor-core path -----
 
+@pytest.mark.parametrize("jensen", [2, 1])
+def test_tc_repeated_runs_identical(jensen):
+    """tcgen05 kernel: 200 repeated calls on one input give bit-identical outputs within the
+    oracle's tolerance.  The EXACT softmax is slow, so Q K^T of tile j and P V of tile j - 2
+    (which share TMEM columns) are issued back to back; an ordering race between them showed
+    as an occasional wrong output here."""
+    case = synth.chunk_case(61, B=2, Hkv=2, Hq=4, d=128, chunks=[300, 77], n_cur=150, n_q=150, dtype="bf16")
+    tc = gpu_uniform(case, 2)
+    oc = oracle_uniform(case, 2)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen)
+    for splits in (3, 1):
+        first = None
+        for _ in range(200):
+            o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_TC, splits=splits)
+            if first is None:
+                check(o, l, ro, rl, "bf16", True)
+                first = (o, l)
+            else:
+                assert np.array_equal(o, first[0]) and np.array_equal(l, first[1])
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("jensen", [0, 1, 2, 3])
 def test_chunk_small_tc(bits, jensen):
