@@ -45,6 +45,60 @@ def test_window_plan_unforced_and_degenerate():
     assert bits.size == 0 and perm.size == 0
 
 
+def test_window_similarity_closed_forms():
+    """Cosine of window means to the question mean (WindowQuant note, 何が新しいのか):
+    a window along the question gives 1, against it -1, orthogonal to it 0; a zero
+    window or an empty question gives 0."""
+    rng = np.random.default_rng(11)
+    H, d, m = 2, 4, 3
+    Kq = rng.normal(size=(1, H, m, d))
+    v = Kq[0].mean(axis=1)                                   # [H, d]
+    vf = v.reshape(-1)
+    r = rng.normal(size=H * d)
+    orth = (r - (r @ vf) / (vf @ vf) * vf).reshape(H, d)     # Gram-Schmidt: orth . v = 0
+    n = 5 * 32 + 7
+    K = rng.normal(size=(1, H, n, d))
+    K[0, :, 0:32] = 2.5 * v[:, None, :]
+    K[0, :, 32:64] = -0.1 * v[:, None, :]
+    K[0, :, 64:96] = orth[:, None, :]
+    K[0, :, 96:128] = 0.0
+    # window 4: tokens whose deviations from 3 v cancel over the window
+    dev = rng.normal(size=(H, 16, d))
+    K[0, :, 128:160] = 3.0 * v[:, None, :] + np.concatenate([dev, -dev], axis=1)
+    K[0, :, 160:] = -v[:, None, :] + 0.0                      # partial window of 7 tokens
+    sim = window.window_similarity(K, Kq)
+    assert sim.shape == (1, 6)
+    assert abs(sim[0, 0] - 1.0) < 1e-12 and abs(sim[0, 1] + 1.0) < 1e-12
+    assert abs(sim[0, 2]) < 1e-12 and sim[0, 3] == 0.0
+    assert abs(sim[0, 4] - 1.0) < 1e-12 and abs(sim[0, 5] + 1.0) < 1e-12
+    assert np.all(window.window_similarity(K, Kq[:, :, :0]) == 0.0)
+
+
+def test_window_similarity_library_and_symmetries():
+    """Against scipy's cosine distance on the concatenated means; invariant to positive
+    scalings, token order inside a window and a common permutation of the kv heads;
+    odd in the question."""
+    from scipy.spatial.distance import cosine
+    rng = np.random.default_rng(12)
+    B, H, n, m, d = 2, 3, 3 * 32 + 10, 5, 8
+    K = rng.normal(size=(B, H, n, d))
+    K[:, :, :, 2] *= 8.0                                      # an outlier channel
+    Kq = rng.normal(size=(B, H, m, d))
+    sim = window.window_similarity(K, Kq)
+    for b in range(B):
+        v = Kq[b].mean(axis=1).reshape(-1)
+        for w in range(sim.shape[1]):
+            u = K[b, :, 32 * w:32 * w + 32].mean(axis=1).reshape(-1)
+            assert abs(sim[b, w] - (1.0 - cosine(u, v))) < 1e-12
+    assert np.allclose(window.window_similarity(3.0 * K, 0.5 * Kq), sim, atol=1e-12)
+    assert np.allclose(window.window_similarity(K, -Kq), -sim, atol=1e-12)
+    Kp = K.copy()
+    Kp[:, :, 32:64] = K[:, :, 32:64][:, :, rng.permutation(32)]
+    assert np.allclose(window.window_similarity(Kp, Kq), sim, atol=1e-12)
+    hp = [2, 0, 1]
+    assert np.allclose(window.window_similarity(K[:, hp], Kq[:, hp]), sim, atol=1e-12)
+
+
 def test_block_bytes():
     assert layout.block_bytes(layout.INT2, 128) == 4096
     assert layout.block_bytes(layout.INT4, 128) == 6144
