@@ -338,7 +338,8 @@ class DecodeRunner:
         caps = [int((bits[0] == k).sum()) for k in (16, 4, 2)]
         self.tc = B.TorchCache(Bn, Hkv, d, B.KV_MIXED, caps, raw_dtype=B.KV_F16, device=dev)
         bits_dev = torch.from_numpy(bits).to(dev)
-        B.kv_quantize_append(to(inputs["K_cache"]), to(inputs["V_cache"]), self.dt, n, self.tc.c,
+        self.K_cache = to(inputs["K_cache"])
+        B.kv_quantize_append(self.K_cache, to(inputs["V_cache"]), self.dt, n, self.tc.c,
                              B.kv_append_opts(bits.ctypes.data, bits_dev.data_ptr()))
         torch.cuda.synchronize(dev)
         # algorithmic cache bytes: codes of valid tokens + all metadata; 16-bit windows' valid rows
@@ -365,6 +366,27 @@ class DecodeRunner:
 
     def append(self, stream):
         pass
+
+    def time_window_similarity(self, flush, steps, stream):
+        """The window-similarity kernel over this workload's cache keys, the current token
+        standing in for the question: mean seconds per call (L2 flushed before each) and
+        the keys' bytes it reads."""
+        import torch
+        s = self.spec
+        Bn, Hkv, n, d = s["B"], s["Hkv"], s["n_cache"], s["d"]
+        sim = torch.empty((Bn, (n + 31) // 32), dtype=torch.float32, device=self.dev)
+        run = lambda: self.B.kv_window_similarity(self.K_cache, self.Kc, self.dt, Bn, Hkv, n, 1, d, sim, stream)
+        for _ in range(3):
+            run()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(torch.cuda.current_stream(self.dev))
+            run()
+            ev[k][1].record(torch.cuda.current_stream(self.dev))
+        torch.cuda.synchronize(self.dev)
+        t = sum(a.elapsed_time(b) for a, b in ev) / steps * 1e-3
+        return t, float(self.K_cache.numel() * self.K_cache.element_size())
 
 
 def with_jensen(spec, jensen):
@@ -487,6 +509,11 @@ def run_own(args, rank, world, dist):
         line.pop("append_ms", None)
     if getattr(r, "calib_ms", None) is not None:
         line["calibration_ms"] = r.calib_ms   # once per prefill, outside the step
+    if spec["kind"] == "decode":
+        # the similarity that feeds the window plan, once per prefill and outside the step
+        t_ws, b_ws = r.time_window_similarity(flush, args.steps, sh)
+        line["window_similarity"] = {"us": t_ws * 1e6, "bytes": b_ws, "gbs": b_ws / t_ws / 1e9,
+                                     "frac_hbm": b_ws / t_ws / 1e9 / peaks["hbm_gbs"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, inputs)
     print(json.dumps(line), flush=True)

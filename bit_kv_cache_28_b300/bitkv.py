@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3:
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_append", "kv_attention_workspace",
-           "kv_attention_plan", "kv_attention", "kv_attention_noalloc", "kv_window_plan", "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
+           "kv_attention_plan", "kv_attention", "kv_attention_noalloc", "kv_window_plan", "kv_window_similarity",
+           "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
            "kv_psac_basis", "kv_dequantize", "kv_last_error", "kv_version"]
 
 
@@ -87,6 +88,7 @@ def lib():
             "kv_attention_noalloc": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P,
                                                P, P]),
             "kv_window_plan": (C.c_int, [P, I, C.POINTER(kv_thresholds), P, P]),
+            "kv_window_similarity": (C.c_int, [P, P, I, I, I, I, I, I, P, P]),
             "kv_codebook_workspace": (S, [C.POINTER(kv_layout), I]),
             "kv_codebook_fit": (C.c_int, [P, I, I, C.POINTER(kv_cache), I, P, I, P, P, S, P]),
             "kv_psac_workspace": (S, [C.POINTER(kv_layout)]),
@@ -186,6 +188,11 @@ def kv_window_plan(sim, n_windows, thresholds: kv_thresholds | None, bits_out, p
     """Host-only: sim, bits_out (int8) and perm_out (int32) are numpy arrays."""
     _check(lib().kv_window_plan(_ptr(sim), n_windows, C.byref(thresholds) if thresholds is not None else None,
                                 _ptr(bits_out), _ptr(perm_out)))
+
+
+def kv_window_similarity(K, Kq, dtype, B, Hkv, n, m, d, sim, stream=None):
+    """Device: K [B][Hkv][n][d], Kq [B][Hkv][m][d] in dtype; sim fp32 [B][ceil(n / 32)]."""
+    _check(lib().kv_window_similarity(_ptr(K), _ptr(Kq), dtype, B, Hkv, n, m, d, _ptr(sim), _stream(stream)))
 
 
 def kv_codebook_workspace(layout, n_tokens) -> int:

@@ -226,6 +226,19 @@ kv_status kv_attention_noalloc(const void* Q, const void* Kcur, const void* Vcur
 kv_status kv_window_plan(const float* sim, int n_windows, const kv_thresholds* th, int8_t* bits_out,
                          int32_t* perm_out);
 
+/* The similarity kv_window_plan ranks by ([WQ] 何が新しいのか: each window's
+ * cosine similarity to the text question): for every 32-token window w of K,
+ * cos(u_w, v) with u_w the mean of the window's valid tokens' keys and v the
+ * mean of the question tokens' keys, all Hkv heads' d channels concatenated;
+ * 0 where either is the zero vector (or m == 0).  fp32 sums on the device.
+ *   K (device) [B][Hkv][n][d], Kq (device) [B][Hkv][m][d], both in dtype and
+ *   16-byte aligned, d * sizeof(dtype) a multiple of 16 and Hkv * d at most
+ *   1024 16-byte groups and B at most 65535 (KV_ERR_UNSUPPORTED otherwise);
+ *   sim (device, fp32) [B][ceil(n / 32)], written by the call (copy it to the
+ *   host for kv_window_plan).  n == 0 does nothing.  Async on `stream`. */
+kv_status kv_window_similarity(const void* K, const void* Kq, kv_dtype dtype, int B, int Hkv, int n, int m, int d,
+                               float* sim, void* stream);
+
 /* Fit CODEBOOK2 key centroids ([QWM] QSAC): per (b, kv head, channel) 1-D
  * Lloyd k-means, 4 centroids, quantile init x_(floor((2k+1)n/8)) of the sorted
  * values, `iters` iterations, nearest by fp64 |x - mu| (ties to the lower index),

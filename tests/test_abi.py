@@ -109,3 +109,19 @@ def test_argument_errors_never_launch():
         B.kv_attention(0x40000, 0x50000, 0x60000, B.KV_F16, 4, 4, 2, c, opts, 0x70000, None, None, 0, 0)
     assert e.value.status == B.KV_ERR_WORKSPACE
     assert "workspace" in B.kv_last_error()
+
+
+def test_window_similarity_argument_errors():
+    """Rejected on the host before any launch (fake, never dereferenced addresses)."""
+    sim = 0x30000
+    cases = [((0x10000, 0x20000, B.KV_F16, 0, 4, 64, 8, 64, sim), B.KV_ERR_INVALID_ARG),   # B = 0
+             ((0x10000, 0x20000, B.KV_F16, 1, 4, -1, 8, 64, sim), B.KV_ERR_INVALID_ARG),  # n < 0
+             ((0x10000, None, B.KV_F16, 1, 4, 64, 8, 64, sim), B.KV_ERR_INVALID_ARG),     # Kq NULL, m > 0
+             ((0x10000, 0x20000, B.KV_F16, 1, 4, 64, 8, 60, sim), B.KV_ERR_UNSUPPORTED),  # rows of 120 bytes
+             ((0x10000, 0x20000, B.KV_F16, 1, 32, 64, 8, 512, sim), B.KV_ERR_UNSUPPORTED),  # 2048 groups
+             ((0x10008, 0x20000, B.KV_F16, 1, 4, 64, 8, 64, sim), B.KV_ERR_ALIGNMENT)]
+    for args, status in cases:
+        with pytest.raises(B.BitKVError) as e:
+            B.kv_window_similarity(*args, 0)
+        assert e.value.status == status
+    B.kv_window_similarity(0x10000, 0x20000, B.KV_F16, 1, 4, 0, 8, 64, sim, 0)   # n == 0: nothing to do
