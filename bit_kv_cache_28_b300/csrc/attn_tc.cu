@@ -135,7 +135,7 @@ enum {
     BAR_STG_FULL = 10,   // [2] staging slot filled by the bulk copy
     BAR_STG_EMPTY = 12,  // [2] all producers finished reading the staging slot
     BAR_V_FULL = 14,   // [2] producers -> MMA: V_hat[s] ready
-    BAR_MMA_DONE = 16, // every MMA the issuer started has completed (before TMEM is freed)
+    BAR_MMA_DONE = 16, // every MMA the issuer started has completed (O final; TMEM may be freed)
     BAR_NEVER = 17,    // never arrived on: the target of the injected stall (failure tests)
 };
 
@@ -908,8 +908,12 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         // ---- epilogue
         const int qi = q0 + i;
         const long long orow = ((long long)b * Hq + hq) * n_q + qi;
+        // O is final once every MMA of the CTA has completed (MMA_DONE, committed once
+        // after the last P V).  A parity wait on O_DONE for the last tile would be
+        // ambiguous here: the tile before it may not have completed either, and a
+        // barrier two phases behind shows the awaited parity as done.
         bool have = T > 0 && !abort_flag;
-        if (have) have = mbar_wait(bar(BAR_O_DONE), (T - 1) & 1, &abort_flag, err, 7);
+        if (have) have = mbar_wait(bar(BAR_MMA_DONE), 0, &abort_flag, err, 7);
         have = __all_sync(0xffffffffu, have);
         fence_after();
         const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
