@@ -5,6 +5,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <numeric>
 #include <string>
 #include <vector>
@@ -60,6 +62,22 @@ kv_status check_launch(const char* what) {
         const cudaError_t e2 = cudaDeviceSynchronize();
         if (e2 != cudaSuccess) return set_error(KV_ERR_CUDA, "%s (sync): %s", what, cudaGetErrorString(e2));
     }
+    return KV_OK;
+}
+
+kv_status set_smem_limit(const void* kernel, size_t bytes, const char* name) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> limits;   // (kernel, device) -> bytes set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(KV_ERR_CUDA, "%s: cudaGetDevice: %s", name, cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = limits[{kernel, dev}];
+    if (bytes <= have) return KV_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess)
+        return set_error(KV_ERR_CUDA, "%s: %zu bytes of shared memory: %s", name, bytes, cudaGetErrorString(e));
+    have = bytes;
     return KV_OK;
 }
 

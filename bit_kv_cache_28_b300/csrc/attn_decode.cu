@@ -859,15 +859,9 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     const DevCache c = make_dev_cache(cache);
     const DecShape sh = dec_shape(cache, Hq);
     const size_t smem = dec_smem_bytes(sh, D);
-    static size_t attr_bytes = 0;
-    if (smem > attr_bytes) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(attn_decode_kernel<T, D, NT, JENSEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return set_error(KV_ERR_CUDA, "attn_decode_kernel: %zu bytes of shared memory: %s", smem,
-                             cudaGetErrorString(e));
-        attr_bytes = smem;
-    }
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(attn_decode_kernel<T, D, NT, JENSEN>), smem,
+                                        "attn_decode_kernel");
+    if (sa != KV_OK) return sa;
     unsigned char* w = static_cast<unsigned char*>(ws);
     int* err = reinterpret_cast<int*>(w);
     int* tickets = reinterpret_cast<int*>(w + 256);

@@ -304,11 +304,8 @@ static void launch_simt_td(const void* Q, const void* Kc, const void* Vc, int n_
                            float tau, int jensen, int psac, int n_splits, int uc, int ut, void* out, int out_f32,
                            float* lse, float* ws_o, float2* ws_ml, cudaStream_t st) {
     const size_t sm = simt_smem_bytes(D, c.r);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
+    // a refusal leaves the limit unset; the launch then fails and the caller reports it
+    (void)set_smem_limit(reinterpret_cast<const void*>(attn_simt_kernel<T, D>), 200 * 1024, "attn_simt_kernel");
     const int n_qt = (n_q + kSQ - 1) / kSQ;
     dim3 grid(n_qt * n_splits, Hq, c.B);
     attn_simt_kernel<T, D><<<grid, kSimtThreads, sm, st>>>(

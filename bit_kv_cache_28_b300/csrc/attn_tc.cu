@@ -988,15 +988,9 @@ kv_status launch_tc_t(const DevCache& c, const void* Q, const void* Kc, const vo
                       float tau, int r16, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
                       int* err, cudaStream_t st) {
     constexpr int kSmem = Smem<FMT>::total;
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<FMT, JENSEN>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess)
-            return set_error(KV_ERR_CUDA, "attn_tc_kernel: %d bytes of shared memory: %s", kSmem,
-                             cudaGetErrorString(e));
-        attr = true;
-    }
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<FMT, JENSEN>), kSmem,
+                                        "attn_tc_kernel");
+    if (sa != KV_OK) return sa;
     const int n_qt = (n_q + kM - 1) / kM;
     dim3 grid(n_qt * n_splits, Hq, c.B);
     attn_tc_kernel<FMT, JENSEN><<<grid, kThreads, kSmem, st>>>(

@@ -189,5 +189,9 @@ __device__ __forceinline__ float log_sinhc(float x) {
 DevCache make_dev_cache(const kv_cache* c);
 kv_status set_error(kv_status st, const char* fmt, ...);
 kv_status check_launch(const char* what);
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at least
+// `bytes`, once per (kernel, device), never lowering it; thread-safe.  KV_ERR_CUDA
+// (with the message set) when the runtime refuses.
+kv_status set_smem_limit(const void* kernel, size_t bytes, const char* name);
 
 }  // namespace bitkv

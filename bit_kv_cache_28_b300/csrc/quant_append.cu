@@ -514,11 +514,8 @@ static kv_status launch_append_t(const void* K, const void* V, int n_tokens, con
                                  int uni_seg, const int8_t* win_bits, int n_win, int grid_x, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     const size_t sm = append_smem_bytes(c.d, c.kind == KV_CODEBOOK2 ? c.rp : 0);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(append_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024);
-        attr_set = true;
-    }
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(append_kernel<T>), 120 * 1024, "append_kernel");
+    if (sa != KV_OK) return sa;
     dim3 grid(grid_x, c.Hkv, c.B);
     append_kernel<T><<<grid, kAppendThreads, sm, st>>>(static_cast<const T*>(K), static_cast<const T*>(V), n_tokens,
                                                        c, mode, uni_seg, win_bits, n_win, cache->n_tokens);
