@@ -417,6 +417,20 @@ def with_jensen(spec, jensen):
     return spec
 
 
+def max_over_ranks(times, dist, device):
+    """Each timing (seconds) as the slowest rank measured it: the job's step ends when its
+    last replica does."""
+    import torch
+    tt = torch.tensor(times, dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tt.tolist()
+
+
+def job_value(units_per_rank, world, seconds):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def run_own(args, rank, world, dist):
     import torch
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -481,9 +495,7 @@ def run_own(args, rank, world, dist):
     t_e2e = sum(a.elapsed_time(b) for a, b in e_ev) / args.steps * 1e-3
 
     if dist:
-        tt = torch.tensor([t_step, t_attn, t_app, t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step, t_attn, t_app, t_e2e = tt.tolist()
+        t_step, t_attn, t_app, t_e2e = max_over_ranks([t_step, t_attn, t_app, t_e2e], dist, dev)
 
     if rank != 0:
         return
@@ -506,7 +518,7 @@ def run_own(args, rank, world, dist):
                  "roofline_time_frac_of_step": max(r.cache_bytes / (peaks["hbm_gbs"] * 1e9),
                                                    spec["attn_flops"] / (peaks["bf16_tflops"] * 1e12)) / t_step})
     line = {
-        "metric": METRIC, "value": world * rows / t_step, "unit": "query-tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_value(rows, world, t_step), "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic (seeded, PCG64)",
         "config": {"workload": spec["label"], "query_tokens": "B*Hq*n_q per step (one row per query head)",
@@ -515,7 +527,7 @@ def run_own(args, rank, world, dist):
         "cache_gbs": world * cache_gbs,
         "attn_ms": t_attn * 1e3, "append_ms": t_app * 1e3,
         "roofline": roof,
-        "e2e": {"value": world * rows / t_e2e, "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(rows, world, t_e2e), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": r.launches_per_step * args.steps,
         "clocks": sampler.summary(),
