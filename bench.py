@@ -510,6 +510,9 @@ def run_own(args, rank, world, dist):
         achieved = spec["attn_flops"] / t_attn / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"]}
+        if peaks.get("bf16_tflops_sustained"):
+            # the kernel is timed alone (burst peak above); the power-capped figure for context
+            roof["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
     roof.update({"traffic": traffic_for(kernel, spec["name"]), "kernel": kernel, "splits": r.splits,
                  "peak_source": peaks["source"],
                  "algorithmic": ("cache bytes (codes of valid tokens + all metadata) per launch"
