@@ -218,6 +218,7 @@ kv_status kv_cache_init(kv_cache* c, const kv_layout* L, void* data, int32_t* bl
 
 kv_status kv_quantize_append(const void* K, const void* V, kv_dtype dtype, int n_tokens, kv_cache* cache,
                              const kv_append_opts* opts, void* stream) {
+    AbiRange nvtx_range("kv_quantize_append");
     kv_status s = check_cache(cache);
     if (s != KV_OK) return s;
     const kv_layout& L = cache->layout;
@@ -321,6 +322,7 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
 kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q, int n_cur, int Hq,
                        const kv_cache* cache, const kv_attn_opts* opts, void* out, float* lse, void* workspace,
                        size_t ws_bytes, void* stream) {
+    AbiRange nvtx_range("kv_attention");
     kv_status s = check_cache(cache);
     if (s != KV_OK) return s;
     const kv_layout& L = cache->layout;
@@ -407,6 +409,7 @@ size_t kv_codebook_workspace(const kv_layout* L, int n_tokens) { return L ? code
 
 kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, int iters, const void* Qhist,
                           int n_hist, float* weights_out, void* workspace, size_t ws_bytes, void* stream) {
+    AbiRange nvtx_range("kv_codebook_fit");
     kv_status s = check_cache(cache);
     if (s != KV_OK) return s;
     if (cache->layout.kind != KV_CODEBOOK2) return set_error(KV_ERR_INVALID_ARG, "cache is not CODEBOOK2");
@@ -424,6 +427,7 @@ size_t kv_psac_workspace(const kv_layout* L) { return L ? psac_ws_bytes(L) : 0; 
 
 kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache* cache, float* eigvals_out,
                         void* workspace, size_t ws_bytes, void* stream) {
+    AbiRange nvtx_range("kv_psac_basis");
     kv_status s = check_cache(cache);
     if (s != KV_OK) return s;
     if (cache->layout.kind != KV_CODEBOOK2 || cache->layout.psac_rank <= 0 || !cache->psac_u)
@@ -436,6 +440,7 @@ kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache*
 }
 
 kv_status kv_dequantize(const kv_cache* cache, float* K_out, float* V_out, void* stream) {
+    AbiRange nvtx_range("kv_dequantize");
     kv_status s = check_cache(cache);
     if (s != KV_OK) return s;
     if (!K_out || !V_out) return set_error(KV_ERR_INVALID_ARG, "K_out or V_out is NULL");

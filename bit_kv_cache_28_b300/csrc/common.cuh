@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/bitkv.h"
 
 namespace bitkv {
@@ -189,6 +191,16 @@ __device__ __forceinline__ float log_sinhc(float x) {
 DevCache make_dev_cache(const kv_cache* c);
 kv_status set_error(kv_status st, const char* fmt, ...);
 kv_status check_launch(const char* what);
+// An NVTX range named for a C-ABI call, open for the call's duration: a profiler
+// (nsys, ncu's range filters) then shows each call with the kernels it launched.
+// Without an attached tool the push and pop do nothing.
+struct AbiRange {
+    explicit AbiRange(const char* name) { nvtxRangePushA(name); }
+    ~AbiRange() { nvtxRangePop(); }
+    AbiRange(const AbiRange&) = delete;
+    AbiRange& operator=(const AbiRange&) = delete;
+};
+
 // Raises `kernel`'s dynamic shared-memory limit on the current device to at least
 // `bytes`, once per (kernel, device), never lowering it; thread-safe.  KV_ERR_CUDA
 // (with the message set) when the runtime refuses.

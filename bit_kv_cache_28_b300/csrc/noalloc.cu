@@ -51,6 +51,7 @@ using namespace bitkv;
 extern "C" kv_status kv_attention_noalloc(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q,
                                           int n_cur, int Hq, const kv_cache* cache, const kv_attn_opts* opts,
                                           void* out, float* lse, void* stream) {
+    AbiRange nvtx_range("kv_attention_noalloc");
     if (!cache) return set_error(KV_ERR_INVALID_ARG, "cache is NULL");
     if (n_q <= 0 || n_cur < 0 || Hq <= 0) return set_error(KV_ERR_INVALID_ARG, "bad sizes n_q=%d n_cur=%d Hq=%d", n_q, n_cur, Hq);
     kv_attn_opts o = opts ? *opts : kv_attn_opts{0.0f, KV_JENSEN_OFF, 0, 0, 0, KV_PATH_AUTO};

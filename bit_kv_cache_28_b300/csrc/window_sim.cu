@@ -238,6 +238,7 @@ using namespace bitkv;
 
 extern "C" kv_status kv_window_similarity(const void* K, const void* Kq, kv_dtype dtype, int B, int Hkv, int n, int m,
                                           int d, float* sim, void* stream) {
+    AbiRange nvtx_range("kv_window_similarity");
     if (B <= 0 || Hkv <= 0 || d <= 0 || n < 0 || m < 0)
         return set_error(KV_ERR_INVALID_ARG, "kv_window_similarity: bad sizes B=%d Hkv=%d n=%d m=%d d=%d", B, Hkv, n,
                          m, d);
