@@ -123,34 +123,28 @@ def lse_merge(ms, ls, os_):
     return o, m + np.log(l)
 
 
-def value_dtype(io_dtype):
-    """Precision of the dequantised cache values entering P V.
-
-    Keys are consumed at the I/O dtype (the Q K^T operands).  The P V product of
-    16-bit inputs runs in fp16: attention weights carry 11 significant bits
-    there, where bf16 would leave 8 and an output error of up to 2^-9 |v|.  So
-    for 16-bit I/O the dequantised values are rounded to fp16, and for fp32
-    I/O they stay fp32.
-    """
-    return "f32" if io_dtype == "f32" else "f16"
-
-
 def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN_OFF,
-                         psac_U=None, rows=None, operands="io"):
-    """Reference attention for every (b, q-head).
+                         psac_U=None, rows=None, operand_dtype=None):
+    """Reference attention for every (b, q-head): the plain definition.
+
+    The precision model (one, for every path): the queries and the current chunk
+    are the exact values given (16-bit inputs are exact in fp32), the cached keys
+    and values are the dequantised entries x_hat = fmaf(code, s, z) exactly as
+    the fp32 values they are, and every product, sum and the softmax run in fp64.
+    Nothing is rounded on the way; the output is returned in fp64.
 
     cache : oracle.layout.Cache (or codebook cache) holding the dequantised view.
     Q     : fp32 [B, Hq, nq, d]; Kcur, Vcur: fp32 [B, Hkv, nn, d] (may have nn = 0).
-    io_dtype: 'f32' | 'f16' | 'bf16' -- dequantised cache keys are rounded to it, cache
-              values to value_dtype(io_dtype).
+    io_dtype: 'f32' | 'f16' | 'bf16' -- the inputs' dtype (informational: the
+              inputs already hold values exact in it).
     psac_U: optional fp32 [B, Hkv, d, r]; adds tau (U^T q) . coeff for cached keys.
     rows  : optional index array of query rows to evaluate (all if None).
-    operands: 'io' -- dequantised cache keys rounded to io_dtype and values to
-              value_dtype(io_dtype) before the products (what a kernel that
-              builds 16-bit operand tiles consumes); 'f32' -- the dequantised
-              fp32 entries themselves (what a kernel consumes that folds the
-              step sizes and zero points into the query and the attention
-              weights instead of forming k_hat, v_hat).
+    operand_dtype: None for the definition above.  'f16' | 'bf16' | 'f32'
+              evaluates the same definition after storing every operand of the two
+              products -- Q, the dequantised cached keys and values and the
+              current chunk -- in that dtype (round to nearest even), for paths
+              documented to hold their operands in 16 bits.  It is a diagnostic
+              with a tighter tolerance, never a replacement for the definition.
     GQA: q-head h reads kv-head h // (Hq // Hkv).
     Returns (o [B, Hq, nrows, d], lse [B, Hq, nrows]) in fp64.
     """
@@ -163,30 +157,30 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
         tau = 1.0 / np.sqrt(d)
     if rows is None:
         rows = np.arange(nq)
+    store = (lambda x: np.asarray(x, np.float32)) if operand_dtype is None else \
+        (lambda x: round_to(x, operand_dtype))
     o = np.zeros((B, Hq, len(rows), d), F64)
     lse = np.zeros((B, Hq, len(rows)), F64)
     for b in range(B):
         for hk in range(Hkv):
             lg = cache.logical(b, hk)
-            if operands == "f32":
-                Kc = np.asarray(lg["khat"], np.float32)
-                Vc = np.asarray(lg["vhat"], np.float32)
-            else:
-                Kc = round_to(lg["khat"], io_dtype)
-                Vc = round_to(lg["vhat"], value_dtype(io_dtype))
+            Kc = store(lg["khat"])
+            Vc = store(lg["vhat"])
+            kn = store(Kcur[b, hk]) if Kcur is not None else np.zeros((0, d), np.float32)
+            vn = store(Vcur[b, hk]) if Vcur is not None else np.zeros((0, d), np.float32)
             for hq in range(hk * grp, (hk + 1) * grp):
-                q = Q[b, hq, rows].astype(F64)
+                # the Jensen term and the PSAC product use the query as given
+                q_in = Q[b, hq, rows].astype(F64)
+                q = store(Q[b, hq, rows]).astype(F64)
                 delta = None
                 if jensen != JENSEN_OFF and Kc.shape[0] > 0:
-                    dg = jensen_delta(q, lg["ks"], tau, jensen)
+                    dg = jensen_delta(q_in, lg["ks"], tau, jensen)
                     dg = dg * lg["quantised"][None, :]
                     delta = dg[:, lg["kgroup"]]
                 extra = None
                 if psac_U is not None and lg["coeff"] is not None and Kc.shape[0] > 0:
                     U = np.asarray(psac_U[b, hk], F64)
-                    uq = q @ U                                   # [nrows, r]
+                    uq = q_in @ U                                # [nrows, r]
                     extra = tau * (uq @ np.asarray(lg["coeff"], F64).T)
-                kn = np.asarray(Kcur[b, hk], F64) if Kcur is not None else np.zeros((0, d))
-                vn = np.asarray(Vcur[b, hk], F64) if Vcur is not None else np.zeros((0, d))
                 o[b, hq], lse[b, hq] = attention_rows(q, Kc, Vc, kn, vn, tau, delta, extra)
     return o, lse

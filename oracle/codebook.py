@@ -133,7 +133,7 @@ def build_codebook(K, V, cent, U, cap_blocks):
                 enc = encode_cb_blocks(Kb, Vb, cent[b, h], co, nv, r)
                 c._put(b, h, 0, j, enc["bytes"][0])
                 rec = dict(pos=j * BLOCK, len=nv, khat=enc["khat"][0], vhat=enc["vhat"][0],
-                           ks=np.zeros(d, F32), quantised=False)
+                           ks=np.zeros(d, F32), quantised=False, seg=0, slot=j)
                 rec["coeff"] = enc["coeff"][0].astype(F64) if r else np.zeros((BLOCK, 0))
                 c.blocks[b][h].append(rec)
                 if h == 0:

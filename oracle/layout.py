@@ -156,7 +156,7 @@ class Cache:
     blk_len, blk_pos : int32 [B, sum(caps)]
     n_blocks: per-segment used blocks (equal across batch)
     tokens  : per (b, h) a dict of arrays over the valid cached tokens, in
-              logical position order: khat, vhat (fp32 before I/O rounding),
+              logical position order: khat, vhat (the exact dequantised fp32 entries),
               kgroup (block index of the token), quantised (bool: carries a
               key step size), and per block the key step sizes ks [nblk, d].
     """
@@ -233,6 +233,8 @@ def build_uniform(K, V, bits, appends, cap_blocks):
             kh = enc["khat"].reshape(B, H, cnt, BLOCK, d)
             vh = enc["vhat"].reshape(B, H, cnt, BLOCK, d)
             ks = enc["ks"].reshape(B, H, cnt, d)
+            kc = enc["kcode"].reshape(B, H, cnt, BLOCK, d)
+            vcd = enc["vcode"].reshape(B, H, cnt, BLOCK, d)
             for b in range(B):
                 for j in range(cnt):
                     idx = c.n_blocks[0] + j0 + j
@@ -244,7 +246,8 @@ def build_uniform(K, V, bits, appends, cap_blocks):
                         c._put(b, h, 0, idx, raw[b, h, j])
                         c.blocks[b][h].append(dict(pos=c.n_tokens + (j0 + j) * BLOCK, len=nv,
                                                    khat=kh[b, h, j], vhat=vh[b, h, j], ks=ks[b, h, j],
-                                                   quantised=True))
+                                                   quantised=True, seg=0, slot=idx,
+                                                   kcode=kc[b, h, j], vcode=vcd[b, h, j]))
         c.n_blocks[0] += nb
         c.n_tokens += n
         t0 += n
@@ -280,9 +283,11 @@ def build_mixed(K, V, window_bits, caps, dtype):
             if seg == 0:
                 enc = encode_raw_blocks(Kb, Vb, nv, dtype)
                 ks = np.zeros((H, d), F32)
+                kcd = vcd = [None] * H
             else:
                 enc = encode_int_blocks(Kb, Vb, 4 if seg == 1 else 2, nv)
                 ks = enc["ks"]
+                kcd, vcd = enc["kcode"], enc["vcode"]
             idx = cnt[seg]
             cnt[seg] += 1
             assert idx < caps[seg]
@@ -292,7 +297,8 @@ def build_mixed(K, V, window_bits, caps, dtype):
             for h in range(H):
                 c._put(b, h, seg, idx, enc["bytes"][h])
                 c.blocks[b][h].append(dict(pos=t0, len=nv, khat=enc["khat"][h], vhat=enc["vhat"][h],
-                                           ks=ks[h], quantised=seg != 0))
+                                           ks=ks[h], quantised=seg != 0, seg=seg, slot=idx,
+                                           kcode=kcd[h], vcode=vcd[h]))
         if counts is None:
             counts = cnt
         assert counts == cnt, "per-sequence segment counts must agree across the batch"

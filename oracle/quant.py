@@ -100,10 +100,10 @@ def dequantize(codes, s, z):
 
 
 def round_to(x, dtype: str):
-    """Round fp32/fp64 values to the I/O dtype with RNE and return them as fp64.
+    """Round fp32/fp64 values to `dtype` with RNE and return them as fp64.
 
-    dtype: 'f32', 'f16' or 'bf16'.  The attention consumes dequantised cache
-    entries at the I/O dtype, the precision of the tensor-core operands.
+    dtype: 'f32', 'f16' or 'bf16' (torch's CPU conversions, which round to
+    nearest even).
     """
     import torch
     t = torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=F32)))

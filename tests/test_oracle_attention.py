@@ -239,18 +239,43 @@ def test_jensen_applies_only_to_quantised_keys():
     assert np.abs(a0 - a1).max() == 0
 
 
-def test_operand_precision_option():
-    """operands='f32' feeds the dequantised fp32 entries; 'io' rounds them first.  For fp32 I/O
-    the two coincide; for bf16 I/O they differ by less than the bf16 rounding of the keys allows."""
+def test_one_precision_model_and_operand_storage():
+    """The oracle has one precision model: the exact dequantised entries, fp64 arithmetic, the
+    same whatever the inputs' dtype.  Hand case: 32 cached tokens whose key channel 0 and value
+    channel 0 are the constant 1 + 2^-10 (a constant group quantises to itself: s = 0, z = x),
+    everything else 0, one query e_0, no current chunk.  All logits are tau x, so
+    lse = tau x + ln 32 and o_0 = x.  x is exact in fp32 and fp16 (10 fraction bits) but rounds
+    to 1 in bf16 (7 fraction bits): the definition and fp16 operand storage keep it, bf16
+    storage gives lse = tau + ln 32 and o_0 = 1."""
+    x = 1.0 + 2.0 ** -10
+    d = 32
+    K = np.zeros((1, 1, 32, d), np.float32)
+    V = np.zeros((1, 1, 32, d), np.float32)
+    K[..., 0] = x
+    V[..., 0] = x
+    Q = np.zeros((1, 1, 1, d), np.float32)
+    Q[..., 0] = 1.0
+    none = np.zeros((1, 1, 0, d), np.float32)
+    cache = layout.build_uniform(K, V, 2, [32], 1)
+    tau = 1.0 / np.sqrt(d)
+    for io in ("f32", "f16", "bf16"):
+        o, l = A.attention_over_cache(cache, Q, none, none, io)
+        assert o[0, 0, 0, 0] == x and l[0, 0, 0] == tau * x + np.log(32.0)
+    o, l = A.attention_over_cache(cache, Q, none, none, "bf16", operand_dtype="f16")
+    assert o[0, 0, 0, 0] == x and l[0, 0, 0] == tau * x + np.log(32.0)
+    o, l = A.attention_over_cache(cache, Q, none, none, "bf16", operand_dtype="bf16")
+    assert o[0, 0, 0, 0] == 1.0 and l[0, 0, 0] == tau + np.log(32.0)
+
+
+def test_operand_storage_stays_within_its_rounding_bound():
+    """Storing the operands in bf16 moves each cached logit by at most tau sum_c |q_c| |k_c| 2^-8
+    (the relative rounding of a key entry), so the lse moves by at most the largest such bound."""
     c = synth.chunk_case(9, Hkv=1, d=64, chunks=[64], n_cur=8, n_q=4, dtype="bf16")
     cache = layout.build_uniform(c["K_cache"], c["V_cache"], 2, [64], 2)
-    a = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "f32")
-    b = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "f32", operands="f32")
-    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
-    io = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16")
-    ex = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16", operands="f32")
-    assert not np.array_equal(io[0], ex[0])
+    ex = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16")
+    rb = A.attention_over_cache(cache, c["Q"], c["K_cur"], c["V_cur"], "bf16", operand_dtype="bf16")
+    assert not np.array_equal(rb[0], ex[0])
     kh = cache.logical(0, 0)["khat"]
     tau = 1 / 8
     bound = tau * np.abs(c["Q"][0, 0]).astype(np.float64) @ np.abs(kh).T.astype(np.float64) * 2.0 ** -8
-    assert np.abs(io[1] - ex[1]).max() <= bound.max()
+    assert np.abs(rb[1] - ex[1]).max() <= bound.max()

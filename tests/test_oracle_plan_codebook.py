@@ -273,8 +273,8 @@ def test_psac_rank_zero_is_plain_codebook():
     cache0 = codebook.build_codebook(c["K_cache"], c["V_cache"], cent, None, 4)
     o0, _ = A.attention_over_cache(cache0, c["Q"], c["K_cur"], c["V_cur"], "bf16")
     lg = cache0.logical(0, 0)
-    Kc = quant.round_to(lg["khat"], "bf16")
-    Vc = quant.round_to(lg["vhat"], A.value_dtype("bf16"))
+    Kc = np.asarray(lg["khat"], np.float64)
+    Vc = np.asarray(lg["vhat"], np.float64)
     o_ref, _ = A.attention_rows(c["Q"][0, 0], Kc, Vc, c["K_cur"][0, 0], c["V_cur"][0, 0], 1 / np.sqrt(32))
     assert np.abs(o0[0, 0] - o_ref).max() == 0
     U, _ = psac.psac_basis(c["Q_hist"][0], 4)
