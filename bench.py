@@ -3,12 +3,12 @@
 Workloads (seeded synthetic inputs; no dataset exists for this path, shapes
 follow the chunk-wise video-diffusion and video-VLM settings of the pages):
 
-* ``chunk`` (default): 24 heads, d 128, bf16; the 1560 queries of the current
-  chunk attend to a cache of 3 INT2 chunks (4680 tokens) plus the chunk itself
-  with the Jensen correction on, then the finished chunk is quantised and
-  appended.  One step = attention + append; the cache is rewound on the host
-  after each step so every step sees the same cache.
-* ``rollout``: the same with 40 heads and 21 cached chunks (32760 tokens).
+* ``rollout`` (default; the largest single-GPU workload): 40 heads, d 128, bf16;
+  the 1560 queries of the current chunk attend to a cache of 21 INT2 chunks
+  (32760 tokens) plus the chunk itself with the Jensen correction on, then the
+  finished chunk is quantised and appended.  One step = attention + append; the
+  cache is rewound on the host after each step so every step sees the same cache.
+* ``chunk``: the same with 24 heads and 3 cached chunks (4680 tokens).
 * ``decode``: batch 8, 28 query heads over 4 kv heads, d 64, fp16; one query per
   sequence attends to 19600 cached tokens in 613 windows of FP16 / INT4 / INT2
   (planned by kv_window_plan from a seeded similarity) plus its own token.
@@ -23,7 +23,7 @@ follow the chunk-wise video-diffusion and video-VLM settings of the pages):
   over a video-diffusion cache.  One step = one split-K decode attention.
 * ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chunk|rollout|decode|codebook|rollout_decode|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rollout|chunk|decode|codebook|rollout_decode|tiny]
                     [--jensen 0|1|2|3]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
@@ -592,14 +592,14 @@ def oracle_sample_step(spec, inputs, heads):
         oc = OL.build_mixed(inputs["K_cache"][b, sl], inputs["V_cache"][b, sl], bits[None], caps, "f16")
         g = spec["Hq"] // spec["Hkv"]
         OA.attention_over_cache(oc, inputs["Q"][b, :heads * g], inputs["K_cur"][b, sl], inputs["V_cur"][b, sl],
-                                "f16", operands="f32")
+                                "f16")
         return heads * g
     sl = slice(0, heads)
     if spec["kind"] == "chunkdecode":
         oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
                               sum((n + 31) // 32 for n in spec["chunks"]))
         OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
-                                spec["dtype"], jensen=spec["jensen"], operands="f32")
+                                spec["dtype"], jensen=spec["jensen"])
         return spec["B"] * heads
     if spec["name"] == "codebook":
         from oracle import codebook as OC, psac as OP
@@ -689,7 +689,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
-    ap.add_argument("--workload", default="chunk")
+    ap.add_argument("--workload", default="rollout")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--jensen", type=int, default=None, choices=[0, 1, 2, 3],
                     help="override the workload's Jensen mode (0 off, 1 TAYLOR2, 2 EXACT, 3 ISOTROPIC)")

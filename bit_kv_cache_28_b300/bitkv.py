@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libbitkv.so")
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CAPACITY = 0, 1, 2, 3
-KV_ERR_WORKSPACE, KV_ERR_ALIGNMENT, KV_ERR_CUDA, KV_ERR_TIMEOUT = 4, 5, 6, 7
+KV_ERR_WORKSPACE, KV_ERR_ALIGNMENT, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_ERR_RANGE = 4, 5, 6, 7, 8
 KV_F32, KV_F16, KV_BF16 = 0, 1, 2
 KV_UNIFORM2, KV_UNIFORM4, KV_MIXED, KV_CODEBOOK2 = 0, 1, 2, 3
 KV_SEG_RAW16, KV_SEG_INT4, KV_SEG_INT2 = 0, 1, 2
@@ -25,13 +25,15 @@ KV_JENSEN_OFF, KV_JENSEN_TAYLOR2, KV_JENSEN_EXACT, KV_JENSEN_ISOTROPIC = 0, 1, 2
 KV_PATH_AUTO, KV_PATH_SIMT, KV_PATH_TC, KV_PATH_DECODE = 0, 1, 2, 3
 
 STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3: "KV_ERR_CAPACITY",
-                4: "KV_ERR_WORKSPACE", 5: "KV_ERR_ALIGNMENT", 6: "KV_ERR_CUDA", 7: "KV_ERR_TIMEOUT"}
+                4: "KV_ERR_WORKSPACE", 5: "KV_ERR_ALIGNMENT", 6: "KV_ERR_CUDA", 7: "KV_ERR_TIMEOUT",
+                8: "KV_ERR_RANGE"}
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_append", "kv_attention_workspace",
-           "kv_attention_plan", "kv_attention", "kv_attention_noalloc", "kv_window_plan", "kv_window_similarity",
+           "kv_attention_plan", "kv_attention", "kv_attention_status", "kv_attention_noalloc",
+           "kv_attention_noalloc_status", "kv_window_plan", "kv_window_similarity",
            "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
-           "kv_psac_basis", "kv_dequantize", "kv_last_error", "kv_version"]
+           "kv_psac_basis", "kv_dequantize", "kv_debug_operands", "kv_last_error", "kv_version"]
 
 
 class kv_layout(C.Structure):
@@ -85,8 +87,10 @@ def lib():
             "kv_attention_plan": (C.c_int, [C.POINTER(kv_cache), I, I, I, I, C.POINTER(kv_attn_opts),
                                             C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
             "kv_attention": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P, P, P, S, P]),
+            "kv_attention_status": (C.c_int, [P, P]),
             "kv_attention_noalloc": (C.c_int, [P, P, P, I, I, I, I, C.POINTER(kv_cache), C.POINTER(kv_attn_opts), P,
                                                P, P]),
+            "kv_attention_noalloc_status": (C.c_int, [P]),
             "kv_window_plan": (C.c_int, [P, I, C.POINTER(kv_thresholds), P, P]),
             "kv_window_similarity": (C.c_int, [P, P, I, I, I, I, I, I, P, P]),
             "kv_codebook_workspace": (S, [C.POINTER(kv_layout), I]),
@@ -94,6 +98,7 @@ def lib():
             "kv_psac_workspace": (S, [C.POINTER(kv_layout)]),
             "kv_psac_basis": (C.c_int, [P, I, I, C.POINTER(kv_cache), P, P, S, P]),
             "kv_dequantize": (C.c_int, [C.POINTER(kv_cache), P, P, P]),
+            "kv_debug_operands": (C.c_int, [C.POINTER(kv_cache), I, P, P, P]),
             "kv_last_error": (C.c_char_p, []),
             "kv_version": (C.c_char_p, []),
         }
@@ -177,6 +182,16 @@ def kv_attention(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, opts, out, lse=Non
                               ws_bytes, _stream(stream)))
 
 
+def kv_attention_status(workspace, stream=None):
+    """Raises BitKVError if the last kv_attention on `workspace` timed out or hit the fp16 range."""
+    _check(lib().kv_attention_status(_ptr(workspace), _stream(stream)))
+
+
+def kv_attention_noalloc_status(stream=None):
+    """kv_attention_status for the last kv_attention_noalloc call on the current device."""
+    _check(lib().kv_attention_noalloc_status(_stream(stream)))
+
+
 def kv_attention_noalloc(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, opts, out, lse=None, stream=None):
     """kv_attention with its scratch in the library's fixed device array (no workspace argument)."""
     _check(lib().kv_attention_noalloc(_ptr(Q), _ptr(Kcur), _ptr(Vcur), dtype, n_q, n_cur, Hq, C.byref(cache),
@@ -216,6 +231,11 @@ def kv_psac_basis(Qhist, dtype, n_hist, cache, eigvals_out=None, workspace=None,
 
 def kv_dequantize(cache, K_out, V_out, stream=None):
     _check(lib().kv_dequantize(C.byref(cache), _ptr(K_out), _ptr(V_out), _stream(stream)))
+
+
+def kv_debug_operands(cache, path, K_out, V_out, stream=None):
+    """The fp16 cache operands the tensor-core (KV_PATH_TC) or decode (KV_PATH_DECODE) kernel builds."""
+    _check(lib().kv_debug_operands(C.byref(cache), path, _ptr(K_out), _ptr(V_out), _stream(stream)))
 
 
 def kv_last_error() -> str:

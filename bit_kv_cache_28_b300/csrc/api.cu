@@ -19,6 +19,8 @@ namespace bitkv {
 kv_status launch_append(const void* K, const void* V, kv_dtype dt, int n_tokens, const kv_cache* cache, int mode,
                         int uni_seg, const int8_t* win_bits, int n_win, int grid_x, cudaStream_t st);
 kv_status launch_dequant(const kv_cache* cache, float* Kout, float* Vout, cudaStream_t st);
+kv_status launch_tc_operands(const kv_cache* cache, void* Kout, void* Vout, cudaStream_t st);
+kv_status launch_dec_operands(const kv_cache* cache, void* Kout, void* Vout, cudaStream_t st);
 kv_status launch_attn_simt(const void* Q, const void* Kc, const void* Vc, kv_dtype dt, int n_q, int n_cur, int Hq,
                            const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out,
                            int out_f32, float* lse, void* ws, cudaStream_t st);
@@ -62,6 +64,25 @@ kv_status check_launch(const char* what) {
         const cudaError_t e2 = cudaDeviceSynchronize();
         if (e2 != cudaSuccess) return set_error(KV_ERR_CUDA, "%s (sync): %s", what, cudaGetErrorString(e2));
     }
+    return KV_OK;
+}
+
+kv_status clear_device(void* p, size_t bytes, cudaStream_t st, const char* who) {
+    const cudaError_t e = cudaMemsetAsync(p, 0, bytes, st);
+    if (e != cudaSuccess) return set_error(KV_ERR_CUDA, "%s: clearing %zu bytes of workspace: %s", who, bytes,
+                                           cudaGetErrorString(e));
+    return KV_OK;
+}
+
+kv_status read_status(const void* ws, cudaStream_t st) {
+    int h[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return set_error(KV_ERR_CUDA, "reading the attention status: %s", cudaGetErrorString(e));
+    if (h[0] != 0)
+        return set_error(KV_ERR_TIMEOUT, "a bounded device-side wait gave up (wait %d); the output is incomplete", h[0]);
+    if (h[1] != 0)
+        return set_error(KV_ERR_RANGE, "an operand of the tensor-core path lies outside the fp16 range (|x| >= 65520)");
     return KV_OK;
 }
 
@@ -347,29 +368,43 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
     if (path == KV_PATH_DECODE) need = decode_workspace(cache, Hq, sp);
     else if (path == KV_PATH_TC) need = tc_workspace(cache, n_q, Hq, sp);
     else need = simt_workspace(cache, n_q, Hq, sp);
-    if (need > 0 && (!workspace || ws_bytes < need))
+    if (!workspace || ws_bytes < need)
         return set_error(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(workspace)) return set_error(KV_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    kv_status r;
     switch (path) {
         case KV_PATH_SIMT:
-            return launch_attn_simt(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, tau, o->jensen, o->psac, sp, out,
-                                    o->out_f32, lse, workspace, st);
+            r = launch_attn_simt(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, tau, o->jensen, o->psac, sp, out,
+                                 o->out_f32, lse, workspace, st);
+            break;
         case KV_PATH_DECODE:
             if (!decode_supported(cache, dtype, n_q, Hq))
                 return set_error(KV_ERR_UNSUPPORTED, "decode path: needs n_q == 1, f16/bf16, d in {64,128}, "
                                  "UNIFORM/MIXED cache and at most 16 query heads per kv head");
             if (o->psac) return set_error(KV_ERR_UNSUPPORTED, "decode path has no PSAC term");
-            return launch_attn_decode(Q, Kcur, Vcur, dtype, n_cur, Hq, cache, tau, o->jensen, sp, out, o->out_f32,
-                                      lse, workspace, st);
+            r = launch_attn_decode(Q, Kcur, Vcur, dtype, n_cur, Hq, cache, tau, o->jensen, sp, out, o->out_f32, lse,
+                                   workspace, st);
+            break;
         case KV_PATH_TC: {
             const char* why = "";
             if (!tc_supported(cache, dtype, n_q, Hq, &why))
                 return set_error(KV_ERR_UNSUPPORTED, "tensor-core path: %s", why);
-            return launch_attn_tc(Q, Kcur, Vcur, n_q, n_cur, Hq, cache, tau, o->jensen, o->psac, sp, out, o->out_f32,
-                                  lse, workspace, st);
+            r = launch_attn_tc(Q, Kcur, Vcur, n_q, n_cur, Hq, cache, tau, o->jensen, o->psac, sp, out, o->out_f32,
+                               lse, workspace, st);
+            break;
         }
+        default:
+            return set_error(KV_ERR_INVALID_ARG, "unknown path %d", path);
     }
-    return set_error(KV_ERR_INVALID_ARG, "unknown path %d", path);
+    // debugging: wait for the call and report its status words at once
+    if (r == KV_OK && getenv("BITKV_DEBUG_SYNC")) r = read_status(workspace, st);
+    return r;
+}
+
+kv_status kv_attention_status(const void* workspace, void* stream) {
+    if (!workspace) return set_error(KV_ERR_INVALID_ARG, "workspace is NULL");
+    return read_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
 kv_status kv_window_plan(const float* sim, int n_windows, const kv_thresholds* th, int8_t* bits_out,
@@ -437,6 +472,18 @@ kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache*
     if (need && (!workspace || ws_bytes < need))
         return set_error(KV_ERR_WORKSPACE, "PSAC workspace of %zu bytes needed, %zu given", need, ws_bytes);
     return launch_psac_basis(Qhist, dtype, n_hist, cache, eigvals_out, workspace, static_cast<cudaStream_t>(stream));
+}
+
+kv_status kv_debug_operands(const kv_cache* cache, int path, void* K_out, void* V_out, void* stream) {
+    AbiRange nvtx_range("kv_debug_operands");
+    kv_status s = check_cache(cache);
+    if (s != KV_OK) return s;
+    if (!K_out || !V_out) return set_error(KV_ERR_INVALID_ARG, "K_out or V_out is NULL");
+    if (!aligned16(K_out) || !aligned16(V_out)) return set_error(KV_ERR_ALIGNMENT, "K_out and V_out must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (path == KV_PATH_TC) return launch_tc_operands(cache, K_out, V_out, st);
+    if (path == KV_PATH_DECODE) return launch_dec_operands(cache, K_out, V_out, st);
+    return set_error(KV_ERR_INVALID_ARG, "kv_debug_operands: path must be KV_PATH_TC or KV_PATH_DECODE");
 }
 
 kv_status kv_dequantize(const kv_cache* cache, float* K_out, float* V_out, void* stream) {

@@ -819,6 +819,113 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     if (tid == 0) tickets[stream] = 0;
 }
 
+// ------------------------------------------------------- operand dump -----
+// Debug view of this kernel's own operands.  The kernel forms no dequantised key
+// or value: the B/A operands of its quantised-block MMAs are the integer codes,
+// turned into exact fp16 values by code_pair() with the lane constants above, and
+// the steps and zeros enter through the query and probability sides.  This kernel
+// runs that same extraction, per warp one block, on the block's code words in
+// global memory, and writes every fragment's fp16 codes at their (token, channel)
+// place: Kout/Vout fp16 [B][Hkv][32 n_total][d] in stream slot order (all segments'
+// blocks in memory order).  RAW16 slots are not written (they enter as stored).
+template <int D, int BITS>
+__global__ void __launch_bounds__(32)
+dec_operands_kernel(DevCache c, int seg, int slot0, int n_total, __half* __restrict__ Kout,
+                    __half* __restrict__ Vout) {
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x;
+    const LaneConst lc = lane_const(lane);
+    const unsigned char* blk = block_ptr(c, b, h, seg, i);
+    const IntBlockOffsets o = int_offsets(D, BITS);
+    const long long base = (((long long)b * c.Hkv + h) * n_total + slot0 + i) * kBlockTokens;
+    auto put = [&](__half* out, int tok, int ch, uint32_t pair) {
+        *reinterpret_cast<uint32_t*>(out + (base + tok) * D + ch) = pair;
+    };
+    auto put_t = [&](__half* out, int ch, int tok, uint32_t pair) {   // pair = (tok, tok + 1) of channel ch
+        const __half2 v = *reinterpret_cast<const __half2*>(&pair);
+        out[(base + tok) * D + ch] = __low2half(v);
+        out[(base + tok + 1) * D + ch] = __high2half(v);
+    };
+    constexpr int KW = D * BITS / 32;
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
+#pragma unroll 1
+    for (int mt = 0; mt < 2; ++mt) {
+        const int ka = 16 * mt + lc.g, kb = ka + 8;
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int c0 = 16 * kk + 2 * lc.tig;
+            uint32_t a[4];
+            if (BITS == 2) {
+                const uint32_t wa = kc[ka * KW + kk], wb = kc[kb * KW + kk];
+                a[0] = code_pair(wa, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[1] = code_pair(wb, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[2] = code_pair(wa, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[3] = code_pair(wb, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+            } else {
+                a[0] = code_pair(kc[ka * KW + 2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[1] = code_pair(kc[kb * KW + 2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[2] = code_pair(kc[ka * KW + 2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[3] = code_pair(kc[kb * KW + 2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+            }
+            // m16n8k16 A fragment: rows (keys) g, g + 8; columns (channels) 2 tig, 2 tig + 8
+            put(Kout, ka, c0, a[0]);
+            put(Kout, kb, c0, a[1]);
+            put(Kout, ka, c0 + 8, a[2]);
+            put(Kout, kb, c0 + 8, a[3]);
+        }
+    }
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc);
+#pragma unroll 1
+    for (int cm = 0; cm < D / 16; ++cm) {
+        const int ca = 16 * cm + lc.g, cb = ca + 8;
+#pragma unroll 1
+        for (int kk = 0; kk < 2; ++kk) {
+            const int t0 = 16 * kk + 2 * lc.tig;
+            uint32_t a[4];
+            if (BITS == 2) {
+                const uint32_t wa = vc[ca * 2 + kk], wb = vc[cb * 2 + kk];
+                a[0] = code_pair(wa, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[1] = code_pair(wb, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[2] = code_pair(wa, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[3] = code_pair(wb, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+            } else {
+                const uint2 wa = *reinterpret_cast<const uint2*>(vc + ca * 4 + 2 * kk);
+                const uint2 wb = *reinterpret_cast<const uint2*>(vc + cb * 4 + 2 * kk);
+                a[0] = code_pair(wa.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[1] = code_pair(wb.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[2] = code_pair(wa.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[3] = code_pair(wb.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+            }
+            // rows (channels) g, g + 8; columns (tokens) 2 tig, 2 tig + 8
+            put_t(Vout, ca, t0, a[0]);
+            put_t(Vout, cb, t0, a[1]);
+            put_t(Vout, ca, t0 + 8, a[2]);
+            put_t(Vout, cb, t0 + 8, a[3]);
+        }
+    }
+}
+
+template <int D>
+kv_status launch_dec_operands_d(const DevCache& c, void* Kout, void* Vout, cudaStream_t st) {
+    const int n_total = c.n_blocks[0] + c.n_blocks[1] + c.n_blocks[2];
+    int slot0 = 0;
+    for (int seg = 0; seg < KV_NUM_SEG; ++seg) {
+        const int cls = seg_class(c.kind, seg), nb = c.n_blocks[seg];
+        if (nb > 0 && (cls == CLS_INT2 || cls == CLS_INT4)) {
+            const dim3 grid(nb, c.Hkv, c.B);
+            if (cls == CLS_INT2)
+                dec_operands_kernel<D, 2><<<grid, 32, 0, st>>>(c, seg, slot0, n_total, static_cast<__half*>(Kout),
+                                                               static_cast<__half*>(Vout));
+            else
+                dec_operands_kernel<D, 4><<<grid, 32, 0, st>>>(c, seg, slot0, n_total, static_cast<__half*>(Kout),
+                                                               static_cast<__half*>(Vout));
+            const kv_status s = check_launch("dec_operands_kernel");
+            if (s != KV_OK) return s;
+        }
+        slot0 += nb;
+    }
+    return KV_OK;
+}
+
 int g_dec_sms = 0;
 int dec_num_sms() {
     if (g_dec_sms == 0) {
@@ -864,22 +971,16 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     if (sa != KV_OK) return sa;
     unsigned char* w = static_cast<unsigned char*>(ws);
     int* err = reinterpret_cast<int*>(w);
-    int* tickets = reinterpret_cast<int*>(w + 256);
-    float* part = reinterpret_cast<float*>(w + 256 + dec_ticket_bytes(cache));
-    cudaMemsetAsync(w, 0, 256 + dec_ticket_bytes(cache), st);
+    int* tickets = reinterpret_cast<int*>(w + kStatusBytes);
+    float* part = reinterpret_cast<float*>(w + kStatusBytes + dec_ticket_bytes(cache));
+    // the status header and the merge tickets start at zero
+    const kv_status sc = clear_device(w, kStatusBytes + dec_ticket_bytes(cache), st, "attn_decode_kernel");
+    if (sc != KV_OK) return sc;
     dim3 grid(n_splits, c.Hkv, c.B);
     attn_decode_kernel<T, D, NT, JENSEN><<<grid, kDThreads, smem, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
         sh, out, out_f32, lse, part, tickets, err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
-    kv_status s = check_launch("attn_decode_kernel");
-    if (s != KV_OK) return s;
-    if (getenv("BITKV_DEBUG_SYNC")) {
-        int h_err = 0;
-        cudaMemcpyAsync(&h_err, err, sizeof(int), cudaMemcpyDeviceToHost, st);
-        cudaStreamSynchronize(st);
-        if (h_err) return set_error(KV_ERR_TIMEOUT, "attn_decode_kernel: bounded wait %d gave up", h_err);
-    }
-    return KV_OK;
+    return check_launch("attn_decode_kernel");
 }
 
 }  // namespace
@@ -911,7 +1012,7 @@ int decode_auto_splits(const kv_cache* cache, int Hq) {
 size_t decode_workspace(const kv_cache* cache, int Hq, int n_splits) {
     const kv_layout& L = cache->layout;
     const int G = Hq / L.Hkv;
-    size_t ws = 256 + dec_ticket_bytes(cache);
+    size_t ws = kStatusBytes + dec_ticket_bytes(cache);
     if (n_splits > 1) ws += (size_t)L.B * L.Hkv * n_splits * G * (L.d + 4) * sizeof(float);
     return ws;
 }
@@ -945,6 +1046,14 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
         else { if (two) BITKV_DEC(BF16, 128, 2); else BITKV_DEC(BF16, 128, 1); }
     }
 #undef BITKV_DEC
+}
+
+kv_status launch_dec_operands(const kv_cache* cache, void* Kout, void* Vout, cudaStream_t st) {
+    const DevCache c = make_dev_cache(cache);
+    if (c.kind == KV_CODEBOOK2) return set_error(KV_ERR_UNSUPPORTED, "decode operands: codebook caches not served");
+    if (c.d == 64) return launch_dec_operands_d<64>(c, Kout, Vout, st);
+    if (c.d == 128) return launch_dec_operands_d<128>(c, Kout, Vout, st);
+    return set_error(KV_ERR_UNSUPPORTED, "decode operands: needs head dim 64 or 128");
 }
 
 }  // namespace bitkv

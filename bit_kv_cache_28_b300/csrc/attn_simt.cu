@@ -1,6 +1,8 @@
 // CUDA-core attention over any cache kind, with split-KV partials and the
-// log-sum-exp merge.  It is the exact-fp32 path (fp32 I/O) and the general
-// path for shapes the tensor-core kernel does not take.
+// log-sum-exp merge.  It is the exact-fp32 path: every operand (queries, the
+// dequantised cache entries fmaf(code, s, z), the current chunk) enters the
+// products as the fp32 value it is, and sums run in fp32.  It serves every dtype
+// and the shapes the tensor-core kernel does not take.
 //
 // "Quantized Keys Steal Attention" (abstract): queries of the current chunk
 // attend to the cached chunks and to the current, unquantised chunk; the
@@ -106,8 +108,8 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
             for (int e = tid; e < kSK * D; e += kSimtThreads) {
                 const int t = e / D, ch = e % D;
                 const float2 kv = t < len ? block_entry(cls, blk, D, c.raw_dtype, cent, t, ch) : make_float2(0.f, 0.f);
-                Ks[t * ld + ch] = round_io<T>(kv.x);
-                Vs[t * ld + ch] = round_val<T>(kv.y);
+                Ks[t * ld + ch] = kv.x;     // the exact dequantised entries
+                Vs[t * ld + ch] = kv.y;
             }
             if (cls == CLS_INT2 || cls == CLS_INT4) {
                 quantised = 1;
@@ -321,7 +323,10 @@ static kv_status launch_simt_t(const void* Q, const void* Kc, const void* Vc, in
     const int uc = simt_units_cache(cache);
     const int ut = uc + (n_cur + kSK - 1) / kSK;
     const long long rows = (long long)c.B * Hq * n_q;
-    float* ws_o = static_cast<float*>(ws);
+    // the status header stays zero: this kernel has no bounded waits and no fp16 operands
+    const kv_status sc = clear_device(ws, kStatusBytes, st, "attn_simt_kernel");
+    if (sc != KV_OK) return sc;
+    float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kStatusBytes);
     float2* ws_ml = reinterpret_cast<float2*>(ws_o + (n_splits > 1 ? (long long)n_splits * rows * c.d : 0));
     switch (c.d) {
         case 32: launch_simt_td<T, 32>(Q, Kc, Vc, n_q, n_cur, Hq, c, tau, jensen, psac, n_splits, uc, ut, out, out_f32, lse, ws_o, ws_ml, st); break;
@@ -349,9 +354,9 @@ kv_status launch_attn_simt(const void* Q, const void* Kc, const void* Vc, kv_dty
 }
 
 size_t simt_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits) {
-    if (n_splits <= 1) return 0;
+    if (n_splits <= 1) return kStatusBytes;
     const long long rows = (long long)cache->layout.B * Hq * n_q;
-    return (size_t)n_splits * rows * (cache->layout.d * sizeof(float) + sizeof(float2));
+    return kStatusBytes + (size_t)n_splits * rows * (cache->layout.d * sizeof(float) + sizeof(float2));
 }
 
 }  // namespace bitkv

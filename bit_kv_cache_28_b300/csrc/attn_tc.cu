@@ -17,13 +17,15 @@
 //   warps 4-11  producers: thread 0 bulk-copies (TMA engine) each packed cache
 //               tile -- 4 contiguous blocks -- into a double-buffered staging
 //               area two tiles ahead; all 256 threads expand the staged codes
-//               into K_hat [128 keys x 128] (bf16, single buffer: free once
+//               into K_hat [128 keys x 128] (fp16, single buffer: free once
 //               Q K_hat^T of the tile completes) and V_hat^T [128 channels x 128
 //               keys] (fp16, double buffer), 128-byte-swizzled K-major, plus the
 //               Jensen weights W [4 groups, hi/lo] of the tile; a current-chunk
-//               tile is read from global memory (values transposed).
-//   warp 12     TMEM owner; lane 0 issues S = Q K_hat^T (bf16, Q read from
-//               tensor memory), the Jensen term Delta = (q^2) W^T (bf16, N = 16;
+//               tile is read from global memory (keys converted to fp16, values
+//               transposed).
+//   warp 12     TMEM owner; lane 0 issues S = Q K_hat^T (fp16, Q converted from
+//               bf16 and read from tensor memory), the Jensen term Delta = (q^2) W^T
+//               (bf16, N = 16;
 //               q^2 of a bf16 q is split exactly into bf16 high and low parts,
 //               two MMAs; W columns g and 4 + g hold the high and low bf16 parts
 //               of group g's weights), and O += P V_hat with P read from tensor
@@ -36,7 +38,7 @@
 //
 // Codebook caches ("QuantWM", Methodology: per-channel 4-centroid INT2 keys plus
 // the rank-r compensation q . U coeff in the logit): K_hat comes from a byte-permute
-// lookup of each key's 2-bit indices in bf16 centroid tables, and the compensation
+// lookup of each key's 2-bit indices in fp16 centroid tables, and the compensation
 // is two more fp16 MMAs into S per 16 ranks -- A = U^T q of the query rows (fp32,
 // split into fp16 high + low parts, TMEM columns 384-415, where the Jensen term
 // lives for INT caches), B = the tile's stored fp16 coefficients.  Codebook keys
@@ -45,6 +47,13 @@
 // Dequantisation is exact: a code c at bits [b i, b i + b) of a word becomes the
 // float c 2^(b i) by or-ing it into the mantissa of 2^23 and subtracting 2^23,
 // and fmaf(c 2^(b i), s 2^(-b i), z) rounds c s + z once, as fmaf(c, s, z) does.
+// The operands of both products are fp16: K_hat and V_hat are the fp16 roundings
+// of the dequantised fp32 entries, Q and the current keys the fp16 conversions of
+// their bf16 values (exact inside the fp16 range), P the fp16 rounding of the
+// softmax weights.  fp16 keeps 11 significant bits where bf16 keeps 8, which holds
+// the logits of keys with large outlier channels within the 16-bit tolerance of the
+// exact result.  An entry whose fp16 rounding would be infinite (|x| >= 65520) sets
+// the range flag, status word 1.
 #include <cstdio>
 #include <cstdlib>
 
@@ -70,7 +79,7 @@ constexpr int kMmaWarp = kSoftWarps + kProdWarps;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColD = 384, kColQ = 448;
-constexpr uint32_t kIdescQK = idesc_bf16(kM, kN);   // S = Q K_hat^T
+constexpr uint32_t kIdescQK = idesc_f16(kM, kN);    // S = Q K_hat^T (fp16 operands)
 constexpr uint32_t kIdescJ = idesc_bf16(kM, 16);    // Delta = (q^2) W^T
 constexpr uint32_t kIdescPV = idesc_f16(kM, kD);    // O += P V_hat
 constexpr float kLog2e = 1.4426950408889634f;
@@ -144,6 +153,19 @@ enum {
 __device__ __forceinline__ uint32_t sw_off(int row, int ch, int rows = kM) {
     return (uint32_t)((ch >> 3) * (rows * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
 }
+
+// A pair of bf16 values (lower element in the low half) as an fp16 pair, rounded
+// to nearest even: exact for magnitudes in [2^-14, 65504] (bf16 carries 8
+// significant bits, fp16 11), within 2^-25 below, infinite above.
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
+    return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// True when either half of an fp16 pair is infinite or NaN.
+__device__ __forceinline__ bool h2_nonfinite(uint32_t h) {
+    return (h & 0x7C00u) == 0x7C00u || (h & 0x7C000000u) == 0x7C000000u;
+}
+// The fp16 rounding of x is finite.
+__device__ __forceinline__ bool f16_finite(float x) { return fabsf(x) < 65520.0f; }
 
 // 2^e for an integer e in [-126, 127] (exact).
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
@@ -220,7 +242,7 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned ch
 }
 
 // Keys of a staged cache tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
-// 8 kg .. 8 kg + 7 (one block) into K_hat (bf16).
+// 8 kg .. 8 kg + 7 (one block) into K_hat (fp16).
 template <int BITS>
 __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigned char* stg, int nb, int p) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
@@ -265,29 +287,33 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigne
             }
         }
         uint4 rr;
-        rr.x = pack_bf16(v[0], v[1]);
-        rr.y = pack_bf16(v[2], v[3]);
-        rr.z = pack_bf16(v[4], v[5]);
-        rr.w = pack_bf16(v[6], v[7]);
+        rr.x = pack_f16(v[0], v[1]);
+        rr.y = pack_f16(v[2], v[3]);
+        rr.z = pack_f16(v[4], v[5]);
+        rr.w = pack_f16(v[6], v[7]);
         *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t, jc)) = rr;
     }
 }
 
 // Centroid tables of one (batch, kv head) for the codebook key lookup: channel c's
-// four centroids rounded to bf16, stored byte-planar as two words -- the four low
+// four centroids rounded to fp16, stored byte-planar as two words -- the four low
 // bytes, then the four high bytes -- so that one byte permute with selector
-// nibbles (k, 4 + k) returns centroid k as a bf16.
-__device__ __forceinline__ void fill_centroid_tables(uint32_t* tab, const float* cent, int tid) {
+// nibbles (k, 4 + k) returns centroid k as an fp16.  Returns false if a centroid's
+// fp16 rounding is not finite.
+__device__ __forceinline__ bool fill_centroid_tables(uint32_t* tab, const float* cent, int tid) {
+    bool ok = true;
     for (int ch = tid; ch < kD; ch += kThreads) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(cent) + ch);
-        const uint32_t c01 = pack_bf16(v.x, v.y), c23 = pack_bf16(v.z, v.w);
+        ok = ok && f16_finite(v.x) && f16_finite(v.y) && f16_finite(v.z) && f16_finite(v.w);
+        const uint32_t c01 = pack_f16(v.x, v.y), c23 = pack_f16(v.z, v.w);
         tab[2 * ch] = __byte_perm(c01, c23, 0x6420);
         tab[2 * ch + 1] = __byte_perm(c01, c23, 0x7531);
     }
+    return ok;
 }
 
 // Keys of a staged codebook tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
-// 8 kg .. 8 kg + 7 (one block) into K_hat (bf16) by looking the 2-bit centroid
+// 8 kg .. 8 kg + 7 (one block) into K_hat (fp16) by looking the 2-bit centroid
 // indices up in its channels' tables, two keys at a time.  For the channel pair
 // (2 i, 2 i + 1) the four index bits n = k0 + 4 k1 of a key become the selector
 // bytes (17 k0 + 0x40, 17 k1 + 0x40), i.e. nibbles (k0, 4 + k0, k1, 4 + k1):
@@ -411,8 +437,9 @@ __device__ __forceinline__ void fill_current_values(unsigned char* Vt, const __n
     }
 }
 
-// Current-chunk keys: bf16 rows copied into the swizzled K_hat buffer.
-__device__ __forceinline__ void fill_current_keys(unsigned char* Kt, const __nv_bfloat16* Kcur, long long row0,
+// Current-chunk keys: bf16 rows converted to fp16 into the swizzled K_hat buffer.
+// Returns false if a key's fp16 rounding is not finite.
+__device__ __forceinline__ bool fill_current_keys(unsigned char* Kt, const __nv_bfloat16* Kcur, long long row0,
                                                   int valid, int p) {
     const int jc = p & 15, r0 = p >> 4;
     const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
@@ -422,8 +449,28 @@ __device__ __forceinline__ void fill_current_keys(unsigned char* Kt, const __nv_
         const int row = r0 + 16 * i;
         kv[i] = row < valid ? __ldg(Kg + row * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
     }
+    bool bad = false;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 16 * i, jc)) = kv[i];
+    for (int i = 0; i < 8; ++i) {
+        const uint4 h = make_uint4(bf2_to_h2(kv[i].x), bf2_to_h2(kv[i].y), bf2_to_h2(kv[i].z), bf2_to_h2(kv[i].w));
+        bad |= h2_nonfinite(h.x) | h2_nonfinite(h.y) | h2_nonfinite(h.z) | h2_nonfinite(h.w);
+        *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 16 * i, jc)) = h;
+    }
+    return !bad;
+}
+
+// The cached keys of a staged INT tile stay inside the fp16 range: every entry of a
+// (block, channel) lies between z and fmaf(2^b - 1, s, z), so checking those two
+// bounds for each of the thread's two channels covers the tile.
+template <int BITS>
+__device__ __forceinline__ bool cache_keys_in_f16_range(const unsigned char* stg, int nb, int p) {
+    const int g = p >> 6, c = 2 * (p & 63);
+    if (g >= nb) return true;
+    const IntBlockOffsets o = int_offsets(kD, BITS);
+    const float4 v = *reinterpret_cast<const float4*>(stg + g * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>() +
+                                                      o.km + c * 8);
+    constexpr float kTop = (float)((1 << BITS) - 1);
+    return f16_finite(v.y) && f16_finite(fmaf(kTop, v.x, v.y)) && f16_finite(v.w) && f16_finite(fmaf(kTop, v.z, v.w));
 }
 
 // --------------------------------------------------------------- kernel -----
@@ -506,8 +553,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     // V_hat stage (written by the producers only after the second barrier below)
     float* Us = reinterpret_cast<float*>(sm + M::v + kTile);
     if (kCb) {
-        fill_centroid_tables(reinterpret_cast<uint32_t*>(sm + M::cent),
-                             c.centroids + ((long long)b * c.Hkv + h) * kD * 4, tid);
+        if (!fill_centroid_tables(reinterpret_cast<uint32_t*>(sm + M::cent),
+                                  c.centroids + ((long long)b * c.Hkv + h) * kD * 4, tid))
+            atomicExch(err + 1, 1);
         if (r16 > 0) {
             const float* U = c.psac_u + ((long long)b * c.Hkv + h) * kD * c.r;
             for (int e = tid; e < kD * r16; e += kThreads) {
@@ -544,22 +592,27 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M::slot);
     if (warp < kSoftWarps) {
-        // Q row i -> TMEM lane i, columns kColQ .. kColQ + 63 (two bf16 per column)
+        // Q row i -> TMEM lane i, columns kColQ .. kColQ + 63 (two fp16 per column: the
+        // bf16 queries converted, exactly inside the fp16 range)
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const bool valid = q0 + tid < n_q;
+        bool qbad = false;
 #pragma unroll
         for (int hf = 0; hf < 4; ++hf) {
             uint32_t u[16];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint4 v = valid ? __ldg(Qg + (long long)(q0 + tid) * (kD / 8) + 4 * hf + k) : make_uint4(0, 0, 0, 0);
-                u[4 * k] = v.x;
-                u[4 * k + 1] = v.y;
-                u[4 * k + 2] = v.z;
-                u[4 * k + 3] = v.w;
+                u[4 * k] = bf2_to_h2(v.x);
+                u[4 * k + 1] = bf2_to_h2(v.y);
+                u[4 * k + 2] = bf2_to_h2(v.z);
+                u[4 * k + 3] = bf2_to_h2(v.w);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qbad |= h2_nonfinite(u[4 * k + e]);
             }
             tmem_st16(tmem + lane_addr + kColQ + 16 * hf, u);
         }
+        if (qbad) atomicExch(err + 1, 1);
         if (kCb && r16 > 0) {
             // u = U^T q of row i in fp32, split into fp16 high + low parts (u = hi + lo up
             // to 2^-22 |u|): the A operand of the PSAC MMAs, TMEM columns kColD + 8 ks
@@ -722,6 +775,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 if (r16 > 0) fill_coeff(sm + M::coef, stg, bb, nb, c.rp, r16 / 8, p);
             } else if (cached) {
                 fill_cache_keys<vbits<FMT>()>(sm + M::k, stg, nb, p);
+                if (!cache_keys_in_f16_range<vbits<FMT>()>(stg, nb, p)) atomicExch(err + 1, 1);
                 // TAYLOR2: bf16 weights read by the Jensen MMA with Q K^T (stage s, free
                 // since Q K^T of tile j - 2 completed); EXACT: fp32 steps read by the
                 // softmax, in a ring of 4 like the tile info
@@ -732,9 +786,16 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 else if (JENSEN == KV_JENSEN_ISOTROPIC)
                     fill_weights<vbits<FMT>(), JENSEN>(nullptr, stg, nb, p, jcoef, inf.ss2);
             } else {
-                fill_current_keys(sm + M::k, Kcur, row0, cvalid, p);
+                if (!fill_current_keys(sm + M::k, Kcur, row0, cvalid, p)) atomicExch(err + 1, 1);
             }
             fence_proxy_async();
+            // publish tile j on K_FULL[s] only after the softmax has finished tile j - 2
+            // (its P_FULL[s]): the softmax then has passed its K_FULL[s] wait for tile j - 2,
+            // so that wait can never find the barrier two phases ahead
+            if (j >= 2) {
+                const bool okp = mbar_wait(bar(BAR_P_FULL + s), ((j - 2) >> 1) & 1, &abort_flag, err, 11);
+                if (!__all_sync(0xffffffffu, okp)) break;
+            }
             mbar_arrive(bar(BAR_K_FULL + s));
             // values: the V_hat stage is free once P V of tile j - 2 completed; Q K^T and
             // the softmax of this tile proceed meanwhile
@@ -971,6 +1032,76 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     }
 }
 
+// ------------------------------------------------------- operand dump -----
+// Debug view of the kernel's own operands: the fp16 K_hat and V_hat that the
+// expansion routines above (the same functions the attention kernel's producers
+// run) build from one staged cache tile, written un-swizzled in block-slot order
+// as fp16 [B][Hkv][32 n_blocks][d] (V_hat transposed back to token rows).  One CTA
+// of 256 threads per (tile, kv head, batch); rows of missing blocks are not written.
+template <int FMT>
+struct DumpSmem {
+    static constexpr int k = 0;
+    static constexpr int v = k + kTile;
+    static constexpr int cent = v + kTile;
+    static constexpr int stg = cent + kCentBytes;
+    static constexpr int total = stg + 4 * max_block_bytes<FMT>() + 1024;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kProd)
+tc_operands_kernel(DevCache c, __half* __restrict__ Kout, __half* __restrict__ Vout) {
+    using M = DumpSmem<FMT>;
+    constexpr bool kCb = FMT == FMT_CB2;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int p = threadIdx.x, pw = p >> 5, lane = p & 31;
+    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int nblk = c.n_blocks[seg];
+    const int nb = min(4, nblk - tile * 4);
+    if (nb <= 0) return;
+    const int bb = kCb ? (int)c.block_bytes[seg] : max_block_bytes<FMT>();
+    // stage the tile's blocks (plain 16-byte copies: the staging method is not under test)
+    const uint4* src = reinterpret_cast<const uint4*>(block_ptr(c, b, h, seg, tile * 4));
+    uint4* dst = reinterpret_cast<uint4*>(sm + M::stg);
+    for (int e = p; e < nb * bb / 16; e += kProd) dst[e] = src[e];
+    if (kCb) fill_centroid_tables(reinterpret_cast<uint32_t*>(sm + M::cent),
+                                  c.centroids + ((long long)b * c.Hkv + h) * kD * 4, p);
+    __syncthreads();
+    // keys first, then values (the value routine rescales the staged steps in place)
+    if (kCb) fill_cb_keys(sm + M::k, sm + M::stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
+    else fill_cache_keys<vbits<FMT>()>(sm + M::k, sm + M::stg, nb, p);
+    __syncthreads();
+    fill_cache_values<FMT>(sm + M::v, sm + M::stg, bb, nb, pw, lane);
+    __syncthreads();
+    const long long row0 = ((long long)b * c.Hkv + h) * (long long)nblk * kBlockTokens + (long long)tile * kN;
+    for (int e = p; e < nb * kBlockTokens * (kD / 8); e += kProd) {
+        const int row = e / (kD / 8), ch = e % (kD / 8);
+        *reinterpret_cast<uint4*>(Kout + (row0 + row) * kD + 8 * ch) =
+            *reinterpret_cast<const uint4*>(sm + M::k + sw_off(row, ch));
+    }
+    for (int e = p; e < nb * kBlockTokens * kD; e += kProd) {
+        const int key = e / kD, ch = e % kD;
+        Vout[(row0 + key) * kD + ch] =
+            *reinterpret_cast<const __half*>(sm + M::v + sw_off(ch, key >> 3) + 2 * (key & 7));
+    }
+}
+
+template <int FMT>
+kv_status launch_tc_operands_t(const DevCache& c, void* Kout, void* Vout, cudaStream_t st) {
+    constexpr int kSmem = DumpSmem<FMT>::total;
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(tc_operands_kernel<FMT>), kSmem,
+                                        "tc_operands_kernel");
+    if (sa != KV_OK) return sa;
+    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int tiles = (c.n_blocks[seg] + 3) / 4;
+    if (tiles == 0) return KV_OK;
+    tc_operands_kernel<FMT><<<dim3(tiles, c.Hkv, c.B), kProd, kSmem, st>>>(c, static_cast<__half*>(Kout),
+                                                                          static_cast<__half*>(Vout));
+    return check_launch("tc_operands_kernel");
+}
+
 int g_num_sms = 0;
 
 int num_sms() {
@@ -1036,7 +1167,7 @@ int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq) {
 }
 
 size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits) {
-    size_t ws = 256;  // error word of the bounded waits
+    size_t ws = kStatusBytes;
     if (n_splits > 1) {
         const long long rows = (long long)cache->layout.B * Hq * n_q;
         ws += (size_t)n_splits * rows * (kD * sizeof(float) + sizeof(float2));
@@ -1049,12 +1180,11 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
                          float* lse, void* ws, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     int* err = static_cast<int*>(ws);
-    float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + 256);
+    float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kStatusBytes);
     const long long rows = (long long)c.B * Hq * n_q;
     float2* ws_ml = reinterpret_cast<float2*>(ws_o + (n_splits > 1 ? (long long)n_splits * rows * kD : 0));
-    const bool debug = getenv("BITKV_DEBUG_SYNC") != nullptr;
-    if (debug) cudaMemsetAsync(err, 0, sizeof(int), st);
-    kv_status s;
+    kv_status s = clear_device(ws, kStatusBytes, st, "attn_tc_kernel");
+    if (s != KV_OK) return s;
 #define BITKV_TC(FMT)                                                                                         \
     switch (jensen) {                                                                                         \
         case KV_JENSEN_TAYLOR2:                                                                               \
@@ -1085,14 +1215,17 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
     }
 #undef BITKV_TC
     if (s != KV_OK) return s;
-    if (debug) {
-        int h_err = 0;
-        cudaMemcpyAsync(&h_err, err, sizeof(int), cudaMemcpyDeviceToHost, st);
-        cudaStreamSynchronize(st);
-        if (h_err) return set_error(KV_ERR_TIMEOUT, "attn_tc_kernel: bounded wait %d gave up", h_err);
-    }
     if (n_splits == 1) return KV_OK;
     return launch_lse_merge(KV_BF16, ws_o, ws_ml, n_splits, rows, kD, out, out_f32, lse, st);
+}
+
+kv_status launch_tc_operands(const kv_cache* cache, void* Kout, void* Vout, cudaStream_t st) {
+    const DevCache c = make_dev_cache(cache);
+    if (c.d != kD) return set_error(KV_ERR_UNSUPPORTED, "tensor-core operands: needs head dim 128");
+    if (c.kind == KV_CODEBOOK2) return launch_tc_operands_t<FMT_CB2>(c, Kout, Vout, st);
+    if (c.kind == KV_UNIFORM4) return launch_tc_operands_t<FMT_INT4>(c, Kout, Vout, st);
+    if (c.kind == KV_UNIFORM2) return launch_tc_operands_t<FMT_INT2>(c, Kout, Vout, st);
+    return set_error(KV_ERR_UNSUPPORTED, "tensor-core operands: needs a UNIFORM2, UNIFORM4 or CODEBOOK2 cache");
 }
 
 }  // namespace bitkv

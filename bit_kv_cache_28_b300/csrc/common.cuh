@@ -144,15 +144,6 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// Round an fp32 value to the I/O dtype and back (the attention consumes
-// dequantised entries at the I/O precision).
-template <typename T> __device__ __forceinline__ float round_io(float x) { return to_f32<T>(from_f32<T>(x)); }
-
-// Dequantised cache values enter P V at fp16 for 16-bit I/O (11 significant bits
-// for the attention weights) and at fp32 for fp32 I/O.
-template <typename T> __device__ __forceinline__ float round_val(float x) { return __half2float(__float2half_rn(x)); }
-template <> __device__ __forceinline__ float round_val<float>(float x) { return x; }
-
 // Raw 16-bit cache entry to fp32.
 __device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype) {
     if (raw_dtype == KV_BF16) return __uint_as_float(((uint32_t)bits) << 16);
@@ -187,8 +178,20 @@ __device__ __forceinline__ float log_sinhc(float x) {
     return x + log1pf(-expf(-2.0f * x)) - logf(2.0f * x);
 }
 
+// Every attention workspace starts with a status header of kStatusBytes: int word 0
+// holds the code of a bounded device-side wait that gave up (0: none), word 1 the
+// range flag (an fp16 operand of the tensor-core path would be infinite).  Each
+// call clears the header before its kernels run.
+constexpr size_t kStatusBytes = 256;
+
 // Host-side helpers shared by the launch code.
 DevCache make_dev_cache(const kv_cache* c);
+// Zeroes `bytes` of device memory at `p` on `st` (the status header and whatever
+// else a launch needs cleared); KV_ERR_CUDA if the runtime refuses.
+kv_status clear_device(void* p, size_t bytes, cudaStream_t st, const char* who);
+// Copies the status header at `ws` to the host after the work queued on `st` and
+// maps it to KV_OK, KV_ERR_TIMEOUT or KV_ERR_RANGE.  Synchronises `st`.
+kv_status read_status(const void* ws, cudaStream_t st);
 kv_status set_error(kv_status st, const char* fmt, ...);
 kv_status check_launch(const char* what);
 // An NVTX range named for a C-ABI call, open for the call's duration: a profiler

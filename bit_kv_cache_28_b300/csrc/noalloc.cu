@@ -20,7 +20,10 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[KV_NOALLOC_SCRATCH_BYT
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_dev[kMaxDevices];  // device address of the array, per device, once looked up
+// Device address of the array, per device, looked up once.  It stays valid for the
+// life of the device's primary context: after cudaDeviceReset() the module is
+// loaded again elsewhere and the kept address is stale.
+void* g_scratch_dev[kMaxDevices];
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name only stands in for the symbol; the address must come from the
@@ -76,4 +79,13 @@ extern "C" kv_status kv_attention_noalloc(const void* Q, const void* Kcur, const
     kv_status s = scratch_address(&scratch);
     if (s != KV_OK) return s;
     return kv_attention(Q, Kcur, Vcur, dtype, n_q, n_cur, Hq, cache, &o, out, lse, scratch, cap, stream);
+}
+
+// The status words of the last no-alloc call sit at the start of the fixed array,
+// where kv_attention put them; callers without a workspace read them here.
+extern "C" kv_status kv_attention_noalloc_status(void* stream) {
+    void* scratch = nullptr;
+    const kv_status s = scratch_address(&scratch);
+    if (s != KV_OK) return s;
+    return read_status(scratch, static_cast<cudaStream_t>(stream));
 }

@@ -40,7 +40,12 @@ typedef enum {
     KV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than kv_attention_workspace() */
     KV_ERR_ALIGNMENT = 5,    /* a pointer is not 16-byte aligned */
     KV_ERR_CUDA = 6,         /* a CUDA launch or query failed */
-    KV_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up */
+    KV_ERR_TIMEOUT = 7,      /* a bounded device-side wait gave up: the output is incomplete.  Kernels run
+                                asynchronously, so kv_attention reports it only through
+                                kv_attention_status() (kv_attention_noalloc_status()), or at once
+                                when the environment variable BITKV_DEBUG_SYNC is set */
+    KV_ERR_RANGE = 8         /* an operand of the tensor-core path lies outside the fp16 range
+                                (|x| >= 65520); reported like KV_ERR_TIMEOUT */
 } kv_status;
 
 typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
@@ -180,15 +185,36 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
  * x_c = tau q_c s_c / 2, ISOTROPIC (tau^2/24) |q|^2 mean_c s_c^2 (the query-norm
  * form; equal to TAYLOR2 when a group's steps are equal), using the step sizes
  * of the key's group; zero for
- * RAW16 windows and codebook keys.  Dequantised cache entries are rounded to
- * the I/O dtype before the products.
+ * RAW16 windows and codebook keys.
+ * Precision: the result is defined over the exact dequantised entries
+ * fmaf(code, s, z) and the inputs as given.  The CUDA-core path (KV_PATH_SIMT)
+ * computes that definition in fp32.  The decode path multiplies exact integer
+ * codes by the query scaled by the step, split into fp16 high and low parts
+ * (about 22 bits), and adds the zero-point term in fp32.  The tensor-core path
+ * holds the operands of both products in fp16: K_hat and V_hat are the fp16
+ * roundings of the dequantised entries, Q and the current keys the fp16
+ * conversions of their bf16 values (exact inside the fp16 range), P the fp16
+ * rounding of the softmax weights; inputs or cache entries whose fp16 rounding
+ * is infinite raise the range flag (KV_ERR_RANGE).  All paths accumulate in
+ * fp32.  The 16-bit output is the round-to-nearest-even of the fp32 result.
  *   Q (device) [B][Hq][n_q][d]; Kcur, Vcur (device) [B][Hkv][n_cur][d] (may be
  *   NULL when n_cur == 0); out (device) [B][Hq][n_q][d] in dtype (fp32 if
  *   opts->out_f32); lse (device, nullable) fp32 [B][Hq][n_q] natural-log
- *   partition function.  workspace (device) of ws_bytes >= kv_attention_workspace(). */
+ *   partition function.  workspace (device, 16-byte aligned) of ws_bytes >=
+ *   kv_attention_workspace() (at least 256 bytes).  Its first 256 bytes are the
+ *   call's status words, cleared by each call before its kernels run; read them
+ *   with kv_attention_status() after the call.  Without BITKV_DEBUG_SYNC a
+ *   KV_OK return means the work was queued, not that no device-side wait gave
+ *   up. */
 kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q, int n_cur,
                        int Hq, const kv_cache* cache, const kv_attn_opts* opts, void* out, float* lse,
                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Status of the last kv_attention call that used `workspace` (device): waits for
+ * the work queued on `stream`, copies the status words to the host and returns
+ * KV_OK, KV_ERR_TIMEOUT (a bounded device-side wait gave up: that call's output
+ * is incomplete) or KV_ERR_RANGE (see kv_attention).  Synchronous. */
+kv_status kv_attention_status(const void* workspace, void* stream);
 
 /* kv_attention without a workspace argument, for callers that cannot allocate
  * device memory: code running where cudaMalloc is unavailable or not allowed
@@ -215,6 +241,14 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
 kv_status kv_attention_noalloc(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q,
                                int n_cur, int Hq, const kv_cache* cache, const kv_attn_opts* opts, void* out,
                                float* lse, void* stream);
+
+/* kv_attention_status() for the last kv_attention_noalloc call on the current
+ * device: reads the status words in the library's fixed array after the work
+ * queued on `stream`.  Synchronous.  The array's device address is looked up once
+ * per device and kept; after cudaDeviceReset() (or any re-creation of the
+ * device's primary context) the kept address is stale, so neither no-alloc call
+ * may be used again in that process. */
+kv_status kv_attention_noalloc_status(void* stream);
 
 /* Per-window bit-widths from window/question similarity ([WQ] 何が新しいのか
  * table, 技術的に面白い点: first window FP16).  Host only.  sim (host) [n_windows];
@@ -267,11 +301,28 @@ size_t kv_psac_workspace(const kv_layout* layout);
 kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache* cache, float* eigvals_out,
                         void* workspace, size_t ws_bytes, void* stream);
 
-/* Debug: write the cache's dequantised entries as fp32 in logical token
- * order, K_out and V_out (device) [B][Hkv][n_tokens][d], computed by the same
- * device dequantisation routine the attention kernels use (before rounding
- * to the I/O dtype).  Positions never appended are left untouched. */
+/* Debug: write the cache's dequantised entries fmaf(code, s, z) (codebook keys:
+ * the centroid; RAW16 entries as stored) as fp32 in logical token order, K_out
+ * and V_out (device) [B][Hkv][n_tokens][d].  Computed by the device routine the
+ * CUDA-core attention kernel (KV_PATH_SIMT) reads the cache with; the tensor-core
+ * and decode kernels expand the cache with their own routines, which
+ * kv_debug_operands() exposes.  Positions never appended are left untouched. */
 kv_status kv_dequantize(const kv_cache* cache, float* K_out, float* V_out, void* stream);
+
+/* Debug: the cache operands an attention kernel builds for its products, made by
+ * that kernel's own device routines and written in stream slot order: K_out and
+ * V_out (device, 16-byte aligned) fp16 [B][Hkv][32 n][d], n the cache's blocks
+ * over all segments in memory order (FP16, INT4, INT2), token t of block i at
+ * slot 32 i + t (pad slots included).
+ *   path KV_PATH_TC (UNIFORM2 / UNIFORM4 / CODEBOOK2, d 128): the tensor-core
+ *     kernel's K_hat and V_hat (the fp16 roundings of the dequantised entries),
+ *     expanded by its producer routines from a staged tile and un-swizzled.
+ *   path KV_PATH_DECODE (UNIFORM2 / UNIFORM4 / MIXED, d 64 or 128): the decode
+ *     kernel forms no dequantised entry; its key and value operands are the codes,
+ *     as the exact fp16 integers its extraction routine feeds the MMAs.  FP16
+ *     slots are not written (that path reads them as stored).
+ * Async on `stream`. */
+kv_status kv_debug_operands(const kv_cache* cache, int path, void* K_out, void* V_out, void* stream);
 
 /* Message of the last failure on this thread ("" if none). */
 const char* kv_last_error(void);

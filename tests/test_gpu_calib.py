@@ -12,7 +12,7 @@ import pytest
 from bit_kv_cache_28_b300 import bitkv as B
 from bit_kv_cache_28_b300 import synth
 from oracle import codebook as OC, psac as OP, attention as OA
-from helpers import to_dev, run_attention, out_tol
+from helpers import to_dev, run_attention, assert_close, TIGHT
 
 pytestmark = pytest.mark.gpu
 
@@ -85,5 +85,4 @@ def test_codebook_calibration_chain():
     assert np.array_equal(tc.data.cpu().numpy().reshape(oc.data.shape), oc.data)
     ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", psac_U=U)
     o, l = run_attention(tc, case, psac=1, out_f32=True, path=B.KV_PATH_SIMT)
-    assert (np.abs(o - ro) <= out_tol("bf16", True, ro)).all()
-    assert np.abs(l - rl).max() < 2e-3
+    assert_close(o, l, ro, rl, TIGHT)      # the CUDA-core path computes the definition

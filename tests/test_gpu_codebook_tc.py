@@ -8,20 +8,9 @@ from bit_kv_cache_28_b300 import bitkv as B
 from bit_kv_cache_28_b300 import synth
 from oracle import codebook as OC, psac as OP
 from oracle import attention as OA
-from helpers import run_attention, out_tol, to_dev
+from helpers import run_attention, to_dev, attention_checked, assert_close, tol, TIGHT
 
 pytestmark = pytest.mark.gpu
-
-
-def check(out, lse, ref_o, ref_lse, out_f32, rows=None):
-    if rows is not None:
-        out = out[:, :, rows]
-        lse = lse[:, :, rows]
-    err = np.abs(out - ref_o)
-    tol = out_tol("bf16", out_f32, ref_o)
-    worst = np.unravel_index(np.argmax(err - tol), err.shape)
-    assert (err <= tol).all(), f"max err {err.max():.3e} at {worst} (tol {tol[worst]:.3e})"
-    assert np.abs(lse - ref_lse).max() < 2e-3
 
 
 def oracle_calibrated_cache(case, n, r):
@@ -50,12 +39,11 @@ def test_codebook_tc_small(r):
     case = synth.codebook_case(seed=71, H=2, d=128, n_cache=450, n_cur=150, n_hist=128)
     tc, oc, U = oracle_calibrated_cache(case, 450, r)
     for psac in ((0, 1) if r else (0,)):
-        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16",
-                                         psac_U=U if psac else None)
+        args = (oc, case["Q"], case["K_cur"], case["V_cur"], "bf16")
+        ref = OA.attention_over_cache(*args, psac_U=U if psac else None)
+        tight = OA.attention_over_cache(*args, psac_U=U if psac else None, operand_dtype="f16")
         for splits in (1, 3):
-            for out_f32 in (True, False):
-                o, l = run_attention(tc, case, psac=psac, out_f32=out_f32, path=B.KV_PATH_TC, splits=splits)
-                check(o, l, ro, rl, out_f32)
+            attention_checked(tc, case, ref, "bf16", tight, psac=psac, path=B.KV_PATH_TC, splits=splits)
 
 
 def test_codebook_tc_matches_simt_and_jensen_has_no_effect():
@@ -67,7 +55,7 @@ def test_codebook_tc_matches_simt_and_jensen_has_no_effect():
     o1, l1 = run_attention(tc, case, psac=1, jensen=1, out_f32=True, path=B.KV_PATH_TC)
     assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
     o2, l2 = run_attention(tc, case, psac=1, out_f32=True, path=B.KV_PATH_SIMT)
-    assert np.abs(o0 - o2).max() < 2e-3 and np.abs(l0 - l2).max() < 2e-3
+    assert_close(o0, l0, o2, l2, tol("bf16"))
 
 
 def test_codebook_workload_tc_sampled():
@@ -91,13 +79,16 @@ def test_codebook_workload_tc_sampled():
     assert path == B.KV_PATH_TC
     o_tc, l_tc = run_attention(tc, case, psac=1, out_f32=True)
     o_si, l_si = run_attention(tc, case, psac=1, out_f32=True, path=B.KV_PATH_SIMT)
-    assert np.abs(o_tc - o_si).max() < 2e-3 and np.abs(l_tc - l_si).max() < 2e-3
+    assert_close(o_tc, l_tc, o_si, l_si, tol("bf16"))
     cent = tc.centroids.cpu().numpy().reshape(1, H, d, 4)
     U = tc.psac_u.cpu().numpy().reshape(1, H, d, r)
     rows = np.random.default_rng(2).choice(1560, 32, replace=False)
     for h in [0, 13]:
         sl = slice(h, h + 1)
         oc = OC.build_codebook(case["K_cache"][:, sl], case["V_cache"][:, sl], cent[:, sl], U[:, sl], nb)
-        ro, rl = OA.attention_over_cache(oc, case["Q"][:, sl], case["K_cur"][:, sl], case["V_cur"][:, sl], "bf16",
-                                         psac_U=U[:, sl], rows=rows)
-        check(o_tc[:, sl], l_tc[:, sl], ro, rl, True, rows=rows)
+        args = (oc, case["Q"][:, sl], case["K_cur"][:, sl], case["V_cur"][:, sl], "bf16")
+        ref = OA.attention_over_cache(*args, psac_U=U[:, sl], rows=rows)
+        tight = OA.attention_over_cache(*args, psac_U=U[:, sl], rows=rows, operand_dtype="f16")
+        assert_close(o_tc[:, sl], l_tc[:, sl], ref[0], ref[1], tol("bf16"), rows=rows)
+        assert_close(o_tc[:, sl], l_tc[:, sl], tight[0], tight[1], TIGHT, rows=rows)
+        assert_close(o_si[:, sl], l_si[:, sl], ref[0], ref[1], TIGHT, rows=rows)

@@ -1,9 +1,10 @@
 """GPU parity of the split-K decode kernel (one query per sequence) against the oracle.
 
 The decode kernel never forms dequantised 16-bit key or value tiles: it folds the
-step sizes and zero points into the query and the attention weights, so it
-consumes the dequantised entries at fp32 and the oracle is run with
-operands='f32'.
+step sizes and zero points into the query (fp16 high + low parts, ~22 bits) and the
+attention weights, so it is held to 2e-3 against the oracle's definition itself (inside
+the benchmark spec 1e-2 for its 16-bit I/O); its 16-bit outputs must be the rounding of the
+fp32 result.
 """
 
 import numpy as np
@@ -13,19 +14,13 @@ from bit_kv_cache_28_b300 import bitkv as B
 from bit_kv_cache_28_b300 import synth
 from oracle import layout as OL, window as OW
 from oracle import attention as OA
-from helpers import gpu_mixed, gpu_uniform, run_attention, out_tol
+from helpers import gpu_mixed, gpu_uniform, run_attention, assert_close, assert_rounding_of, TIGHT
 
 pytestmark = pytest.mark.gpu
 
 
-def check(out, lse, ref_o, ref_lse, dtype, out_f32):
-    err = np.abs(out - ref_o)
-    tol = out_tol(dtype, out_f32, ref_o)
-    worst = np.unravel_index(np.argmax(err - tol), err.shape)
-    assert (err <= tol).all(), f"max err {err.max():.3e} at {worst} (tol {tol[worst]:.3e})"
-    fin = np.isfinite(ref_lse)
-    assert (np.isfinite(lse) == fin).all()
-    assert np.abs(lse[fin] - ref_lse[fin]).max(initial=0.0) < 2e-3
+def check(out, lse, ref_o, ref_lse):
+    assert_close(out, lse, ref_o, ref_lse, TIGHT)
 
 
 def mixed_case(case, frac16=0.2, frac4=0.3):
@@ -44,11 +39,11 @@ def test_decode_workload_full():
     path, splits = B.kv_attention_plan(tc.c, B.KV_F16, 1, 1, 28)
     assert path == B.KV_PATH_DECODE and splits > 1
     for jensen in (0, 1, 3):
-        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=jensen, operands="f32")
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=jensen)
         o, l = run_attention(tc, case, jensen=jensen, out_f32=True)
-        check(o, l, ro, rl, "f16", True)
+        check(o, l, ro, rl)
         o16, l16 = run_attention(tc, case, jensen=jensen, out_f32=False)
-        check(o16, l16, ro, rl, "f16", False)
+        assert_rounding_of(o16, o, "f16")
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -62,10 +57,10 @@ def test_decode_mixed_ragged(dtype, n_cur):
         case["V_cur"] = synth.to_dtype_values(rng.standard_normal((3, 2, n_cur, 64)), dtype)
     tc, oc = mixed_case(case)
     for jensen in (0, 1, 2, 3):
-        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], dtype, jensen=jensen, operands="f32")
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], dtype, jensen=jensen)
         for splits in (1, 3, 7):
             o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
-            check(o, l, ro, rl, dtype, True)
+            check(o, l, ro, rl)
 
 
 @pytest.mark.parametrize("bits", [2, 4])
@@ -77,20 +72,20 @@ def test_decode_uniform(bits, d, Hq, Hkv):
     oc = OL.build_uniform(case["K_cache"], case["V_cache"], bits, case["chunks"],
                           sum((n + 31) // 32 for n in case["chunks"]))
     for jensen in (0, 1, 3):
-        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen, operands="f32")
+        ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "bf16", jensen=jensen)
         for splits in (0, 2):
             o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
-            check(o, l, ro, rl, "bf16", True)
-        o, l = run_attention(tc, case, jensen=jensen, out_f32=False, path=B.KV_PATH_DECODE)
-        check(o, l, ro, rl, "bf16", False)
+            check(o, l, ro, rl)
+        o16, _ = run_attention(tc, case, jensen=jensen, out_f32=False, path=B.KV_PATH_DECODE, splits=2)
+        assert_rounding_of(o16, o, "bf16")
 
 
 def test_decode_mixed_d128_f16():
     case = synth.decode_case(seed=83, B=2, Hq=8, Hkv=2, d=128, n_cache=700)
     tc, oc = mixed_case(case)
-    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=1, operands="f32")
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=1)
     o, l = run_attention(tc, case, jensen=1, out_f32=True)
-    check(o, l, ro, rl, "f16", True)
+    check(o, l, ro, rl)
 
 
 def test_decode_empty_cache_and_single_block():
@@ -98,13 +93,13 @@ def test_decode_empty_cache_and_single_block():
     empty = B.TorchCache(1, 1, 64, B.KV_MIXED, (1, 1, 1), raw_dtype=B.KV_F16)
     oc0 = OL.build_mixed(case["K_cache"][:, :, :0], case["V_cache"][:, :, :0], np.zeros((1, 0), int),
                          [1, 1, 1], "f16")
-    ro, rl = OA.attention_over_cache(oc0, case["Q"], case["K_cur"], case["V_cur"], "f16", operands="f32")
+    ro, rl = OA.attention_over_cache(oc0, case["Q"], case["K_cur"], case["V_cur"], "f16")
     o, l = run_attention(empty, case, out_f32=True, path=B.KV_PATH_DECODE)
-    check(o, l, ro, rl, "f16", True)
+    check(o, l, ro, rl)
     tc, oc = mixed_case(case)          # one window of 20 tokens, FP16 (window 0)
-    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", operands="f32")
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16")
     o, l = run_attention(tc, case, out_f32=True, path=B.KV_PATH_DECODE, splits=4)
-    check(o, l, ro, rl, "f16", True)
+    check(o, l, ro, rl)
 
 
 def test_decode_matches_simt_path():
@@ -113,7 +108,7 @@ def test_decode_matches_simt_path():
     tc, _ = mixed_case(case, 0.1, 0.4)
     o_d, l_d = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_DECODE)
     o_s, l_s = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_SIMT)
-    assert np.abs(o_d - o_s).max() < 2e-3 and np.abs(l_d - l_s).max() < 2e-3
+    assert_close(o_d, l_d, o_s, l_s, TIGHT)
 
 
 def test_decode_over_rollout_cache_sampled():
@@ -131,5 +126,5 @@ def test_decode_over_rollout_cache_sampled():
         sl = slice(h, h + 1)
         oc = OL.build_uniform(case["K_cache"][:, sl], case["V_cache"][:, sl], 2, chunks, nb)
         ro, rl = OA.attention_over_cache(oc, case["Q"][:, sl], case["K_cur"][:, sl], case["V_cur"][:, sl], "bf16",
-                                         jensen=1, operands="f32")
-        check(o[:, sl], l[:, sl], ro, rl, "bf16", True)
+                                         jensen=1)
+        check(o[:, sl], l[:, sl], ro, rl)

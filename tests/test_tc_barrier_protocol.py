@@ -17,18 +17,13 @@ checks on every schedule that:
   the softmax's P over it, read by P V), O (the P V sums, read at the end), and the
   4-slot rings of per-tile data the softmax reads;
 - every schedule ends with every role done.
-Two earlier versions of the protocol are kept as switches, and the model must find
-their races: Q K^T of tile j issued once P V of tile j - 2 was issued (not completed),
-and the epilogue waiting on the per-P V barrier with the last tile's parity.
-
-One property rests on timing, not on a barrier, and the model states it as an
-assumption (``softmax_keeps_up``): the softmax reaches its K_FULL wait for tile j before
-the producers publish the keys of tile j + 2 on the same barrier.  The barriers let the
-producers publish tile j + 2 as soon as the softmax has finished tile j - 1; the softmax
-then needs only a loop back-edge (at the first tile, its short prologue) to reach the
-wait, while the producers need a Q K^T and a full key expansion.  Without the
-assumption the model finds the schedule where the wait is two phases behind (a bounded
-wait then gives up); ``test_model_finds_the_softmax_lead`` keeps that visible.
+No property rests on timing: the schedules are arbitrary interleavings.  Three earlier
+versions of the protocol are kept as switches, and the model must find their races:
+Q K^T of tile j issued once P V of tile j - 2 was issued (not completed); the epilogue
+waiting on the per-P V barrier with the last tile's parity; and the producers publishing
+tile j's keys without waiting for the softmax's P_FULL of tile j - 2, where the
+softmax's K_FULL wait for tile j - 2 can then find the barrier two phases ahead (the
+kernel once relied on the softmax being fast enough instead).
 """
 
 import random
@@ -49,11 +44,10 @@ class Bar:
 
 
 class Model:
-    def __init__(self, T, seed, old_qk_rule=False, old_epilogue=False, softmax_keeps_up=True):
+    def __init__(self, T, seed, old_qk_rule=False, old_epilogue=False, old_publish=False):
         self.T, self.rng = T, random.Random(seed)
         self.old_qk_rule, self.old_epilogue = old_qk_rule, old_epilogue
-        self.softmax_keeps_up = softmax_keeps_up
-        self.softmax_at = 0                   # K_FULL waits the softmax has passed
+        self.old_publish = old_publish
         names = ["K_FULL0", "K_FULL1", "V_FULL0", "V_FULL1", "V_EMPTY0", "V_EMPTY1", "S_FULL0", "S_FULL1",
                  "P_FULL0", "P_FULL1", "O_DONE", "K_EMPTY", "MMA_DONE"]
         self.bar = {n: Bar(n) for n in names}
@@ -131,9 +125,9 @@ class Model:
                 yield from self.wait("K_EMPTY", j - 1)
             self.khat = j
             self.ring[j & 3] = j
-            # timing assumption: the softmax has passed its K_FULL wait for tile j - 2
-            while self.softmax_keeps_up and j >= 2 and self.softmax_at < j - 1:
-                yield
+            # tile j is published only after the softmax finished tile j - 2
+            if j >= 2 and not self.old_publish:
+                yield from self.wait(f"P_FULL{s}", (j - 2) >> 1)
             self.bar[f"K_FULL{s}"].done += 1
             yield
             if j >= 2:
@@ -167,7 +161,6 @@ class Model:
         for j in range(T):
             s = j & 1
             yield from self.wait(f"K_FULL{s}", j >> 1)
-            self.softmax_at = j + 1
             if self.ring[j & 3] != j:
                 self.errors.append(f"softmax({j}) reads ring slot holding {self.ring[j & 3]}")
             yield from self.wait(f"S_FULL{s}", j >> 1)
@@ -241,12 +234,12 @@ def test_model_finds_the_epilogue_parity_race():
     assert hits > 0
 
 
-def test_model_finds_the_softmax_lead():
-    """Without the timing assumption the producers can publish tile j + 2 before the softmax
-    waits for tile j, and that wait is two phases behind."""
+def test_model_finds_the_unguarded_publish():
+    """Without the P_FULL wait the producers can publish tile j + 2 before the softmax waits
+    for tile j, and that wait is two phases behind."""
     hits = 0
     for seed in range(400):
-        m = Model(3, seed, softmax_keeps_up=False)
+        m = Model(3, seed, old_publish=True)
         m.run()
         hits += any(e.startswith("K_FULL") for e in m.errors)
     assert hits > 0
