@@ -26,6 +26,21 @@ which equals delta_taylor2 whenever a group's steps are all equal.
 
 applied to quantised cached keys only (zero for RAW16 windows and the current
 chunk).  All sums and the softmax are fp64; the output is returned in fp64.
+
+Codebook keys (QuantWM) have no step size.  Their second-order form follows the
+same expansion, log E[exp(X)] = Var(X) / 2 for a zero-mean logit error X =
+tau q.e, with the channels' residuals e_c independent of variance v_c (measured
+on the fitted keys):
+
+    delta_taylor2 = (tau^2 / 2) sum_c q'_c^2 v_c,
+    delta_isotropic = (tau^2 / 2) |q'|^2 mean_c v_c,
+
+where q' = q - U (U^T q) when the PSAC term is on (PSAC restores the error
+component along U, so only the query's part outside that subspace sees the
+remaining error) and q' = q otherwise.  For uniform steps v_c = s_c^2 / 12 this is
+delta_taylor2 above.  EXACT has no closed form for an empirical residual and is
+not defined for codebook keys.  The term is one value per query row, the same for
+every cached key.
 """
 
 from __future__ import annotations
@@ -71,6 +86,23 @@ def jensen_delta(Q, s_groups, tau, mode):
         ms2 = (S * S).mean(-1)                     # mean_c s_c^2 of each group
         return (tau * tau / 24.0) * qn2[:, None] * ms2[None, :]
     raise ValueError(mode)
+
+
+def codebook_jensen(Q, v, tau, mode, U=None):
+    """Per-query Jensen correction for codebook keys: Q [nq, d], v [d] residual variances,
+    U [d, r] PSAC basis (None: PSAC off).  Returns delta [nq] (fp64)."""
+    Q = np.asarray(Q, F64)
+    v = np.asarray(v, F64)
+    if U is not None:
+        U = np.asarray(U, F64)
+        Q = Q - (Q @ U) @ U.T
+    if mode == JENSEN_OFF:
+        return np.zeros(Q.shape[0], F64)
+    if mode == JENSEN_TAYLOR2:
+        return 0.5 * tau * tau * ((Q * Q) @ v)
+    if mode == JENSEN_ISOTROPIC:
+        return 0.5 * tau * tau * (Q * Q).sum(-1) * v.mean()
+    raise ValueError("the EXACT Jensen form is not defined for codebook keys")
 
 
 def softmax_attend(logits, Vall):
@@ -159,6 +191,7 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
         rows = np.arange(nq)
     store = (lambda x: np.asarray(x, np.float32)) if operand_dtype is None else \
         (lambda x: round_to(x, operand_dtype))
+    cb_var = getattr(cache, "resid_var", None)     # codebook caches with residual variances
     o = np.zeros((B, Hq, len(rows), d), F64)
     lse = np.zeros((B, Hq, len(rows)), F64)
     for b in range(B):
@@ -173,7 +206,11 @@ def attention_over_cache(cache, Q, Kcur, Vcur, io_dtype, tau=None, jensen=JENSEN
                 q_in = Q[b, hq, rows].astype(F64)
                 q = store(Q[b, hq, rows]).astype(F64)
                 delta = None
-                if jensen != JENSEN_OFF and Kc.shape[0] > 0:
+                if jensen != JENSEN_OFF and Kc.shape[0] > 0 and cb_var is not None:
+                    U = None if psac_U is None else psac_U[b, hk]
+                    dq = codebook_jensen(q_in, cb_var[b, hk], tau, jensen, U)
+                    delta = np.repeat(dq[:, None], Kc.shape[0], axis=1)
+                elif jensen != JENSEN_OFF and Kc.shape[0] > 0:
                     dg = jensen_delta(q_in, lg["ks"], tau, jensen)
                     dg = dg * lg["quantised"][None, :]
                     delta = dg[:, lg["kgroup"]]

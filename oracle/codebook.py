@@ -19,6 +19,27 @@ reading is a per-(head, channel) 1-D Lloyd k-means with 4 centroids:
 The exact member sum (``math.fsum``) equals any-order fp64 summation whenever
 that summation is exact, which holds for bf16 inputs of magnitude >= 2^-30 at
 these sizes.
+
+QSAC with residual ranges.  The pages say QSAC weighs the historical queries'
+sensitivity together with the range of the residuals, protecting the channels
+that matter more for attention.  A per-channel weight cannot do that inside a
+1-D mean-squared k-means (it cancels), so the reading that lets it act is a
+per-channel choice of objective:
+
+* relative sensitivity rho_c = w_c / max_c' w_c' (fp64 of the fp32 weights), in
+  [0, 1]; rho = 0 when every weight is 0;
+* the same quantile initialisation and nearest-centroid assignment, and the
+  update mu_k = mean_k + rho_c (mid_k - mean_k): mean_k the members' mean (the
+  mean-squared centroid) and mid_k = (min_k + max_k) / 2 the members' mid-range
+  (the centroid that minimises the cluster's largest residual |x - mu|), each
+  operation one fp64 rounding in that order.
+
+rho = 0 is Lloyd; the most sensitive channel (rho = 1) iterates towards the
+smallest residual range; channels in between blend the two.
+
+Residual variance (for the Jensen term of codebook keys): v_c = (1/n) sum_t
+(x_t - mu_a(t))^2 over the fitted keys with the stored fp32 centroids and the
+stored nearest index a(t), summed in fp64.
 """
 
 from __future__ import annotations
@@ -62,6 +83,59 @@ def sensitivity(Qhist):
     return (Q * Q).mean(axis=0)
 
 
+def sensitivity_f32(Qhist):
+    """The stored weight: fp32 of (sum_t q_{t,c}^2, summed in token order in fp64) / n."""
+    Q = np.asarray(Qhist, F64)
+    return (np.cumsum(Q * Q, axis=0)[-1] / Q.shape[0]).astype(F32)
+
+
+def relative_sensitivity(w32):
+    """rho_c = w_c / max_c' w_c' in fp64 from the fp32 weights (0 when all are 0)."""
+    w = np.asarray(w32, F32).astype(F64)
+    m = w.max()
+    return np.zeros_like(w) if m == 0.0 else w / m
+
+
+def kmeans_1d_range(x, rho, k=4, iters=20):
+    """QSAC with residual range of one channel: quantile init, nearest assignment, and
+    mu_k = mean_k + rho (mid_k - mean_k); returns fp64 centroids [k]."""
+    x = np.asarray(x, F64)
+    n = x.shape[0]
+    xs = np.sort(x)
+    mu = np.array([xs[(2 * j + 1) * n // (2 * k)] for j in range(k)], F64)
+    rho = F64(rho)
+    for _ in range(iters):
+        a = nearest(x, mu)
+        new = mu.copy()
+        for j in range(k):
+            mem = x[a == j]
+            if mem.shape[0] > 0:
+                mean = F64(math.fsum(mem.tolist()) / mem.shape[0])
+                mid = (F64(mem.min()) + F64(mem.max())) * 0.5
+                new[j] = mean + rho * (mid - mean)
+        mu = new
+    return mu
+
+
+def fit_centroids_range(Kh, w32, iters=20):
+    """QSAC-with-residual-range centroids fp32 [d, 4] of one head's keys Kh [n, d], given the
+    channels' fp32 sensitivity weights w32 [d]."""
+    Kh = np.asarray(Kh, F64)
+    rho = relative_sensitivity(w32)
+    return np.stack([kmeans_1d_range(Kh[:, c], rho[c], 4, iters) for c in range(Kh.shape[1])]).astype(F32)
+
+
+def residual_var(Kh, cent):
+    """v_c = mean_t (x_t - mu_a(t))^2 of one head's keys Kh [n, d] against fp32 centroids [d, 4]."""
+    Kh = np.asarray(Kh, F64)
+    v = np.zeros(Kh.shape[1], F64)
+    for c in range(Kh.shape[1]):
+        mu = np.asarray(cent[c], F32).astype(F64)
+        e = Kh[:, c] - mu[nearest(Kh[:, c], mu)]
+        v[c] = (e * e).sum() / Kh.shape[0]
+    return v
+
+
 def fit_centroids(Kh, iters=20):
     """Centroids fp32 [d, 4] of one head's cached keys Kh [n, d]."""
     Kh = np.asarray(Kh, F64)
@@ -99,12 +173,14 @@ def encode_cb_blocks(Kb, Vb, cent, coeff, nvalid, r):
     return dict(bytes=raw, idx=idx, khat=khat, vhat=vhat, coeff=cq[..., :r])
 
 
-def build_codebook(K, V, cent, U, cap_blocks):
+def build_codebook(K, V, cent, U, cap_blocks, resid_var=None):
     """Codebook cache of one prefill of n tokens per (b, head).
 
     K, V: fp32 [B, H, n, d] (bf16 values); cent fp32 [B, H, d, 4];
     U: fp32 [B, H, d, r] PSAC basis or None (r = 0).
-    Key step sizes do not exist for codebook keys, so no Jensen term applies.
+    resid_var: fp32 [B, H, d] per-channel residual variances, or None.  Codebook
+    keys have no step sizes: without residual variances no Jensen term applies;
+    with them, the attention applies the codebook form (attention.codebook_jensen).
     """
     from .psac import psac_coeff
     K = np.asarray(K, F32)
@@ -141,4 +217,5 @@ def build_codebook(K, V, cent, U, cap_blocks):
                     c.blk_pos[b, j] = j * BLOCK
     c.n_blocks = [nb]
     c.n_tokens = n
+    c.resid_var = None if resid_var is None else np.asarray(resid_var, F32)
     return c

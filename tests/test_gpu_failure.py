@@ -106,7 +106,7 @@ def test_tc_range_flag_for_queries_beyond_fp16():
     case = synth.chunk_case(98, B=1, Hkv=1, d=128, chunks=[64], n_cur=32, n_q=32, dtype="bf16")
     tc = gpu_uniform(case, 2)
     Q = case["Q"].copy()
-    Q[0, 0, 5, 17] = synth.to_bf16_values(np.float32(70000.0))
+    Q[0, 0, 5, 17] = synth.to_bf16_values(np.array([70000.0], np.float32))[0]
     _, _, ws = _call(tc, case, B.KV_PATH_TC, jensen=0, Q=Q)
     with pytest.raises(B.BitKVError) as e:
         B.kv_attention_status(ws)
