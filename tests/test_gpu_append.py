@@ -27,8 +27,10 @@ def uniform_pair(case, bits):
 
 
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 64), ("bf16", 256), ("f32", 32)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 128), ("f16", 64), ("f32", 64), ("bf16", 256),
+                                     ("f32", 32), ("f32", 128)])
 def test_uniform_append_ragged(bits, dtype, d):
+    """16-bit inputs of head dim 128 take the warp-per-block kernel, the rest the general one."""
     case = synth.chunk_case(21, B=2, Hkv=3, d=d, chunks=[100, 77, 32, 1], n_cur=5, dtype=dtype)
     tc, oc = uniform_pair(case, bits)
     assert_same_cache(tc, oc)
@@ -54,9 +56,10 @@ def test_rollout_workload_append_full():
     assert_same_cache(tc, oc)
 
 
-def test_degenerate_groups():
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f16", 128)])
+def test_degenerate_groups(dtype, d):
     """Constant groups (s = 0), signed zeros, and a 1-token chunk."""
-    case = synth.chunk_case(22, B=1, Hkv=2, d=64, chunks=[40, 1], n_cur=1, dtype="f32")
+    case = synth.chunk_case(22, B=1, Hkv=2, d=d, chunks=[40, 1], n_cur=1, dtype=dtype)
     K = case["K_cache"]
     K[:, 0, :32, 5] = 2.5                  # constant key channel group
     K[:, 1, :32, 7] = -0.0
