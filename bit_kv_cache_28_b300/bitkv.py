@@ -21,6 +21,7 @@ KV_F32, KV_F16, KV_BF16 = 0, 1, 2
 KV_UNIFORM2, KV_UNIFORM4, KV_MIXED, KV_CODEBOOK2 = 0, 1, 2, 3
 KV_SEG_RAW16, KV_SEG_INT4, KV_SEG_INT2 = 0, 1, 2
 KV_REGION_DATA, KV_REGION_BLK_LEN, KV_REGION_BLK_POS, KV_REGION_CENTROIDS, KV_REGION_PSAC_U = 0, 1, 2, 3, 4
+KV_REGION_RESID_VAR = 5
 KV_JENSEN_OFF, KV_JENSEN_TAYLOR2, KV_JENSEN_EXACT, KV_JENSEN_ISOTROPIC = 0, 1, 2, 3
 KV_PATH_AUTO, KV_PATH_SIMT, KV_PATH_TC, KV_PATH_DECODE = 0, 1, 2, 3
 
@@ -32,7 +33,8 @@ STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3:
 EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_append", "kv_attention_workspace",
            "kv_attention_plan", "kv_attention", "kv_attention_status", "kv_attention_noalloc",
            "kv_attention_noalloc_status", "kv_window_plan", "kv_window_similarity",
-           "kv_codebook_workspace", "kv_codebook_fit", "kv_psac_workspace",
+           "kv_codebook_workspace", "kv_codebook_fit", "kv_codebook_fit_range", "kv_codebook_residual_var",
+           "kv_psac_workspace",
            "kv_psac_basis", "kv_dequantize", "kv_debug_operands", "kv_last_error", "kv_version"]
 
 
@@ -45,7 +47,7 @@ class kv_layout(C.Structure):
 class kv_cache(C.Structure):
     _fields_ = [("layout", kv_layout), ("data", C.c_void_p), ("blk_len", C.c_void_p), ("blk_pos", C.c_void_p),
                 ("centroids", C.c_void_p), ("psac_u", C.c_void_p), ("n_blocks", C.c_int32 * 3),
-                ("n_tokens", C.c_int32)]
+                ("n_tokens", C.c_int32), ("resid_var", C.c_void_p)]
 
 
 class kv_append_opts(C.Structure):
@@ -95,6 +97,8 @@ def lib():
             "kv_window_similarity": (C.c_int, [P, P, I, I, I, I, I, I, P, P]),
             "kv_codebook_workspace": (S, [C.POINTER(kv_layout), I]),
             "kv_codebook_fit": (C.c_int, [P, I, I, C.POINTER(kv_cache), I, P, I, P, P, S, P]),
+            "kv_codebook_fit_range": (C.c_int, [P, I, I, C.POINTER(kv_cache), I, P, I, P, P]),
+            "kv_codebook_residual_var": (C.c_int, [P, I, I, C.POINTER(kv_cache), P]),
             "kv_psac_workspace": (S, [C.POINTER(kv_layout)]),
             "kv_psac_basis": (C.c_int, [P, I, I, C.POINTER(kv_cache), P, P, S, P]),
             "kv_dequantize": (C.c_int, [C.POINTER(kv_cache), P, P, P]),
@@ -220,6 +224,15 @@ def kv_codebook_fit(K, dtype, n_tokens, cache, iters=20, Qhist=None, n_hist=0, w
                                  _ptr(weights_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def kv_codebook_fit_range(K, dtype, n_tokens, cache, iters, Qhist, n_hist, weights_out, stream=None):
+    _check(lib().kv_codebook_fit_range(_ptr(K), dtype, n_tokens, C.byref(cache), iters, _ptr(Qhist), n_hist,
+                                       _ptr(weights_out), _stream(stream)))
+
+
+def kv_codebook_residual_var(K, dtype, n_tokens, cache, stream=None):
+    _check(lib().kv_codebook_residual_var(_ptr(K), dtype, n_tokens, C.byref(cache), _stream(stream)))
+
+
 def kv_psac_workspace(layout) -> int:
     return int(lib().kv_psac_workspace(C.byref(layout)))
 
@@ -256,7 +269,7 @@ def torch_dtype_code(t):
 class TorchCache:
     """A cache whose regions are torch tensors on one CUDA device (allocation only)."""
 
-    def __init__(self, B, Hkv, d, kind, cap_blocks, raw_dtype=KV_F16, psac_rank=0, device="cuda"):
+    def __init__(self, B, Hkv, d, kind, cap_blocks, raw_dtype=KV_F16, psac_rank=0, device="cuda", resid_var=False):
         import torch
         self.layout = kv_layout_init(B, Hkv, d, kind, raw_dtype, cap_blocks, psac_rank)
         nb = lambda r: kv_layout_bytes(self.layout, r)
@@ -268,6 +281,11 @@ class TorchCache:
         self.psac_u = (torch.zeros(nb(KV_REGION_PSAC_U) // 4, dtype=torch.float32, device=device)
                        if nb(KV_REGION_PSAC_U) else None)
         self.c = kv_cache_init(self.layout, self.data, self.blk_len, self.blk_pos, self.centroids, self.psac_u)
+        # CODEBOOK2: the keys' residual variances, which turn on their Jensen term
+        self.resid_var = None
+        if resid_var and nb(KV_REGION_RESID_VAR):
+            self.resid_var = torch.zeros(nb(KV_REGION_RESID_VAR) // 4, dtype=torch.float32, device=device)
+            self.c.resid_var = self.resid_var.data_ptr()
 
     @property
     def n_tokens(self):

@@ -39,7 +39,8 @@ size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits);
 int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq);
 bool tc_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const char** why);
 kv_status launch_codebook_fit(const void* K, kv_dtype dt, int n_tokens, const kv_cache* cache, int iters,
-                              const void* Qhist, int n_hist, float* weights_out, void* ws, cudaStream_t st);
+                              const void* Qhist, int n_hist, float* weights_out, int range, void* ws, cudaStream_t st);
+kv_status launch_residual_var(const void* K, kv_dtype dt, int n_tokens, const kv_cache* cache, cudaStream_t st);
 size_t codebook_ws_bytes(const kv_layout* L, int n_tokens);
 kv_status launch_psac_basis(const void* Qhist, kv_dtype dt, int n_hist, const kv_cache* cache, float* eig_out,
                             void* ws, cudaStream_t st);
@@ -122,6 +123,7 @@ DevCache make_dev_cache(const kv_cache* cc) {
     c.blk_pos = cc->blk_pos;
     c.centroids = cc->centroids;
     c.psac_u = cc->psac_u;
+    c.resid_var = cc->layout.kind == KV_CODEBOOK2 ? cc->resid_var : nullptr;
     c.B = L.B;
     c.Hkv = L.Hkv;
     c.d = L.d;
@@ -215,6 +217,8 @@ size_t kv_layout_bytes(const kv_layout* L, kv_region region) {
             return L->kind == KV_CODEBOOK2 ? (size_t)L->B * L->Hkv * L->d * 4 * sizeof(float) : 0;
         case KV_REGION_PSAC_U:
             return L->kind == KV_CODEBOOK2 ? (size_t)L->B * L->Hkv * L->d * L->psac_rank * sizeof(float) : 0;
+        case KV_REGION_RESID_VAR:
+            return L->kind == KV_CODEBOOK2 ? (size_t)L->B * L->Hkv * L->d * sizeof(float) : 0;
     }
     return 0;
 }
@@ -361,6 +365,8 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
     if (o->jensen < KV_JENSEN_OFF || o->jensen > KV_JENSEN_ISOTROPIC) return set_error(KV_ERR_INVALID_ARG, "bad jensen mode");
     if (o->psac && (L.kind != KV_CODEBOOK2 || L.psac_rank == 0 || !cache->psac_u))
         return set_error(KV_ERR_INVALID_ARG, "psac needs a CODEBOOK2 cache with psac_rank > 0 and a basis");
+    if (L.kind == KV_CODEBOOK2 && cache->resid_var && o->jensen == KV_JENSEN_EXACT)
+        return set_error(KV_ERR_UNSUPPORTED, "the EXACT Jensen form is not defined for codebook keys");
     const float tau = o->scale != 0.0f ? o->scale : 1.0f / sqrtf((float)L.d);
     const int path = pick_path(cache, dtype, n_q, Hq, o);
     const int sp = pick_splits(cache, path, n_q, n_cur, Hq, o);
@@ -454,8 +460,35 @@ kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache*
     const size_t need = codebook_ws_bytes(&cache->layout, n_tokens);
     if (need && (!workspace || ws_bytes < need))
         return set_error(KV_ERR_WORKSPACE, "codebook workspace of %zu bytes needed, %zu given", need, ws_bytes);
-    return launch_codebook_fit(K, dtype, n_tokens, cache, iters, Qhist, n_hist, weights_out, workspace,
+    return launch_codebook_fit(K, dtype, n_tokens, cache, iters, Qhist, n_hist, weights_out, 0, workspace,
                                static_cast<cudaStream_t>(stream));
+}
+
+kv_status kv_codebook_fit_range(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, int iters,
+                                const void* Qhist, int n_hist, float* weights_out, void* stream) {
+    AbiRange nvtx_range("kv_codebook_fit_range");
+    kv_status s = check_cache(cache);
+    if (s != KV_OK) return s;
+    if (cache->layout.kind != KV_CODEBOOK2) return set_error(KV_ERR_INVALID_ARG, "cache is not CODEBOOK2");
+    if (!K || !cache->centroids) return set_error(KV_ERR_INVALID_ARG, "K or centroids NULL");
+    if (n_tokens <= 0 || iters < 0) return set_error(KV_ERR_INVALID_ARG, "n_tokens must be > 0, iters >= 0");
+    if (!Qhist || n_hist <= 0 || !weights_out)
+        return set_error(KV_ERR_INVALID_ARG, "the residual-range fit needs Qhist, n_hist > 0 and weights_out");
+    if (dtype < KV_F32 || dtype > KV_BF16) return set_error(KV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    return launch_codebook_fit(K, dtype, n_tokens, cache, iters, Qhist, n_hist, weights_out, 1, nullptr,
+                               static_cast<cudaStream_t>(stream));
+}
+
+kv_status kv_codebook_residual_var(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, void* stream) {
+    AbiRange nvtx_range("kv_codebook_residual_var");
+    kv_status s = check_cache(cache);
+    if (s != KV_OK) return s;
+    if (cache->layout.kind != KV_CODEBOOK2) return set_error(KV_ERR_INVALID_ARG, "cache is not CODEBOOK2");
+    if (!K || !cache->centroids || !cache->resid_var)
+        return set_error(KV_ERR_INVALID_ARG, "K, centroids or resid_var NULL");
+    if (n_tokens <= 0) return set_error(KV_ERR_INVALID_ARG, "n_tokens must be > 0");
+    if (dtype < KV_F32 || dtype > KV_BF16) return set_error(KV_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    return launch_residual_var(K, dtype, n_tokens, cache, static_cast<cudaStream_t>(stream));
 }
 
 size_t kv_psac_workspace(const kv_layout* L) { return L ? psac_ws_bytes(L) : 0; }

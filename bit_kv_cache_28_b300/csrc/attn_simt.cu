@@ -83,6 +83,32 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
         }
     }
 
+    // codebook keys with residual variances: the row's Jensen term (tau^2/2) sum_c q'_c^2 v_c
+    // (ISOTROPIC: |q'|^2 mean_c v_c), q' = q - U (U^T q) with the PSAC term on, the same
+    // for every cached key; the 4 threads of a row split the channels
+    float cb_delta = 0.0f;
+    if (c.kind == KV_CODEBOOK2 && c.resid_var && jensen != KV_JENSEN_OFF) {
+        __syncthreads();                   // U^T q of the rows is in shared memory
+        const float* vv = c.resid_var + ((long long)b * c.Hkv + h) * D;
+        const float* U = r > 0 ? c.psac_u + ((long long)b * c.Hkv + h) * D * r : nullptr;
+        float acc = 0.0f, qn = 0.0f, vs = 0.0f;
+        for (int ch = part; ch < D; ch += 4) {
+            float qc = Qs[row * ld + ch];
+            for (int jj = 0; jj < r; ++jj) qc = fmaf(-U[ch * r + jj], Uq[row * r + jj], qc);
+            const float var = vv[ch];
+            acc = fmaf(qc * qc, var, acc);
+            qn = fmaf(qc, qc, qn);
+            vs += var;
+        }
+#pragma unroll
+        for (int m = 1; m < 4; m <<= 1) {
+            acc += __shfl_xor_sync(0xffffffffu, acc, m);
+            qn += __shfl_xor_sync(0xffffffffu, qn, m);
+            vs += __shfl_xor_sync(0xffffffffu, vs, m);
+        }
+        cb_delta = 0.5f * tau * tau * (jensen == KV_JENSEN_ISOTROPIC ? qn * (vs * (1.0f / D)) : acc);
+    }
+
     float m_run = -INFINITY, l_run = 0.0f;
     float o[D / 4];
 #pragma unroll
@@ -94,7 +120,7 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
 
     for (int u = u0; u < u1; ++u) {
         __syncthreads();
-        int len, quantised = 0, has_coeff = 0;
+        int len, quantised = 0, has_coeff = 0, codebook = 0;
         if (u < units_cache) {
             int seg = 0, i = u;
             while (i >= c.n_blocks[seg]) {
@@ -116,6 +142,7 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
                 const float2* km = reinterpret_cast<const float2*>(blk + int_offsets(D, cls == CLS_INT4 ? 4 : 2).km);
                 for (int ch = tid; ch < D; ch += kSimtThreads) Sk[ch] = km[ch].x;
             }
+            codebook = cls == CLS_CB2;
             if (cls == CLS_CB2 && r > 0) {
                 has_coeff = 1;
                 const __half* kq = reinterpret_cast<const __half*>(blk + cb_offsets(D).kq);
@@ -137,7 +164,7 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
         __syncthreads();
 
         // Jensen correction of this block for this row
-        float delta = 0.0f;
+        float delta = codebook ? cb_delta : 0.0f;
         if (quantised && jensen != KV_JENSEN_OFF) {
             float qn2 = 0.0f, ss2 = 0.0f;    // ISOTROPIC: |q|^2 and sum_c s_c^2
             for (int ch = part; ch < D; ch += 4) {

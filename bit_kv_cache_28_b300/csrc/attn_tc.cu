@@ -591,6 +591,10 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     __syncthreads();
     fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M::slot);
+    // codebook keys with residual variances: the Jensen term of this thread's query row,
+    // (tau^2/2) log2(e) sum_c q'_c^2 v_c (ISOTROPIC: |q'|^2 mean_c v_c), q' = q - U (U^T q)
+    // with the PSAC term on, the same for every cached key
+    float jrow = 0.0f;
     if (warp < kSoftWarps) {
         // Q row i -> TMEM lane i, columns kColQ .. kColQ + 63 (two fp16 per column: the
         // bf16 queries converted, exactly inside the fp16 range)
@@ -613,12 +617,14 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             tmem_st16(tmem + lane_addr + kColQ + 16 * hf, u);
         }
         if (qbad) atomicExch(err + 1, 1);
+        float uall[32];
         if (kCb && r16 > 0) {
             // u = U^T q of row i in fp32, split into fp16 high + low parts (u = hi + lo up
             // to 2^-22 |u|): the A operand of the PSAC MMAs, TMEM columns kColD + 8 ks
             // (high) and kColD + 16 + 8 ks (low) for the 16-wide rank chunk ks
-#pragma unroll 1
-            for (int ks = 0; ks < r16 / 16; ++ks) {
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                if (ks >= r16 / 16) break;
                 float u[16];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) u[jj] = 0.0f;
@@ -640,6 +646,10 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                         }
                     }
                 }
+                if (JENSEN != KV_JENSEN_OFF) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) uall[16 * ks + jj] = u[jj];
+                }
                 uint32_t uh[8], ul[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -650,6 +660,29 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 tmem_st8(tmem + lane_addr + kColD + 8 * ks, uh);
                 tmem_st8(tmem + lane_addr + kColD + 16 + 8 * ks, ul);
             }
+        }
+        if (kCb && JENSEN != KV_JENSEN_OFF) {
+            const float* vv = c.resid_var + ((long long)b * c.Hkv + h) * kD;
+            float acc = 0.0f, qn = 0.0f, vs = 0.0f;
+#pragma unroll 1
+            for (int c8 = 0; c8 < kD / 8; ++c8) {
+                const uint4 v = valid ? __ldg(Qg + (long long)(q0 + tid) * (kD / 8) + c8) : make_uint4(0, 0, 0, 0);
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int ch = 8 * c8 + k;
+                    float qc = __uint_as_float(k & 1 ? (wv[k >> 1] & 0xFFFF0000u) : (wv[k >> 1] << 16));
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (jj < r16) qc = fmaf(-Us[ch * r16 + jj], uall[jj], qc);
+                    const float var = __ldg(vv + ch);
+                    acc = fmaf(qc * qc, var, acc);
+                    qn = fmaf(qc, qc, qn);
+                    vs += var;
+                }
+            }
+            const float jc = 0.5f * tau * tau * kLog2e;
+            jrow = JENSEN == KV_JENSEN_ISOTROPIC ? jc * qn * (vs * (1.0f / kD)) : jc * acc;
         }
         tmem_wait_st();
     }
@@ -680,7 +713,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                                        kIdescPV, 1);
                     }
                 }
-                if (JENSEN == KV_JENSEN_TAYLOR2 && tile_of(j) < n_cache_tiles) {
+                if (!kCb && JENSEN == KV_JENSEN_TAYLOR2 && tile_of(j) < n_cache_tiles) {
                     const uint32_t sW = sbase + M::w + s * kWBytes;
 #pragma unroll
                     for (int kk = 0; kk < 2 * (kD / 16); ++kk) {
@@ -769,7 +802,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             // tile j - 3 was issued, which Q K^T of tile j - 1 waited for
             TileInfo& inf = infos[j & 3];
             if (p < 4) inf.nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
-            if (p == 0) inf.quantised = cached && !kCb ? 1 : 0;
+            if (p == 0) inf.quantised = cached ? 1 : 0;
             if (cached && kCb) {
                 fill_cb_keys(sm + M::k, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
                 if (r16 > 0) fill_coeff(sm + M::coef, stg, bb, nb, c.rp, r16 / 8, p);
@@ -861,7 +894,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (!__all_sync(0xffffffffu, ok1)) break;
             fence_after();
             float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (info.quantised) {
+            if (kCb) {
+                if (JENSEN != KV_JENSEN_OFF && info.quantised) dl[0] = dl[1] = dl[2] = dl[3] = jrow;
+            } else if (info.quantised) {
                 if (JENSEN == KV_JENSEN_TAYLOR2) {
                     float dv[8];
                     tmem_ld8(tmem + lane_addr + kColD + 16 * s, dv);
@@ -1204,10 +1239,18 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
                                                 lse, ws_o, ws_ml, err, st);                                   \
     }
     if (c.kind == KV_CODEBOOK2) {
-        // codebook keys carry no step sizes: no Jensen term
+        // codebook keys carry no step sizes: their Jensen term needs the residual variances
         const int r16 = psac ? (c.r + 15) / 16 * 16 : 0;
-        s = launch_tc_t<FMT_CB2, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32, lse,
-                                                ws_o, ws_ml, err, st);
+        const int jm = c.resid_var ? jensen : KV_JENSEN_OFF;
+        if (jm == KV_JENSEN_TAYLOR2)
+            s = launch_tc_t<FMT_CB2, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32,
+                                                        lse, ws_o, ws_ml, err, st);
+        else if (jm == KV_JENSEN_ISOTROPIC)
+            s = launch_tc_t<FMT_CB2, KV_JENSEN_ISOTROPIC>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out,
+                                                          out_f32, lse, ws_o, ws_ml, err, st);
+        else
+            s = launch_tc_t<FMT_CB2, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32,
+                                                    lse, ws_o, ws_ml, err, st);
     } else if (c.kind == KV_UNIFORM4) {
         BITKV_TC(FMT_INT4)
     } else {

@@ -11,6 +11,14 @@
 // Member sums of 16-bit inputs are exact in fp64 at these sizes, so the block
 // reduction order does not matter.
 //
+// QSAC with residual ranges (the pages: the clustering weighs the queries'
+// sensitivity together with the range of the residuals, protecting the channels
+// that matter more): given the weights, channel c of a (b, h) gets rho_c = w_c / max w
+// (fp64 of the fp32 weights) and each update moves the cluster's mean towards its
+// mid-range, mu_k = mean_k + rho_c (mid_k - mean_k), mid_k = (min_k + max_k) / 2,
+// every fp64 operation rounded once in that order (no contraction), so the centroids
+// match the oracle's bit for bit.  rho = 0 is Lloyd.
+//
 // "QuantWM" (Innovations 3): PSAC compensates the remaining key error along the
 // dominant subspace of the queries.  U = the top-r eigenvectors of the uncentred
 // second moment C = (1/n) sum_t q_t q_t^T of the historical queries, eigenvalues
@@ -46,16 +54,32 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     return v;
 }
 
-// One CTA per (channel, kv head, batch row).
+// One CTA per (channel, kv head, batch row).  w (nullable): the fp32 sensitivity
+// weights [B][Hkv][d] for the residual-range update; NULL for Lloyd.
 template <typename T>
 __global__ void __launch_bounds__(kCbThreads)
-codebook_fit_kernel(const T* __restrict__ K, int n, int npow2, int d, int Hkv, int iters, float* __restrict__ cent) {
+codebook_fit_kernel(const T* __restrict__ K, int n, int npow2, int d, int Hkv, int iters, const float* __restrict__ w,
+                    float* __restrict__ cent) {
     extern __shared__ float xs[];                   // [npow2] values, sorted in place
     __shared__ double s_sum[kCbThreads / 32][4];
     __shared__ int s_cnt[kCbThreads / 32][4];
+    __shared__ float s_mn[kCbThreads / 32][4], s_mx[kCbThreads / 32][4];
     __shared__ double s_mu[4];
+    __shared__ float s_wmax[kCbThreads / 32];
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    double rho = 0.0;
+    if (w) {
+        const float* wb = w + ((long long)b * Hkv + h) * d;
+        float m = 0.0f;
+        for (int e = tid; e < d; e += kCbThreads) m = fmaxf(m, wb[e]);
+        m = warp_max(m);
+        if (lane == 0) s_wmax[warp] = m;
+        __syncthreads();
+        float wm = 0.0f;
+        for (int q = 0; q < kCbThreads / 32; ++q) wm = fmaxf(wm, s_wmax[q]);
+        rho = wm > 0.0f ? (double)wb[c] / (double)wm : 0.0;
+    }
     const T* src = K + ((long long)b * Hkv + h) * n * d + c;
     for (int t = tid; t < npow2; t += kCbThreads) xs[t] = t < n ? load_f32(src + (long long)t * d) : INFINITY;
     __syncthreads();
@@ -82,8 +106,10 @@ codebook_fit_kernel(const T* __restrict__ K, int n, int npow2, int d, int Hkv, i
         const double mu0 = s_mu[0], mu1 = s_mu[1], mu2 = s_mu[2], mu3 = s_mu[3];
         double sum[4] = {0.0, 0.0, 0.0, 0.0};
         int cnt[4] = {0, 0, 0, 0};
+        float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         for (int t = tid; t < n; t += kCbThreads) {
-            const double x = xs[t];
+            const float xf = xs[t];
+            const double x = xf;
             double best = fabs(x - mu0);
             int k = 0;
             const double d1 = fabs(x - mu1), d2 = fabs(x - mu2), d3 = fabs(x - mu3);
@@ -95,28 +121,45 @@ codebook_fit_kernel(const T* __restrict__ K, int n, int npow2, int d, int Hkv, i
                 if (q == k) {
                     sum[q] += x;
                     cnt[q] += 1;
+                    mn[q] = fminf(mn[q], xf);
+                    mx[q] = fmaxf(mx[q], xf);
                 }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             sum[q] = warp_sum_d(sum[q]);
             cnt[q] = warp_sum_i(cnt[q]);
+            mn[q] = warp_min(mn[q]);
+            mx[q] = warp_max(mx[q]);
         }
         if (lane == 0)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 s_sum[warp][q] = sum[q];
                 s_cnt[warp][q] = cnt[q];
+                s_mn[warp][q] = mn[q];
+                s_mx[warp][q] = mx[q];
             }
         __syncthreads();
         if (tid < 4) {
             double sm = 0.0;
             int cn = 0;
-            for (int w = 0; w < kCbThreads / 32; ++w) {
-                sm += s_sum[w][tid];
-                cn += s_cnt[w][tid];
+            float lo = INFINITY, hi = -INFINITY;
+            for (int q = 0; q < kCbThreads / 32; ++q) {
+                sm += s_sum[q][tid];
+                cn += s_cnt[q][tid];
+                lo = fminf(lo, s_mn[q][tid]);
+                hi = fmaxf(hi, s_mx[q][tid]);
             }
-            if (cn > 0) s_mu[tid] = sm / (double)cn;
+            if (cn > 0) {
+                const double mean = sm / (double)cn;
+                if (w) {
+                    const double mid = __dmul_rn(__dadd_rn((double)lo, (double)hi), 0.5);
+                    s_mu[tid] = __dadd_rn(mean, __dmul_rn(rho, __dsub_rn(mid, mean)));
+                } else {
+                    s_mu[tid] = mean;
+                }
+            }
         }
         __syncthreads();
     }
@@ -137,6 +180,46 @@ __global__ void sensitivity_kernel(const T* __restrict__ Qh, int n_hist, int d, 
         acc += q * q;
     }
     w[i] = (float)(acc / (double)n_hist);
+}
+
+// Residual variance of codebook keys, v_c = (1/n) sum_t (x_t - mu_a(t))^2, with the
+// cache's fp32 centroids and the nearest index a(t) (fp64 distance, ties to the lower
+// index, as the append stores it), summed in fp64; one CTA per (channel, kv head, batch).
+template <typename T>
+__global__ void __launch_bounds__(kCbThreads)
+residual_var_kernel(const T* __restrict__ K, int n, int d, int Hkv, const float* __restrict__ cent,
+                    float* __restrict__ var) {
+    __shared__ double s_acc[kCbThreads / 32];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x;
+    const long long bh = (long long)b * Hkv + h;
+    const float4 m4 = *reinterpret_cast<const float4*>(cent + (bh * d + c) * 4);
+    const double mu[4] = {m4.x, m4.y, m4.z, m4.w};
+    const T* src = K + bh * n * d + c;
+    double acc = 0.0;
+    for (int t = tid; t < n; t += kCbThreads) {
+        const double x = load_f32(src + (long long)t * d);
+        int k = 0;
+        double best = fabs(x - mu[0]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+            const double dq = fabs(x - mu[q]);
+            if (dq < best) {
+                best = dq;
+                k = q;
+            }
+        }
+        const double e = x - mu[k];
+        acc += e * e;
+    }
+    acc = warp_sum_d(acc);
+    if ((tid & 31) == 0) s_acc[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+        double a = 0.0;
+        for (int q = 0; q < kCbThreads / 32; ++q) a += s_acc[q];
+        var[bh * d + c] = (float)(a / (double)n);
+    }
 }
 
 // C = (1/n) sum_t q_t q_t^T in fp64, one CTA per (b, h); C [d][d] into the workspace.
@@ -296,7 +379,7 @@ size_t codebook_ws_bytes(const kv_layout* L, int n_tokens) {
 }
 
 kv_status launch_codebook_fit(const void* K, kv_dtype dt, int n_tokens, const kv_cache* cache, int iters,
-                              const void* Qhist, int n_hist, float* weights_out, void* ws, cudaStream_t st) {
+                              const void* Qhist, int n_hist, float* weights_out, int range, void* ws, cudaStream_t st) {
     (void)ws;
     const kv_layout& L = cache->layout;
     if (n_tokens > kMaxCbTokens)
@@ -305,17 +388,19 @@ kv_status launch_codebook_fit(const void* K, kv_dtype dt, int n_tokens, const kv
     const int npow2 = pow2_at_least(n_tokens);
     const size_t smem = (size_t)npow2 * sizeof(float);
     dim3 grid(L.d, L.Hkv, L.B);
+    // the weights come first: the residual-range update reads them
 #define BITKV_CB(T)                                                                                          \
     do {                                                                                                     \
-        cudaFuncSetAttribute(codebook_fit_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        codebook_fit_kernel<T><<<grid, kCbThreads, smem, st>>>(static_cast<const T*>(K), n_tokens, npow2, L.d, \
-                                                               L.Hkv, iters, cache->centroids);             \
         if (Qhist) {                                                                                         \
             const long long total = (long long)L.B * L.Hkv * L.d;                                            \
             sensitivity_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(static_cast<const T*>(Qhist), \
                                                                                   n_hist, L.d, total,        \
                                                                                   weights_out);              \
         }                                                                                                    \
+        cudaFuncSetAttribute(codebook_fit_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        codebook_fit_kernel<T><<<grid, kCbThreads, smem, st>>>(static_cast<const T*>(K), n_tokens, npow2, L.d, \
+                                                               L.Hkv, iters, range ? weights_out : nullptr, \
+                                                               cache->centroids);                           \
     } while (0)
     switch (dt) {
         case KV_F32: BITKV_CB(float); break;
@@ -324,6 +409,27 @@ kv_status launch_codebook_fit(const void* K, kv_dtype dt, int n_tokens, const kv
     }
 #undef BITKV_CB
     return check_launch("codebook_fit_kernel");
+}
+
+kv_status launch_residual_var(const void* K, kv_dtype dt, int n_tokens, const kv_cache* cache, cudaStream_t st) {
+    const kv_layout& L = cache->layout;
+    dim3 grid(L.d, L.Hkv, L.B);
+    switch (dt) {
+        case KV_F32:
+            residual_var_kernel<float><<<grid, kCbThreads, 0, st>>>(static_cast<const float*>(K), n_tokens, L.d, L.Hkv,
+                                                                   cache->centroids, cache->resid_var);
+            break;
+        case KV_F16:
+            residual_var_kernel<__half><<<grid, kCbThreads, 0, st>>>(static_cast<const __half*>(K), n_tokens, L.d,
+                                                                    L.Hkv, cache->centroids, cache->resid_var);
+            break;
+        case KV_BF16:
+            residual_var_kernel<__nv_bfloat16><<<grid, kCbThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(K),
+                                                                           n_tokens, L.d, L.Hkv, cache->centroids,
+                                                                           cache->resid_var);
+            break;
+    }
+    return check_launch("residual_var_kernel");
 }
 
 size_t psac_ws_bytes(const kv_layout* L) {

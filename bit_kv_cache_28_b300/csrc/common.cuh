@@ -33,6 +33,7 @@ struct DevCache {
     int32_t* blk_pos;
     const float* centroids;
     const float* psac_u;
+    const float* resid_var;        // CODEBOOK2 residual variances [B][Hkv][d], or NULL
     int B, Hkv, d, kind, raw_dtype, r, rp;
     int cap_total;
     int seg_base[KV_NUM_SEG];      // index of a segment's first block in blk_len / blk_pos rows

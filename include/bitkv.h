@@ -67,7 +67,8 @@ typedef enum {
     KV_REGION_BLK_LEN = 1,   /* int32 [B][cap_total]: valid tokens per block */
     KV_REGION_BLK_POS = 2,   /* int32 [B][cap_total]: logical position of a block's first token */
     KV_REGION_CENTROIDS = 3, /* float [B][Hkv][d][4]: CODEBOOK2 key centroids */
-    KV_REGION_PSAC_U = 4     /* float [B][Hkv][d][r]: CODEBOOK2 PSAC basis (row-major d x r) */
+    KV_REGION_PSAC_U = 4,    /* float [B][Hkv][d][r]: CODEBOOK2 PSAC basis (row-major d x r) */
+    KV_REGION_RESID_VAR = 5  /* float [B][Hkv][d]: CODEBOOK2 per-channel key residual variances */
 } kv_region;
 
 /* Packed block format (32 token slots of one batch row and kv head).
@@ -100,7 +101,10 @@ typedef struct {
 
 /* A cache: the caller allocates every region (sizes from kv_layout_bytes),
  * zero-fills DATA, and keeps this struct on the host.  n_blocks / n_tokens
- * are host-side counters updated by kv_quantize_append. */
+ * are host-side counters updated by kv_quantize_append.  resid_var is optional
+ * and set by the caller after kv_cache_init: a CODEBOOK2 cache whose resid_var
+ * holds the keys' residual variances (kv_codebook_residual_var) applies the
+ * Jensen term to its codebook keys; with NULL they carry none. */
 typedef struct {
     kv_layout layout;
     void* data;          /* (device) */
@@ -110,6 +114,7 @@ typedef struct {
     float* psac_u;       /* (device) CODEBOOK2 with psac_rank > 0, else NULL */
     int32_t n_blocks[KV_NUM_SEG];
     int32_t n_tokens;
+    float* resid_var;    /* (device, nullable) CODEBOOK2: [B][Hkv][d] residual variances */
 } kv_cache;
 
 typedef struct {
@@ -184,8 +189,12 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
  * TAYLOR2 (tau^2/24) sum_c q_c^2 s_c^2, EXACT sum_c log(sinh x_c / x_c) with
  * x_c = tau q_c s_c / 2, ISOTROPIC (tau^2/24) |q|^2 mean_c s_c^2 (the query-norm
  * form; equal to TAYLOR2 when a group's steps are equal), using the step sizes
- * of the key's group; zero for
- * RAW16 windows and codebook keys.
+ * of the key's group; zero for RAW16 windows.  Codebook keys have no step size:
+ * with cache->resid_var set, the second-order term of their residuals applies,
+ * TAYLOR2 (tau^2/2) sum_c q'_c^2 v_c, ISOTROPIC (tau^2/2) |q'|^2 mean_c v_c, with
+ * q' = q - U (U^T q) when opts->psac is on (PSAC restores the error along U) and
+ * q' = q otherwise, one value per query row ([QWM] PSAC; [JB] second-order
+ * correction); EXACT is KV_ERR_UNSUPPORTED there; without resid_var, none.
  * Precision: the result is defined over the exact dequantised entries
  * fmaf(code, s, z) and the inputs as given.  The CUDA-core path (KV_PATH_SIMT)
  * computes that definition in fp32.  The decode path multiplies exact integer
@@ -297,6 +306,25 @@ kv_status kv_codebook_fit(const void* K, kv_dtype dtype, int n_tokens, kv_cache*
  * accumulated in fp64 and diagonalised by a cyclic Jacobi method in fp64 on
  * the device (d even, <= 128); workspace (device) >= kv_psac_workspace() =
  * 2 B Hkv d^2 doubles. */
+/* QSAC with residual ranges ([QWM] QSAC: the clustering weighs the historical
+ * queries' sensitivity together with the range of the residuals, protecting the
+ * channels that matter more).  As kv_codebook_fit, with Qhist and weights_out
+ * required: the weights w_c are computed first, channel c gets the relative
+ * sensitivity rho_c = w_c / max_c' w_c' of its (b, kv head) (fp64 of the fp32
+ * weights; 0 when all are 0), and every update moves a cluster's member mean
+ * towards its mid-range (min + max) / 2, mu_k = mean_k + rho_c (mid_k - mean_k), each
+ * fp64 operation rounded once in that order: rho = 0 is Lloyd, the most sensitive
+ * channel minimises its largest residual.  Centroids fp32 as kv_codebook_fit. */
+kv_status kv_codebook_fit_range(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, int iters,
+                                const void* Qhist, int n_hist, float* weights_out, void* stream);
+
+/* Residual variances of codebook keys, for the Jensen term of CODEBOOK2 caches:
+ * v_c = (1/n) sum_t (k_tc - mu_a)^2 over K (device) [B][Hkv][n_tokens][d] in dtype
+ * against the cache's fp32 centroids, a = the nearest centroid (fp64 distance,
+ * ties to the lower index, the index the append stores), summed in fp64 and
+ * stored as fp32 in cache->resid_var (which must be set).  Async on `stream`. */
+kv_status kv_codebook_residual_var(const void* K, kv_dtype dtype, int n_tokens, kv_cache* cache, void* stream);
+
 size_t kv_psac_workspace(const kv_layout* layout);
 kv_status kv_psac_basis(const void* Qhist, kv_dtype dtype, int n_hist, kv_cache* cache, float* eigvals_out,
                         void* workspace, size_t ws_bytes, void* stream);
