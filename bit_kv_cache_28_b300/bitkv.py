@@ -23,7 +23,7 @@ KV_SEG_RAW16, KV_SEG_INT4, KV_SEG_INT2 = 0, 1, 2
 KV_REGION_DATA, KV_REGION_BLK_LEN, KV_REGION_BLK_POS, KV_REGION_CENTROIDS, KV_REGION_PSAC_U = 0, 1, 2, 3, 4
 KV_REGION_RESID_VAR = 5
 KV_JENSEN_OFF, KV_JENSEN_TAYLOR2, KV_JENSEN_EXACT, KV_JENSEN_ISOTROPIC = 0, 1, 2, 3
-KV_PATH_AUTO, KV_PATH_SIMT, KV_PATH_TC, KV_PATH_DECODE = 0, 1, 2, 3
+KV_PATH_AUTO, KV_PATH_SIMT, KV_PATH_TC, KV_PATH_DECODE, KV_PATH_TC_SINGLE = 0, 1, 2, 3, 4
 
 STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_UNSUPPORTED", 3: "KV_ERR_CAPACITY",
                 4: "KV_ERR_WORKSPACE", 5: "KV_ERR_ALIGNMENT", 6: "KV_ERR_CUDA", 7: "KV_ERR_TIMEOUT",

@@ -34,7 +34,7 @@ int decode_auto_splits(const kv_cache* cache, int Hq);
 bool decode_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq);
 kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
                          const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out, int out_f32,
-                         float* lse, void* ws, cudaStream_t st);
+                         float* lse, void* ws, bool pair, cudaStream_t st);
 size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits);
 int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq);
 bool tc_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const char** why);
@@ -315,7 +315,7 @@ static int pick_path(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const 
 static int pick_splits(const kv_cache* cache, int path, int n_q, int n_cur, int Hq, const kv_attn_opts* o) {
     if (o && o->num_splits > 0) return o->num_splits;
     if (path == KV_PATH_DECODE) return decode_auto_splits(cache, Hq);
-    if (path == KV_PATH_TC) return tc_auto_splits(cache, n_q, n_cur, Hq);
+    if (path == KV_PATH_TC || path == KV_PATH_TC_SINGLE) return tc_auto_splits(cache, n_q, n_cur, Hq);
     // SIMT: enough CTAs to fill the GPU about twice
     const long long ctas = (long long)cache->layout.B * Hq * ((n_q + 31) / 32);
     const int units = simt_units_cache(cache) + (n_cur + 31) / 32;
@@ -329,7 +329,7 @@ size_t kv_attention_workspace(const kv_cache* cache, kv_dtype dt, int n_q, int n
     const int path = pick_path(cache, dt, n_q, Hq, opts);
     const int sp = pick_splits(cache, path, n_q, n_cur, Hq, opts);
     if (path == KV_PATH_DECODE) return decode_workspace(cache, Hq, sp);
-    if (path == KV_PATH_TC) return tc_workspace(cache, n_q, Hq, sp);
+    if (path == KV_PATH_TC || path == KV_PATH_TC_SINGLE) return tc_workspace(cache, n_q, Hq, sp);
     return simt_workspace(cache, n_q, Hq, sp);
 }
 
@@ -372,7 +372,7 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
     const int sp = pick_splits(cache, path, n_q, n_cur, Hq, o);
     size_t need = 0;
     if (path == KV_PATH_DECODE) need = decode_workspace(cache, Hq, sp);
-    else if (path == KV_PATH_TC) need = tc_workspace(cache, n_q, Hq, sp);
+    else if (path == KV_PATH_TC || path == KV_PATH_TC_SINGLE) need = tc_workspace(cache, n_q, Hq, sp);
     else need = simt_workspace(cache, n_q, Hq, sp);
     if (!workspace || ws_bytes < need)
         return set_error(KV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
@@ -392,12 +392,13 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
             r = launch_attn_decode(Q, Kcur, Vcur, dtype, n_cur, Hq, cache, tau, o->jensen, sp, out, o->out_f32, lse,
                                    workspace, st);
             break;
-        case KV_PATH_TC: {
+        case KV_PATH_TC:
+        case KV_PATH_TC_SINGLE: {
             const char* why = "";
             if (!tc_supported(cache, dtype, n_q, Hq, &why))
                 return set_error(KV_ERR_UNSUPPORTED, "tensor-core path: %s", why);
             r = launch_attn_tc(Q, Kcur, Vcur, n_q, n_cur, Hq, cache, tau, o->jensen, o->psac, sp, out, o->out_f32,
-                               lse, workspace, st);
+                               lse, workspace, path == KV_PATH_TC, st);
             break;
         }
         default:

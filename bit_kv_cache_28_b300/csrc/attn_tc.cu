@@ -33,8 +33,17 @@
 // TMEM columns: S double buffer 0-255 (a tile's P overwrites the first 64
 // columns of its S once they are read; Q K^T of the tile two later is issued
 // only after P V of this one has completed), O 256-383, Delta double buffer
-// 384-415, Q 448-511.  Every wait is bounded; every warp-collective tcgen05
-// load/store runs with the whole warp converged.
+// 384-415 (384-447 in a pair), Q 448-511.  Every wait is bounded; every
+// warp-collective tcgen05 load/store runs with the whole warp converged.
+//
+// CTA pairs (the default): two query tiles of one (batch, head, key-range split)
+// run in a 2-CTA cluster whose MMAs have M = 256 (tcgen05 cta_group::2).  Each CTA
+// keeps its own 128 rows of Q, S, P, O and the Jensen term, and holds half of
+// every B operand: keys 64 r .. 64 r + 63 of the K_hat tile and channels
+// 64 r .. 64 r + 63 of the V_hat^T tile (r = the CTA's rank), so each CTA expands
+// half of every packed tile -- the expansion per query row is halved.  The even
+// CTA issues the MMAs and commits to both CTAs' barriers; the odd CTA's MMA warp
+// forwards its K_FULL, V_FULL and P_FULL phases to the even CTA.
 //
 // Codebook caches ("QuantWM", Methodology: per-channel 4-centroid INT2 keys plus
 // the rank-r compensation q . U coeff in the logit): K_hat comes from a byte-permute
@@ -79,9 +88,22 @@ constexpr int kMmaWarp = kSoftWarps + kProdWarps;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColD = 384, kColQ = 448;
-constexpr uint32_t kIdescQK = idesc_f16(kM, kN);    // S = Q K_hat^T (fp16 operands)
-constexpr uint32_t kIdescJ = idesc_bf16(kM, 16);    // Delta = (q^2) W^T
-constexpr uint32_t kIdescPV = idesc_f16(kM, kD);    // O += P V_hat
+// Single CTA (M = 128) or CTA pair (cta_group::2, M = 256: each CTA's 128 query rows,
+// half of every B operand in each CTA: keys 64 r .. 64 r + 63 of K_hat, channels
+// 64 r .. 64 r + 63 of V_hat^T, r = the CTA's rank).  The pair's Jensen MMA has N = 32:
+// the even CTA holds the 16 weight rows (as a single CTA does), the odd CTA 16 zero rows,
+// and the term's TMEM stages are 32 columns apart (384-447, below Q at 448).
+template <bool PAIR> struct Geo {
+    static constexpr int kKBuf = PAIR ? 2 : 1;       // K_hat (and PSAC coefficient) buffers
+    static constexpr int kMM = PAIR ? 256 : 128;     // MMA M
+    static constexpr int kNK = PAIR ? 64 : 128;      // K_hat rows (keys) held by this CTA
+    static constexpr int kNV = PAIR ? 64 : 128;      // V_hat^T rows (channels) held by this CTA
+    static constexpr int kWR = 16;                   // Jensen weight rows held by this CTA
+    static constexpr int kJN = PAIR ? 32 : 16;       // Jensen MMA N; TMEM columns per stage
+    static constexpr uint32_t kIdescQK = idesc_f16(kMM, kN);   // S = Q K_hat^T (fp16 operands)
+    static constexpr uint32_t kIdescJ = idesc_bf16(kMM, kJN);  // Delta = (q^2) W^T
+    static constexpr uint32_t kIdescPV = idesc_f16(kMM, kD);   // O += P V_hat (and the PSAC term)
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -104,7 +126,7 @@ constexpr int kWBytes = 16 * kD * 2;        // 4 KB: 16 x 128 bf16 Jensen weight
 constexpr int kExactW = 4 * kD * 4;         // 2 KB: fp32 steps [4 blocks][128] (EXACT Jensen)
 constexpr int kCoefTile = kN * 128;         // 16 KB: 128 keys x 64 fp16 PSAC coefficients (swizzled)
 constexpr int kCentBytes = kD * 8;          // 1 KB: byte-planar bf16 centroid tables
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 25;
 
 struct TileInfo {
     int nvalid[4];
@@ -115,15 +137,19 @@ struct TileInfo {
 
 // Shared memory map (bytes from a 1024-aligned base).  INT formats: the bf16 high
 // and low parts of q^2 for the Jensen MMA; CB2: the PSAC coefficient tile and the
-// centroid tables instead.
-template <int FMT> struct Smem {
+// centroid tables instead.  In a CTA pair the K_hat, V_hat^T and coefficient tiles
+// hold this CTA's half.
+template <int FMT, bool PAIR> struct Smem {
     static constexpr bool cb = FMT == FMT_CB2;
+    static constexpr int kTileK = Geo<PAIR>::kNK * kD * 2;     // K_hat
+    static constexpr int kTileV = Geo<PAIR>::kNV * kN * 2;     // one V_hat^T stage
     static constexpr int q2h = 0;                               // bf16 high part of q^2
     static constexpr int q2l = q2h + (cb ? 0 : kTile);          // low part (q^2 = high + low exactly)
-    static constexpr int k = q2l + (cb ? 0 : kTile);            // K_hat, 1 buffer
-    static constexpr int coef = k + kTile;                      // CB2: PSAC coefficients, 1 buffer
-    static constexpr int v = coef + (cb ? kCoefTile : 0);       // V_hat^T, 2 stages
-    static constexpr int w = v + 2 * kTile;                     // Jensen weights, 2 stages
+    static constexpr int kTileC = Geo<PAIR>::kNK * 128;        // CB2: PSAC coefficients
+    static constexpr int k = q2l + (cb ? 0 : kTile);            // K_hat, kKBuf buffers
+    static constexpr int coef = k + Geo<PAIR>::kKBuf * kTileK;  // CB2: PSAC coefficients, kKBuf buffers
+    static constexpr int v = coef + (cb ? Geo<PAIR>::kKBuf * kTileC : 0);   // V_hat^T, 2 stages
+    static constexpr int w = v + 2 * kTileV;                    // Jensen weights, 2 stages
     static constexpr int cent = w + 2 * kWBytes;                // CB2: centroid tables
     static constexpr int stg = cent + (cb ? kCentBytes : 0);    // staged packed blocks, 2 slots
     static constexpr int stage = 4 * max_block_bytes<FMT>();
@@ -146,6 +172,12 @@ enum {
     BAR_V_FULL = 14,   // [2] producers -> MMA: V_hat[s] ready
     BAR_MMA_DONE = 16, // every MMA the issuer started has completed (O final; TMEM may be freed)
     BAR_NEVER = 17,    // never arrived on: the target of the injected stall (failure tests)
+    // CTA pair, in the even CTA: the odd CTA's K_FULL / V_FULL / P_FULL, forwarded by its
+    // MMA warp (the MMAs are issued from the even CTA and read both CTAs' halves)
+    BAR_PK_FULL = 18,  // [2]
+    BAR_PV_FULL = 20,  // [2]
+    BAR_PP_FULL = 22,  // [2]
+    BAR_K_EMPTY2 = 24, // CTA pair: Q K_hat^T of a tile in the second K_hat buffer completed
 };
 
 // Byte offset of 16-byte chunk `ch` of row `row` in a `rows`-row x 128-column
@@ -187,20 +219,25 @@ __device__ __forceinline__ void dequant2(float& v0, float& v1, float m0, float m
 }
 
 // ------------------------------------------------------------- producers ----
-// Values of a staged cache tile.  Warp pw expands value group g = pw & 3
-// (channels 32 g .. 32 g + 31, one per lane) of blocks 2 (pw >> 2) and
-// 2 (pw >> 2) + 1 into V_hat^T[stage] (fp16).  The group's per-token steps are
-// first pre-scaled in the staging copy by 2^(-b i), i = the token's slot in its
-// half word.
-template <int FMT>
+// Values of a staged cache tile into this CTA's V_hat^T rows (fp16; rows = channels,
+// K-major along the 128 keys).  Single CTA: warp pw expands value group g = pw & 3
+// (channels 32 g .. 32 g + 31, one per lane) of blocks 2 (pw >> 2) and 2 (pw >> 2) + 1.
+// CTA pair of rank r: channels 64 r .. 64 r + 63, warp pw takes group 2 r + (pw & 1) of
+// block pw >> 1.  The group's per-token steps are first pre-scaled in the staging copy
+// by 2^(-b i), i = the token's slot in its half word.
+template <int FMT, bool PAIR>
 __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned char* stg, int stride, int nb, int pw,
-                                                  int lane) {
+                                                  int lane, int rank) {
     constexpr int BITS = vbits<FMT>();
-    const int g = pw & 3, c = 32 * g + lane;
+    constexpr int kRows = Geo<PAIR>::kNV;
+    const int g = PAIR ? 2 * rank + (pw & 1) : (pw & 3), c = 32 * g + lane;
+    const int row = (PAIR ? 32 * (pw & 1) : 32 * g) + lane;          // this CTA's tile row
+    const int qb = PAIR ? (pw >> 1) : 2 * (pw >> 2);
+    constexpr int kNq = PAIR ? 1 : 2;
     constexpr int kSlots = 16 / BITS;    // tokens per half word
 #pragma unroll 1
-    for (int k2 = 0; k2 < 2; ++k2) {
-        const int q = 2 * (pw >> 2) + k2;
+    for (int k2 = 0; k2 < kNq; ++k2) {
+        const int q = qb + k2;
         if (q < nb) {
             unsigned char* blk = stg + q * stride;
             float* vm = reinterpret_cast<float*>(blk + voff_meta<FMT>()) + g * 64;
@@ -232,24 +269,45 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned ch
                 r.y = pack_f16(v[2], v[3]);
                 r.z = pack_f16(v[4], v[5]);
                 r.w = pack_f16(v[6], v[7]);
-                *reinterpret_cast<uint4*>(Vt + sw_off(c, 4 * q + k8)) = r;
+                *reinterpret_cast<uint4*>(Vt + sw_off(row, 4 * q + k8, kRows)) = r;
             }
         } else {
 #pragma unroll
-            for (int k8 = 0; k8 < 4; ++k8) *reinterpret_cast<uint4*>(Vt + sw_off(c, 4 * q + k8)) = make_uint4(0, 0, 0, 0);
+            for (int k8 = 0; k8 < 4; ++k8)
+                *reinterpret_cast<uint4*>(Vt + sw_off(row, 4 * q + k8, kRows)) = make_uint4(0, 0, 0, 0);
         }
     }
 }
 
-// Keys of a staged cache tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
-// 8 kg .. 8 kg + 7 (one block) into K_hat (fp16).
-template <int BITS>
-__device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigned char* stg, int nb, int p) {
+// Key rows of a staged cache tile: thread p expands channels 8 jc .. 8 jc + 7 (jc = p & 15)
+// of NR consecutive keys of one block into K_hat (fp16).  Single CTA: 8 keys per thread,
+// the tile's 128 keys; CTA pair of rank r: 4 keys per thread, keys 64 r .. 64 r + 63
+// (blocks 2 r and 2 r + 1).  *q, *t0, *row0: the block, its first token, the tile row.
+template <bool PAIR>
+__device__ __forceinline__ void key_rows(int p, int rank, int* q, int* t0, int* row0) {
+    if (PAIR) {
+        const int kg = (p >> 4) & 7, rh = p >> 7, ql = kg >> 2;
+        *q = 2 * rank + ql;
+        *t0 = 8 * (kg & 3) + 4 * rh;
+        *row0 = 32 * ql + *t0;
+    } else {
+        const int kg = p >> 4;
+        *q = kg >> 2;
+        *t0 = 8 * (kg & 3);
+        *row0 = 32 * *q + *t0;
+    }
+}
+
+template <int BITS, bool PAIR>
+__device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigned char* stg, int nb, int p, int rank) {
+    constexpr int NR = PAIR ? 4 : 8, kRows = Geo<PAIR>::kNK;
     const IntBlockOffsets o = int_offsets(kD, BITS);
-    const int jc = p & 15, kg = p >> 4, q = kg >> 2, t0 = 8 * (kg & 3);
+    const int jc = p & 15;
+    int q, t0, row0;
+    key_rows<PAIR>(p, rank, &q, &t0, &row0);
     if (q >= nb) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(8 * kg + r, jc)) = make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < NR; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = make_uint4(0, 0, 0, 0);
         return;
     }
     const unsigned char* blk = stg + q * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>();
@@ -269,7 +327,7 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigne
     constexpr int KW = kD * BITS / 32;   // code words per key
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < NR; ++r) {
         const int t = t0 + r;
         float v[8];
         if (BITS == 2) {
@@ -291,7 +349,7 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigne
         rr.y = pack_f16(v[2], v[3]);
         rr.z = pack_f16(v[4], v[5]);
         rr.w = pack_f16(v[6], v[7]);
-        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t, jc)) = rr;
+        *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = rr;
     }
 }
 
@@ -312,18 +370,21 @@ __device__ __forceinline__ bool fill_centroid_tables(uint32_t* tab, const float*
     return ok;
 }
 
-// Keys of a staged codebook tile: thread p expands channels 8 jc .. 8 jc + 7 of keys
-// 8 kg .. 8 kg + 7 (one block) into K_hat (fp16) by looking the 2-bit centroid
-// indices up in its channels' tables, two keys at a time.  For the channel pair
-// (2 i, 2 i + 1) the four index bits n = k0 + 4 k1 of a key become the selector
-// bytes (17 k0 + 0x40, 17 k1 + 0x40), i.e. nibbles (k0, 4 + k0, k1, 4 + k1):
+// Keys of a staged codebook tile (the rows of fill_cache_keys) into K_hat (fp16) by
+// looking the 2-bit centroid indices up in the channels' tables, two keys at a time.
+// For the channel pair (2 i, 2 i + 1) the four index bits n = k0 + 4 k1 of a key become
+// the selector bytes (17 k0 + 0x40, 17 k1 + 0x40), i.e. nibbles (k0, 4 + k0, k1, 4 + k1):
 // 17 n + 1071 (n & 12) + 0x4040 = 17 k0 + 4352 k1 + 0x4040.
+template <bool PAIR>
 __device__ __forceinline__ void fill_cb_keys(unsigned char* Kt, const unsigned char* stg, int stride, int nb,
-                                             const uint32_t* tab, int p) {
-    const int jc = p & 15, kg = p >> 4, q = kg >> 2, t0 = 8 * (kg & 3);
+                                             const uint32_t* tab, int p, int rank) {
+    constexpr int NR = PAIR ? 4 : 8, kRows = Geo<PAIR>::kNK;
+    const int jc = p & 15;
+    int q, t0, row0;
+    key_rows<PAIR>(p, rank, &q, &t0, &row0);
     if (q >= nb) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(8 * kg + r, jc)) = make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < NR; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = make_uint4(0, 0, 0, 0);
         return;
     }
     uint32_t lo[8], hi[8];
@@ -339,7 +400,7 @@ __device__ __forceinline__ void fill_cb_keys(unsigned char* Kt, const unsigned c
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(stg + q * stride);
     const uint32_t half = (jc & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
-    for (int r = 0; r < 8; r += 2) {
+    for (int r = 0; r < NR; r += 2) {
         const int t = t0 + r;
         // key t's 8 indices in the low half, key t + 1's in the high half
         const uint32_t x = __byte_perm(kc[t * KW + (jc >> 1)], kc[(t + 1) * KW + (jc >> 1)], half);
@@ -354,33 +415,36 @@ __device__ __forceinline__ void fill_cb_keys(unsigned char* Kt, const unsigned c
             o1[i] = __byte_perm(__byte_perm(lo[2 * i], hi[2 * i], sel1),
                                 __byte_perm(lo[2 * i + 1], hi[2 * i + 1], sel1), 0x7610);
         }
-        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t, jc)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-        *reinterpret_cast<uint4*>(Kt + sw_off(32 * q + t + 1, jc)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+        *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r + 1, jc, kRows)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
     }
 }
 
 // PSAC coefficients of a staged codebook tile -> the K-major swizzled B operand
-// [128 keys x nch 8-element chunks] (fp16); chunks at or beyond the stored rp and
-// rows of missing blocks are zero.
+// [this CTA's keys x nch 8-element chunks] (fp16); chunks at or beyond the stored rp
+// and rows of missing blocks are zero.
+template <bool PAIR>
 __device__ __forceinline__ void fill_coeff(unsigned char* Ct, const unsigned char* stg, int stride, int nb, int rp,
-                                           int nch, int p) {
-    for (int e = p; e < kN * nch; e += kProd) {
-        const int row = e / nch, ch = e - (e / nch) * nch, q = row >> 5, t = row & 31;
+                                           int nch, int p, int rank) {
+    constexpr int kRows = Geo<PAIR>::kNK;
+    const int qbase = PAIR ? 2 * rank : 0;
+    for (int e = p; e < kRows * nch; e += kProd) {
+        const int row = e / nch, ch = e - (e / nch) * nch, q = qbase + (row >> 5), t = row & 31;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (q < nb && 8 * ch < rp)
             v = *reinterpret_cast<const uint4*>(stg + q * stride + kCbCoeffOff + (t * rp + 8 * ch) * 2);
-        *reinterpret_cast<uint4*>(Ct + sw_off(row, ch)) = v;
+        *reinterpret_cast<uint4*>(Ct + sw_off(row, ch, kRows)) = v;
     }
 }
 
-// Jensen weights of a staged tile.  TAYLOR2: W rows g and 4 + g hold the bf16
-// high and low parts of w_c = s_c^2 tau^2 / 24 log2(e) of block g (zero for
-// missing blocks); rows 8-15 stay zero.  EXACT: the block steps s_c as fp32 [4][128].
+// Jensen weights of a staged tile.  TAYLOR2: W rows g and 4 + g hold the bf16 high and
+// low parts of w_c = s_c^2 tau^2 / 24 log2(e) of block g (zero for missing blocks); the
+// other rows stay zero (`wrows` rows in the tile).  EXACT: the block steps s_c as fp32 [4][128].
 // ISOTROPIC: the two warps of block g each sum s_c^2 over their 64 channels into
 // ss2[g][w] (the softmax adds the two in a fixed order).
 template <int BITS, int JENSEN>
 __device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned char* stg, int nb, int p, float coef,
-                                             float (*ss2)[2] = nullptr) {
+                                             int wrows, float (*ss2)[2] = nullptr) {
     const IntBlockOffsets o = int_offsets(kD, BITS);
     const int g = p >> 6, c = 2 * (p & 63);
     float2 s = make_float2(0.0f, 0.0f);
@@ -395,8 +459,8 @@ __device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned ch
         const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
         const uint32_t lo = pack_bf16(w0 - h0, w1 - h1);
         const int cb = (c & 7) * 2;
-        *reinterpret_cast<uint32_t*>(W + sw_off(g, c >> 3, 16) + cb) = hi;
-        *reinterpret_cast<uint32_t*>(W + sw_off(4 + g, c >> 3, 16) + cb) = lo;
+        *reinterpret_cast<uint32_t*>(W + sw_off(g, c >> 3, wrows) + cb) = hi;
+        *reinterpret_cast<uint32_t*>(W + sw_off(4 + g, c >> 3, wrows) + cb) = lo;
     } else if (JENSEN == KV_JENSEN_EXACT) {
         reinterpret_cast<float2*>(W)[(g * kD + c) >> 1] = s;
     } else if (JENSEN == KV_JENSEN_ISOTROPIC) {
@@ -405,17 +469,22 @@ __device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned ch
     }
 }
 
-// Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T.
-// Thread p transposes the 8 x 8 block (keys 8 (p >> 4) .., channels 8 (p & 15) ..).
+// Current-chunk tile (unquantised bf16): values transposed to fp16 V_hat^T rows.  Each
+// thread transposes one 8 x 8 block (keys 8 kc8 .., channels 8 cch ..): single CTA all
+// 128 channels (16 chunks); pair of rank r its 64 (8 chunks, threads 0-127).
+template <bool PAIR>
 __device__ __forceinline__ void fill_current_values(unsigned char* Vt, const __nv_bfloat16* Vcur, long long row0,
-                                                    int valid, int p) {
+                                                    int valid, int p, int rank) {
+    constexpr int kRows = Geo<PAIR>::kNV;
+    if (PAIR && p >= 128) return;
     const uint4* Vg = reinterpret_cast<const uint4*>(Vcur + row0 * kD);
-    const int kc8 = p >> 4, cch = p & 15;
+    const int kc8 = PAIR ? (p >> 3) : (p >> 4), cch = PAIR ? (p & 7) : (p & 15);
+    const int gch = PAIR ? 8 * rank + cch : cch;     // the 16-byte chunk of the key row
     uint32_t x[8][4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int key = 8 * kc8 + k;
-        const uint4 v = key < valid ? __ldg(Vg + key * (kD / 8) + cch) : make_uint4(0, 0, 0, 0);
+        const uint4 v = key < valid ? __ldg(Vg + key * (kD / 8) + gch) : make_uint4(0, 0, 0, 0);
         x[k][0] = v.x;
         x[k][1] = v.y;
         x[k][2] = v.z;
@@ -423,7 +492,7 @@ __device__ __forceinline__ void fill_current_values(unsigned char* Vt, const __n
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        // channel 8 cch + i: element i of every key row (word i / 2, half i & 1)
+        // channel 8 gch + i: element i of every key row (word i / 2, half i & 1)
         const int wi = i >> 1, hf = i & 1;
         float f[8];
 #pragma unroll
@@ -433,28 +502,30 @@ __device__ __forceinline__ void fill_current_values(unsigned char* Vt, const __n
         y.y = pack_f16(f[2], f[3]);
         y.z = pack_f16(f[4], f[5]);
         y.w = pack_f16(f[6], f[7]);
-        *reinterpret_cast<uint4*>(Vt + sw_off(8 * cch + i, kc8)) = y;
+        *reinterpret_cast<uint4*>(Vt + sw_off(8 * cch + i, kc8, kRows)) = y;
     }
 }
 
-// Current-chunk keys: bf16 rows converted to fp16 into the swizzled K_hat buffer.
-// Returns false if a key's fp16 rounding is not finite.
+// Current-chunk keys: bf16 rows converted to fp16 into the swizzled K_hat buffer (pair of
+// rank r: keys 64 r .. 64 r + 63).  Returns false if a key's fp16 rounding is not finite.
+template <bool PAIR>
 __device__ __forceinline__ bool fill_current_keys(unsigned char* Kt, const __nv_bfloat16* Kcur, long long row0,
-                                                  int valid, int p) {
-    const int jc = p & 15, r0 = p >> 4;
+                                                  int valid, int p, int rank) {
+    constexpr int kRows = Geo<PAIR>::kNK, NI = kRows / 16;
+    const int jc = p & 15, r0 = p >> 4, kb = PAIR ? 64 * rank : 0;
     const uint4* Kg = reinterpret_cast<const uint4*>(Kcur + row0 * kD);
-    uint4 kv[8];
+    uint4 kv[NI];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = r0 + 16 * i;
-        kv[i] = row < valid ? __ldg(Kg + row * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < NI; ++i) {
+        const int key = kb + r0 + 16 * i;
+        kv[i] = key < valid ? __ldg(Kg + key * (kD / 8) + jc) : make_uint4(0, 0, 0, 0);
     }
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NI; ++i) {
         const uint4 h = make_uint4(bf2_to_h2(kv[i].x), bf2_to_h2(kv[i].y), bf2_to_h2(kv[i].z), bf2_to_h2(kv[i].w));
         bad |= h2_nonfinite(h.x) | h2_nonfinite(h.y) | h2_nonfinite(h.z) | h2_nonfinite(h.w);
-        *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 16 * i, jc)) = h;
+        *reinterpret_cast<uint4*>(Kt + sw_off(r0 + 16 * i, jc, kRows)) = h;
     }
     return !bad;
 }
@@ -474,13 +545,14 @@ __device__ __forceinline__ bool cache_keys_in_f16_range(const unsigned char* stg
 }
 
 // --------------------------------------------------------------- kernel -----
-template <int FMT, int JENSEN>
+template <int FMT, int JENSEN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kcur,
                const __nv_bfloat16* __restrict__ Vcur, int n_q, int n_cur, int Hq, DevCache c, float tau, int r16,
                int n_splits, void* __restrict__ out, int out_f32, float* __restrict__ lse, float* __restrict__ ws_o,
                float2* __restrict__ ws_ml, int* __restrict__ err, int stall) {
-    using M = Smem<FMT>;
+    using M = Smem<FMT, PAIR>;
+    using G = Geo<PAIR>;
     constexpr bool kCb = FMT == FMT_CB2;
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
@@ -489,7 +561,12 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_qt = (n_q + kM - 1) / kM;
-    const int qt = blockIdx.x % n_qt, split = blockIdx.x / n_qt;
+    // a CTA pair takes two query tiles of one (batch, head, split); with an odd tile count
+    // the last pair's odd CTA has no valid row and only contributes its operand halves
+    const int rank = PAIR ? (int)cluster_rank() : 0;
+    const int n_qp = (n_qt + 1) / 2;
+    const int qt = PAIR ? 2 * ((blockIdx.x >> 1) % n_qp) + rank : blockIdx.x % n_qt;
+    const int split = PAIR ? (int)(blockIdx.x >> 1) / n_qp : blockIdx.x / n_qt;
     const int hq = blockIdx.y, b = blockIdx.z;
     const int h = hq / (Hq / c.Hkv);
     const int q0 = qt * kM;
@@ -541,17 +618,21 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         mbar_init(bar(BAR_STG_FULL + 1), 1);
         mbar_init(bar(BAR_STG_EMPTY + 0), kProd);
         mbar_init(bar(BAR_STG_EMPTY + 1), kProd);
+        for (int i = 0; i < 7; ++i) mbar_init(bar(BAR_PK_FULL + i), 1);   // PK, PV, PP, K_EMPTY2
         mbar_fence_init();
         // the first two cache tiles' copies start now, under the prologue
         stage_copy(0);
         stage_copy(1);
     }
-    if (warp == kMmaWarp) tmem_alloc(sbase + M::slot, kTmemCols);
+    if (warp == kMmaWarp) {
+        if (PAIR) tmem_alloc2(sbase + M::slot, kTmemCols);
+        else tmem_alloc(sbase + M::slot, kTmemCols);
+    }
 
     const uint4* Qg = reinterpret_cast<const uint4*>(Q + (((long long)b * Hq + hq) * n_q) * kD);
     // PSAC basis U of this head, zero-padded to [d][r16] fp32, staged in the second
     // V_hat stage (written by the producers only after the second barrier below)
-    float* Us = reinterpret_cast<float*>(sm + M::v + kTile);
+    float* Us = reinterpret_cast<float*>(sm + M::v + M::kTileV);
     if (kCb) {
         if (!fill_centroid_tables(reinterpret_cast<uint32_t*>(sm + M::cent),
                                   c.centroids + ((long long)b * c.Hkv + h) * kD * 4, tid))
@@ -589,6 +670,8 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     fence_proxy_async();
     fence_before();
     __syncthreads();
+    // a pair's barriers are initialised in both CTAs before either signals the other
+    if (PAIR) cluster_sync();
     fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M::slot);
     // codebook keys with residual variances: the Jensen term of this thread's query row,
@@ -692,25 +775,33 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
 
     if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             const uint32_t sQ2h = sbase + M::q2h, sQ2l = sbase + M::q2l, sK = sbase + M::k;
+            auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t bd, uint32_t id, uint32_t acc) {
+                if (PAIR) mma_f16kind_ts2(d, a, bd, id, acc);
+                else mma_f16kind_ts(d, a, bd, id, acc);
+            };
+            auto commit = [&](uint32_t bq) {
+                if (PAIR) mma_commit2(bq);
+                else mma_commit(bq);
+            };
             auto issue_qk = [&](int j) {
                 const int s = j & 1;
+                const uint32_t sKb = sK + (PAIR ? s * M::kTileK : 0);
                 fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-                    mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColQ + 8 * kk, desc_sw128(sK + off), kIdescQK, kk > 0);
+                    const uint32_t off = (kk >> 2) * (G::kNK * 128) + (kk & 3) * 32;
+                    mma_ts(tmem + kColS + s * kN, tmem + kColQ + 8 * kk, desc_sw128(sKb + off), G::kIdescQK, kk > 0);
                 }
                 if (kCb && r16 > 0 && tile_of(j) < n_cache_tiles) {
                     // S += (U^T q) coeff^T: fp16, K = the rank padded to 16, high and low
                     // parts of U^T q against the same coefficients
-                    const uint32_t sC = sbase + M::coef;
+                    const uint32_t sC = sbase + M::coef + (PAIR ? s * M::kTileC : 0);
                     for (int ks = 0; ks < r16 / 16; ++ks) {
-                        mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColD + 8 * ks, desc_sw128(sC + 32 * ks),
-                                       kIdescPV, 1);
-                        mma_f16kind_ts(tmem + kColS + s * kN, tmem + kColD + 16 + 8 * ks, desc_sw128(sC + 32 * ks),
-                                       kIdescPV, 1);
+                        mma_ts(tmem + kColS + s * kN, tmem + kColD + 8 * ks, desc_sw128(sC + 32 * ks), G::kIdescPV, 1);
+                        mma_ts(tmem + kColS + s * kN, tmem + kColD + 16 + 8 * ks, desc_sw128(sC + 32 * ks), G::kIdescPV,
+                               1);
                     }
                 }
                 if (!kCb && JENSEN == KV_JENSEN_TAYLOR2 && tile_of(j) < n_cache_tiles) {
@@ -719,25 +810,30 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     for (int kk = 0; kk < 2 * (kD / 16); ++kk) {
                         const int k = kk & 7;
                         const uint32_t offa = (k >> 2) * (kM * 128) + (k & 3) * 32;
-                        const uint32_t offb = (k >> 2) * (16 * 128) + (k & 3) * 32;
-                        mma_f16kind(tmem + kColD + 16 * s, desc_sw128((kk < 8 ? sQ2h : sQ2l) + offa),
-                                    desc_sw128(sW + offb), kIdescJ, kk > 0);
+                        const uint32_t offb = (k >> 2) * (G::kWR * 128) + (k & 3) * 32;
+                        const uint64_t ad = desc_sw128((kk < 8 ? sQ2h : sQ2l) + offa), bd = desc_sw128(sW + offb);
+                        if (PAIR) mma_f16kind2(tmem + kColD + G::kJN * s, ad, bd, G::kIdescJ, kk > 0);
+                        else mma_f16kind(tmem + kColD + G::kJN * s, ad, bd, G::kIdescJ, kk > 0);
                     }
                 }
-                mma_commit(bar(BAR_S_FULL + s));
-                mma_commit(bar(BAR_K_EMPTY));
+                commit(bar(BAR_S_FULL + s));
+                commit(bar(PAIR && s ? BAR_K_EMPTY2 : BAR_K_EMPTY));
             };
             auto issue_pv = [&](int jj) {
                 fence_after();
-                const uint32_t sV = sbase + M::v + (jj & 1) * kTile;
+                const uint32_t sV = sbase + M::v + (jj & 1) * M::kTileV;
 #pragma unroll
                 for (int kk = 0; kk < kN / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-                    mma_f16kind_ts(tmem + kColO, tmem + kColS + (jj & 1) * kN + 8 * kk, desc_sw128(sV + off), kIdescPV,
-                                   (jj > 0 || kk > 0));
+                    const uint32_t off = (kk >> 2) * (G::kNV * 128) + (kk & 3) * 32;
+                    mma_ts(tmem + kColO, tmem + kColS + (jj & 1) * kN + 8 * kk, desc_sw128(sV + off), G::kIdescPV,
+                           (jj > 0 || kk > 0));
                 }
-                mma_commit(bar(BAR_O_DONE));
-                mma_commit(bar(BAR_V_EMPTY + (jj & 1)));
+                commit(bar(BAR_O_DONE));
+                commit(bar(BAR_V_EMPTY + (jj & 1)));
+            };
+            // the odd CTA's halves, forwarded by its MMA warp (a pair only)
+            auto peer = [&](int base, int j) {
+                return !PAIR || mbar_test_wait_cluster(bar(base + (j & 1)), (j >> 1) & 1);
             };
             // Issue Q K^T of tile j as soon as its operands are staged and P V of
             // tile i as soon as its P is written, whichever is ready first (P V of a
@@ -745,17 +841,20 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             // writes the S columns that P V of tile j - 2 reads its P from.  MMAs into
             // different accumulators are not ordered with one another, so Q K^T of
             // tile j waits until P V of tile j - 2 has completed (its V stage's empty
-            // barrier, which nothing else can have advanced past it yet).  The wait is
+            // barrier, which nothing else can have advanced past it yet); that wait also
+            // keeps Q K^T at most one tile ahead of the P V issued so far.  The wait is
             // bounded: no progress for ~2^30 cycles gives up.
             int nq = 0, np = 0;
             long long t_prog = clock64();
             while (np < T) {
                 bool progressed = false;
                 if (np < nq && mbar_test_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1) &&
-                    mbar_test_wait(bar(BAR_V_FULL + (np & 1)), (np >> 1) & 1)) {
+                    mbar_test_wait(bar(BAR_V_FULL + (np & 1)), (np >> 1) & 1) && peer(BAR_PP_FULL, np) &&
+                    peer(BAR_PV_FULL, np)) {
                     issue_pv(np++);
                     progressed = true;
                 } else if (nq < T && nq <= np + 1 && mbar_test_wait(bar(BAR_K_FULL + (nq & 1)), (nq >> 1) & 1) &&
+                           peer(BAR_PK_FULL, nq) &&
                            (nq < 2 || mbar_test_wait(bar(BAR_V_EMPTY + (nq & 1)), ((nq - 2) >> 1) & 1))) {
                     issue_qk(nq++);
                     progressed = true;
@@ -771,9 +870,34 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 }
             }
             // every MMA issued so far completes before TMEM is freed (also after an abort)
-            mma_commit(bar(BAR_MMA_DONE));
+            commit(bar(BAR_MMA_DONE));
             const long long t_done = clock64();
             while (!mbar_try_wait(bar(BAR_MMA_DONE), 0) && clock64() - t_done < 100000000LL) {
+            }
+        } else if (PAIR && rank == 1 && lane < 3) {
+            // the odd CTA of a pair: lanes 0, 1 and 2 forward this CTA's K_FULL, V_FULL and
+            // P_FULL phases to the even CTA, whose MMAs read this CTA's halves; one lane per
+            // barrier, so that a forward waits for no other (a cluster-scope release arrive
+            // takes long).  No phase can run two ahead of its forwarding: K_FULL of tile
+            // j + 2 needs this CTA's P_FULL of tile j, V_FULL of j + 2 the completion of
+            // P V of j, P_FULL of j + 2 the Q K^T of j + 2, each issued only after tile j's
+            // phase was forwarded.
+            const int lb = lane == 0 ? BAR_K_FULL : (lane == 1 ? BAR_V_FULL : BAR_P_FULL);
+            const int rb = lane == 0 ? BAR_PK_FULL : (lane == 1 ? BAR_PV_FULL : BAR_PP_FULL);
+            int f = 0;
+            long long t_prog = clock64();
+            while (f < T) {
+                if (mbar_test_wait(bar(lb + (f & 1)), (f >> 1) & 1)) {
+                    mbar_arrive_remote(bar(rb + (f & 1)), 0);
+                    ++f;
+                    t_prog = clock64();
+                } else if (abort_flag) {
+                    break;
+                } else if (clock64() - t_prog > 1000000000LL) {
+                    abort_flag = 1;
+                    atomicExch(err, 3);
+                    break;
+                }
             }
         }
         __syncwarp();
@@ -787,11 +911,20 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             const int s = j & 1;
             const int tile = tile_of(j);
             const bool cached = tile < n_cache_tiles;
-            // keys first: the single K_hat buffer (and W[s], the PSAC coefficients) is
-            // free once Q K_hat^T of tile j - 1 completed
+            // keys first: a single K_hat buffer (and W[s], the PSAC coefficients) is free
+            // once Q K_hat^T of tile j - 1 completed; with two (a CTA pair), buffer j & 1
+            // once Q K_hat^T of tile j - 2 completed, signalled on that buffer's own barrier
+            // (one barrier for both could not express tile j - 2 once j - 1 completed too)
             bool ok = true;
             if (cached) ok = mbar_wait(bar(BAR_STG_FULL + s), (j >> 1) & 1, &abort_flag, err, 9);
-            if (ok && j > 0) ok = mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
+            if (PAIR) {
+                if (ok && j >= 2)
+                    ok = mbar_wait(bar(s ? BAR_K_EMPTY2 : BAR_K_EMPTY), ((j - 2) >> 1) & 1, &abort_flag, err, 8);
+            } else if (ok && j > 0) {
+                ok = mbar_wait(bar(BAR_K_EMPTY), (j - 1) & 1, &abort_flag, err, 8);
+            }
+            unsigned char* Kt = sm + M::k + (PAIR ? s * M::kTileK : 0);
+            unsigned char* Ct = sm + M::coef + (PAIR ? s * M::kTileC : 0);
             if (!__all_sync(0xffffffffu, ok)) break;
             unsigned char* stg = sm + M::stg + s * M::stage;
             const int nb = cached ? min(4, nblk - tile * 4) : 0;
@@ -804,22 +937,24 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             if (p < 4) inf.nvalid[p] = cached ? (p < nb ? stg_len[s * 4 + p] : 0) : min(32, max(0, cvalid - 32 * p));
             if (p == 0) inf.quantised = cached ? 1 : 0;
             if (cached && kCb) {
-                fill_cb_keys(sm + M::k, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
-                if (r16 > 0) fill_coeff(sm + M::coef, stg, bb, nb, c.rp, r16 / 8, p);
+                fill_cb_keys<PAIR>(Kt, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p, rank);
+                if (r16 > 0) fill_coeff<PAIR>(Ct, stg, bb, nb, c.rp, r16 / 8, p, rank);
             } else if (cached) {
-                fill_cache_keys<vbits<FMT>()>(sm + M::k, stg, nb, p);
+                fill_cache_keys<vbits<FMT>(), PAIR>(Kt, stg, nb, p, rank);
                 if (!cache_keys_in_f16_range<vbits<FMT>()>(stg, nb, p)) atomicExch(err + 1, 1);
                 // TAYLOR2: bf16 weights read by the Jensen MMA with Q K^T (stage s, free
-                // since Q K^T of tile j - 2 completed); EXACT: fp32 steps read by the
+                // since Q K^T of tile j - 2 completed; in a pair the even CTA holds the
+                // weight rows, the odd CTA's rows stay zero); EXACT: fp32 steps read by the
                 // softmax, in a ring of 4 like the tile info
-                if (JENSEN == KV_JENSEN_TAYLOR2)
-                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef);
-                else if (JENSEN == KV_JENSEN_EXACT)
-                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef);
-                else if (JENSEN == KV_JENSEN_ISOTROPIC)
-                    fill_weights<vbits<FMT>(), JENSEN>(nullptr, stg, nb, p, jcoef, inf.ss2);
+                if (JENSEN == KV_JENSEN_TAYLOR2) {
+                    if (rank == 0) fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef, G::kWR);
+                } else if (JENSEN == KV_JENSEN_EXACT) {
+                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef, G::kWR);
+                } else if (JENSEN == KV_JENSEN_ISOTROPIC) {
+                    fill_weights<vbits<FMT>(), JENSEN>(nullptr, stg, nb, p, jcoef, G::kWR, inf.ss2);
+                }
             } else {
-                if (!fill_current_keys(sm + M::k, Kcur, row0, cvalid, p)) atomicExch(err + 1, 1);
+                if (!fill_current_keys<PAIR>(Kt, Kcur, row0, cvalid, p, rank)) atomicExch(err + 1, 1);
             }
             fence_proxy_async();
             // publish tile j on K_FULL[s] only after the softmax has finished tile j - 2
@@ -834,9 +969,9 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             // the softmax of this tile proceed meanwhile
             const bool ok2 = j < 2 || mbar_wait(bar(BAR_V_EMPTY + s), ((j - 2) >> 1) & 1, &abort_flag, err, 2);
             if (!__all_sync(0xffffffffu, ok2)) break;
-            unsigned char* Vt = sm + M::v + s * kTile;
-            if (cached) fill_cache_values<FMT>(Vt, stg, bb, nb, pw, lane);
-            else fill_current_values(Vt, Vcur, row0, cvalid, p);
+            unsigned char* Vt = sm + M::v + s * M::kTileV;
+            if (cached) fill_cache_values<FMT, PAIR>(Vt, stg, bb, nb, pw, lane, rank);
+            else fill_current_values<PAIR>(Vt, Vcur, row0, cvalid, p, rank);
             fence_proxy_async();
             mbar_arrive(bar(BAR_V_FULL + s));
             if (cached) {
@@ -899,7 +1034,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
             } else if (info.quantised) {
                 if (JENSEN == KV_JENSEN_TAYLOR2) {
                     float dv[8];
-                    tmem_ld8(tmem + lane_addr + kColD + 16 * s, dv);
+                    tmem_ld8(tmem + lane_addr + kColD + G::kJN * s, dv);
 #pragma unroll
                     for (int g = 0; g < 4; ++g) dl[g] = dv[g] + dv[4 + g];
                 } else if (JENSEN == KV_JENSEN_EXACT) {
@@ -1061,9 +1196,13 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     }
     fence_before();
     __syncthreads();
+    // a pair: neither CTA frees its tensor memory or exits (its shared memory) while the
+    // other may still signal it; the even CTA's MMAs have all completed (MMA_DONE)
+    if (PAIR) cluster_sync();
     if (warp == kMmaWarp) {
         fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if (PAIR) tmem_dealloc2(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -1105,10 +1244,10 @@ tc_operands_kernel(DevCache c, __half* __restrict__ Kout, __half* __restrict__ V
                                   c.centroids + ((long long)b * c.Hkv + h) * kD * 4, p);
     __syncthreads();
     // keys first, then values (the value routine rescales the staged steps in place)
-    if (kCb) fill_cb_keys(sm + M::k, sm + M::stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p);
-    else fill_cache_keys<vbits<FMT>()>(sm + M::k, sm + M::stg, nb, p);
+    if (kCb) fill_cb_keys<false>(sm + M::k, sm + M::stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p, 0);
+    else fill_cache_keys<vbits<FMT>(), false>(sm + M::k, sm + M::stg, nb, p, 0);
     __syncthreads();
-    fill_cache_values<FMT>(sm + M::v, sm + M::stg, bb, nb, pw, lane);
+    fill_cache_values<FMT, false>(sm + M::v, sm + M::stg, bb, nb, pw, lane, 0);
     __syncthreads();
     const long long row0 = ((long long)b * c.Hkv + h) * (long long)nblk * kBlockTokens + (long long)tile * kN;
     for (int e = p; e < nb * kBlockTokens * (kD / 8); e += kProd) {
@@ -1149,21 +1288,53 @@ int num_sms() {
     return g_num_sms;
 }
 
+template <int FMT, int JENSEN, bool PAIR>
+kv_status launch_tc_p(const DevCache& c, const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
+                      float tau, int r16, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
+                      int* err, cudaStream_t st) {
+    constexpr int kSmem = Smem<FMT, PAIR>::total;
+    auto kern = attn_tc_kernel<FMT, JENSEN, PAIR>;
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(kern), kSmem, "attn_tc_kernel");
+    if (sa != KV_OK) return sa;
+    const int n_qt = (n_q + kM - 1) / kM;
+    const int stall = getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(Q);
+    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(Kc);
+    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(Vc);
+    if (!PAIR) {
+        dim3 grid(n_qt * n_splits, Hq, c.B);
+        kern<<<grid, kThreads, kSmem, st>>>(q, kc, vc, n_q, n_cur, Hq, c, tau, r16, n_splits, out, out_f32, lse, ws_o,
+                                            ws_ml, err, stall);
+        return check_launch("attn_tc_kernel");
+    }
+    // pairs of query tiles in 2-CTA clusters
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((n_qt + 1) / 2) * n_splits, Hq, c.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q, kc, vc, n_q, n_cur, Hq, c, tau, r16, n_splits, out, out_f32,
+                                             lse, ws_o, ws_ml, err, stall);
+    if (e != cudaSuccess) return set_error(KV_ERR_CUDA, "attn_tc_kernel (CTA pairs): %s", cudaGetErrorString(e));
+    return check_launch("attn_tc_kernel");
+}
+
 template <int FMT, int JENSEN>
 kv_status launch_tc_t(const DevCache& c, const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
                       float tau, int r16, int n_splits, void* out, int out_f32, float* lse, float* ws_o, float2* ws_ml,
-                      int* err, cudaStream_t st) {
-    constexpr int kSmem = Smem<FMT>::total;
-    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(attn_tc_kernel<FMT, JENSEN>), kSmem,
-                                        "attn_tc_kernel");
-    if (sa != KV_OK) return sa;
-    const int n_qt = (n_q + kM - 1) / kM;
-    dim3 grid(n_qt * n_splits, Hq, c.B);
-    attn_tc_kernel<FMT, JENSEN><<<grid, kThreads, kSmem, st>>>(
-        static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(Kc),
-        static_cast<const __nv_bfloat16*>(Vc), n_q, n_cur, Hq, c, tau, r16, n_splits, out, out_f32, lse, ws_o, ws_ml,
-        err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
-    return check_launch("attn_tc_kernel");
+                      int* err, bool pair, cudaStream_t st) {
+    if (pair)
+        return launch_tc_p<FMT, JENSEN, true>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32, lse,
+                                              ws_o, ws_ml, err, st);
+    return launch_tc_p<FMT, JENSEN, false>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32, lse, ws_o,
+                                           ws_ml, err, st);
 }
 
 }  // namespace
@@ -1212,7 +1383,7 @@ size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits) {
 
 kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
                          const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out, int out_f32,
-                         float* lse, void* ws, cudaStream_t st) {
+                         float* lse, void* ws, bool pair, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     int* err = static_cast<int*>(ws);
     float* ws_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kStatusBytes);
@@ -1224,19 +1395,19 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
     switch (jensen) {                                                                                         \
         case KV_JENSEN_TAYLOR2:                                                                               \
             s = launch_tc_t<FMT, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out,      \
-                                                    out_f32, lse, ws_o, ws_ml, err, st);                      \
+                                                    out_f32, lse, ws_o, ws_ml, err, pair, st);                      \
             break;                                                                                            \
         case KV_JENSEN_EXACT:                                                                                 \
             s = launch_tc_t<FMT, KV_JENSEN_EXACT>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32, \
-                                                  lse, ws_o, ws_ml, err, st);                                 \
+                                                  lse, ws_o, ws_ml, err, pair, st);                                 \
             break;                                                                                            \
         case KV_JENSEN_ISOTROPIC:                                                                             \
             s = launch_tc_t<FMT, KV_JENSEN_ISOTROPIC>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out,    \
-                                                      out_f32, lse, ws_o, ws_ml, err, st);                    \
+                                                      out_f32, lse, ws_o, ws_ml, err, pair, st);                    \
             break;                                                                                            \
         default:                                                                                              \
             s = launch_tc_t<FMT, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, 0, n_splits, out, out_f32,   \
-                                                lse, ws_o, ws_ml, err, st);                                   \
+                                                lse, ws_o, ws_ml, err, pair, st);                                   \
     }
     if (c.kind == KV_CODEBOOK2) {
         // codebook keys carry no step sizes: their Jensen term needs the residual variances
@@ -1244,13 +1415,13 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
         const int jm = c.resid_var ? jensen : KV_JENSEN_OFF;
         if (jm == KV_JENSEN_TAYLOR2)
             s = launch_tc_t<FMT_CB2, KV_JENSEN_TAYLOR2>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32,
-                                                        lse, ws_o, ws_ml, err, st);
+                                                        lse, ws_o, ws_ml, err, pair, st);
         else if (jm == KV_JENSEN_ISOTROPIC)
             s = launch_tc_t<FMT_CB2, KV_JENSEN_ISOTROPIC>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out,
-                                                          out_f32, lse, ws_o, ws_ml, err, st);
+                                                          out_f32, lse, ws_o, ws_ml, err, pair, st);
         else
             s = launch_tc_t<FMT_CB2, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32,
-                                                    lse, ws_o, ws_ml, err, st);
+                                                    lse, ws_o, ws_ml, err, pair, st);
     } else if (c.kind == KV_UNIFORM4) {
         BITKV_TC(FMT_INT4)
     } else {

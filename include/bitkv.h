@@ -130,8 +130,10 @@ typedef enum { KV_JENSEN_OFF = 0, KV_JENSEN_TAYLOR2 = 1, KV_JENSEN_EXACT = 2, KV
 typedef enum {
     KV_PATH_AUTO = 0,   /* decode kernel for n_q == 1, tensor-core kernel for bf16 d=128 chunks, else SIMT */
     KV_PATH_SIMT = 1,   /* CUDA-core fp32 kernel, any dtype/kind */
-    KV_PATH_TC = 2,     /* tcgen05/TMEM kernel: bf16, d = 128, UNIFORM2 / UNIFORM4 / CODEBOOK2 */
-    KV_PATH_DECODE = 3  /* split-K streaming decode: n_q == 1, f16/bf16, d = 64 or 128 */
+    KV_PATH_TC = 2,     /* tcgen05/TMEM kernel: bf16, d = 128, UNIFORM2 / UNIFORM4 / CODEBOOK2; CTA pairs
+                           (2-CTA clusters, M = 256: each CTA expands half of every key and value tile) */
+    KV_PATH_DECODE = 3, /* split-K streaming decode: n_q == 1, f16/bf16, d = 64 or 128 */
+    KV_PATH_TC_SINGLE = 4 /* the tensor-core kernel with one CTA per query tile (M = 128) */
 } kv_path;
 
 typedef struct {

@@ -128,8 +128,12 @@ def test_chunk_workload_simt_sampled():
 
 # ------------------------------------------------------ tensor-core path -----
 
+TC_PATHS = [B.KV_PATH_TC, B.KV_PATH_TC_SINGLE]     # CTA pairs (the default) and one CTA per query tile
+
+
+@pytest.mark.parametrize("path", TC_PATHS)
 @pytest.mark.parametrize("jensen", [2, 1])
-def test_tc_repeated_runs_identical(jensen):
+def test_tc_repeated_runs_identical(jensen, path):
     """tcgen05 kernel: 200 repeated calls on one input give bit-identical outputs within the
     oracle's bounds.  The EXACT softmax is slow, so Q K^T of tile j and P V of tile j - 2
     (which share TMEM columns) are issued back to back; an ordering race between them showed
@@ -140,7 +144,7 @@ def test_tc_repeated_runs_identical(jensen):
     for splits in (3, 1):
         first = None
         for _ in range(200):
-            o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_TC, splits=splits)
+            o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=path, splits=splits)
             if first is None:
                 assert_close(o, l, ref[0], ref[1], tol("bf16"))
                 assert_close(o, l, tight[0], tight[1], 2e-3)
@@ -149,29 +153,33 @@ def test_tc_repeated_runs_identical(jensen):
                 assert np.array_equal(o, first[0]) and np.array_equal(l, first[1])
 
 
+@pytest.mark.parametrize("path", TC_PATHS)
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("jensen", [0, 1, 2, 3])
-def test_chunk_small_tc(bits, jensen):
-    """tcgen05 kernel: ragged cache blocks, ragged current tile, partial query tile, GQA."""
-    case = synth.chunk_case(61, B=2, Hkv=2, Hq=4, d=128, chunks=[300, 77], n_cur=150, n_q=150, dtype="bf16")
-    tc = gpu_uniform(case, bits)
-    ref, tight = refs(oracle_uniform(case, bits), case, "bf16", tc_path=True, jensen=jensen)
-    for splits in (1, 3):
-        attention_checked(tc, case, ref, "bf16", tight, jensen=jensen, path=B.KV_PATH_TC, splits=splits)
+def test_chunk_small_tc(bits, jensen, path):
+    """tcgen05 kernel: ragged cache blocks, ragged current tile, partial query tile, GQA; 150
+    and 300 queries (2 and 3 query tiles: a full pair, and a pair with an empty odd CTA)."""
+    for n_q in (150, 300):
+        case = synth.chunk_case(61, B=2, Hkv=2, Hq=4, d=128, chunks=[300, 77], n_cur=150, n_q=n_q, dtype="bf16")
+        tc = gpu_uniform(case, bits)
+        ref, tight = refs(oracle_uniform(case, bits), case, "bf16", tc_path=True, jensen=jensen)
+        for splits in (1, 3):
+            attention_checked(tc, case, ref, "bf16", tight, jensen=jensen, path=path, splits=splits)
 
 
-def test_tc_only_current_or_only_cache():
+@pytest.mark.parametrize("path", TC_PATHS)
+def test_tc_only_current_or_only_cache(path):
     case = synth.chunk_case(62, B=1, Hkv=2, d=128, chunks=[200], n_cur=130, n_q=64, dtype="bf16")
     empty = B.TorchCache(1, 2, 128, B.KV_UNIFORM2, (0, 0, 8))
     oc0 = OL.build_uniform(case["K_cache"][:, :, :0], case["V_cache"][:, :, :0], 2, [], 8)
     ref, tight = refs(oc0, case, "bf16", tc_path=True)
-    attention_checked(empty, case, ref, "bf16", tight, path=B.KV_PATH_TC)
+    attention_checked(empty, case, ref, "bf16", tight, path=path)
     tc = gpu_uniform(case, 2)
     oc = oracle_uniform(case, 2)
     z = np.zeros((1, 2, 0, 128), np.float32)
     ref = OA.attention_over_cache(oc, case["Q"], z, z, "bf16", jensen=1)
     tight = OA.attention_over_cache(oc, case["Q"], z, z, "bf16", jensen=1, operand_dtype="f16")
-    attention_checked(tc, case, ref, "bf16", tight, jensen=1, path=B.KV_PATH_TC, Kcur=z, Vcur=z)
+    attention_checked(tc, case, ref, "bf16", tight, jensen=1, path=path, Kcur=z, Vcur=z)
 
 
 def _workload_tc_sampled(case, heads, rows, jensen):

@@ -32,8 +32,9 @@ def oracle_calibrated_cache(case, n, r):
     return tc, oc, U
 
 
+@pytest.mark.parametrize("path", [B.KV_PATH_TC, B.KV_PATH_TC_SINGLE])
 @pytest.mark.parametrize("r", [0, 8, 24, 32])
-def test_codebook_tc_small(r):
+def test_codebook_tc_small(r, path):
     """Ragged cache (15 blocks, the last partial: tiles of 4, 4, 4, 3 blocks), ragged current
     tile, partial query tile; rank 24 leaves a zero 8-wide chunk in the 32-wide PSAC operand."""
     case = synth.codebook_case(seed=71, H=2, d=128, n_cache=450, n_cur=150, n_hist=128)
@@ -43,7 +44,7 @@ def test_codebook_tc_small(r):
         ref = OA.attention_over_cache(*args, psac_U=U if psac else None)
         tight = OA.attention_over_cache(*args, psac_U=U if psac else None, operand_dtype="f16")
         for splits in (1, 3):
-            attention_checked(tc, case, ref, "bf16", tight, psac=psac, path=B.KV_PATH_TC, splits=splits)
+            attention_checked(tc, case, ref, "bf16", tight, psac=psac, path=path, splits=splits)
 
 
 def test_codebook_tc_matches_simt_and_jensen_has_no_effect():

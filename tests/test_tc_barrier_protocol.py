@@ -44,16 +44,18 @@ class Bar:
 
 
 class Model:
-    def __init__(self, T, seed, old_qk_rule=False, old_epilogue=False, old_publish=False):
+    def __init__(self, T, seed, old_qk_rule=False, old_epilogue=False, old_publish=False, kbuf=1, old_kbuf_wait=False):
         self.T, self.rng = T, random.Random(seed)
+        self.kbuf = kbuf                      # K_hat buffers (2 in the CTA-pair kernel)
+        self.old_kbuf_wait = old_kbuf_wait    # with 2 buffers, wait only for Q K^T of tile j - 1 to start
         self.old_qk_rule, self.old_epilogue = old_qk_rule, old_epilogue
         self.old_publish = old_publish
         names = ["K_FULL0", "K_FULL1", "V_FULL0", "V_FULL1", "V_EMPTY0", "V_EMPTY1", "S_FULL0", "S_FULL1",
-                 "P_FULL0", "P_FULL1", "O_DONE", "K_EMPTY", "MMA_DONE"]
+                 "P_FULL0", "P_FULL1", "O_DONE", "K_EMPTY", "K_EMPTY0", "K_EMPTY1", "MMA_DONE"]
         self.bar = {n: Bar(n) for n in names}
         self.errors = []
         # buffer contents: what each holds now
-        self.khat = None
+        self.khat = [None, None]              # K_hat buffer b holds tile ...
         self.vhat = [None, None]
         self.s = [None, None]                 # ("S", j) after Q K^T, ("P", j) after the softmax
         self.o = set()                        # tiles whose P V is summed into O
@@ -74,8 +76,8 @@ class Model:
 
     def check_reads(self, op):
         j = op["j"]
-        if op["kind"] == "QK" and self.khat != j:
-            self.errors.append(f"QK({j}) reads K_hat holding {self.khat}")
+        if op["kind"] == "QK" and self.khat[j % self.kbuf] != j:
+            self.errors.append(f"QK({j}) reads K_hat holding {self.khat[j % self.kbuf]}")
         if op["kind"] == "PV":
             if self.s[j & 1] != ("P", j):
                 self.errors.append(f"PV({j}) reads P from S columns holding {self.s[j & 1]}")
@@ -121,9 +123,17 @@ class Model:
     def producers(self):
         for j in range(self.T):
             s = j & 1
-            if j > 0:
-                yield from self.wait("K_EMPTY", j - 1)
-            self.khat = j
+            # the K_hat buffer of tile j is free once Q K^T of tile j - kbuf completed: one
+            # barrier with one buffer; with two, each buffer's own barrier (one barrier for
+            # both cannot express "tile j - 2" once tile j - 1 has also completed)
+            if j >= self.kbuf:
+                if self.kbuf == 1:
+                    yield from self.wait("K_EMPTY", j - 1)
+                elif self.old_kbuf_wait:
+                    yield from self.wait("K_EMPTY", j - 2)
+                else:
+                    yield from self.wait(f"K_EMPTY{j & 1}", (j - 2) >> 1)
+            self.khat[j % self.kbuf] = j
             self.ring[j & 3] = j
             # tile j is published only after the softmax finished tile j - 2
             if j >= 2 and not self.old_publish:
@@ -150,7 +160,7 @@ class Model:
                        or self.bar[f"V_EMPTY{nq & 1}"].test((nq - 2) >> 1, self.errors))):
                 self.issue("QK", nq)
                 self.commit(f"S_FULL{nq & 1}")
-                self.commit("K_EMPTY")
+                self.commit("K_EMPTY" if self.kbuf == 1 or self.old_kbuf_wait else f"K_EMPTY{nq & 1}")
                 nq += 1
             yield
         self.commit("MMA_DONE")
@@ -242,4 +252,26 @@ def test_model_finds_the_unguarded_publish():
         m = Model(3, seed, old_publish=True)
         m.run()
         hits += any(e.startswith("K_FULL") for e in m.errors)
+    assert hits > 0
+
+
+@pytest.mark.parametrize("T", [2, 3, 5, 8])
+def test_two_key_buffers_have_no_race(T):
+    """The CTA-pair kernel's two K_hat buffers: tile j is expanded into buffer j & 1 once Q K^T of
+    tile j - 2 has completed (that buffer's own K_EMPTY barrier); on every schedule no wait is
+    two phases off and every Q K^T reads its own tile."""
+    for seed in range(400):
+        m = Model(T, seed, kbuf=2)
+        m.run()
+        assert not m.errors, f"T={T} seed={seed}: {m.errors[:3]}"
+
+
+def test_model_finds_the_shared_empty_barrier_race():
+    """Two buffers behind one K_EMPTY barrier: waiting there for Q K^T of tile j - 2 fails once
+    Q K^T of tile j - 1 has completed too (two phases past: the wait blocks)."""
+    hits = 0
+    for seed in range(2000):
+        m = Model(6, seed, kbuf=2, old_kbuf_wait=True)
+        m.run()
+        hits += any(e.startswith("K_EMPTY") or "reads K_hat" in e for e in m.errors)
     assert hits > 0
