@@ -36,7 +36,7 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
                          const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out, int out_f32,
                          float* lse, void* ws, bool pair, cudaStream_t st);
 size_t tc_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits);
-int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq);
+int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq, bool pair);
 bool tc_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const char** why);
 kv_status launch_codebook_fit(const void* K, kv_dtype dt, int n_tokens, const kv_cache* cache, int iters,
                               const void* Qhist, int n_hist, float* weights_out, int range, void* ws, cudaStream_t st);
@@ -315,7 +315,8 @@ static int pick_path(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const 
 static int pick_splits(const kv_cache* cache, int path, int n_q, int n_cur, int Hq, const kv_attn_opts* o) {
     if (o && o->num_splits > 0) return o->num_splits;
     if (path == KV_PATH_DECODE) return decode_auto_splits(cache, Hq);
-    if (path == KV_PATH_TC || path == KV_PATH_TC_SINGLE) return tc_auto_splits(cache, n_q, n_cur, Hq);
+    if (path == KV_PATH_TC || path == KV_PATH_TC_SINGLE)
+        return tc_auto_splits(cache, n_q, n_cur, Hq, path == KV_PATH_TC);
     // SIMT: enough CTAs to fill the GPU about twice
     const long long ctas = (long long)cache->layout.B * Hq * ((n_q + 31) / 32);
     const int units = simt_units_cache(cache) + (n_cur + 31) / 32;

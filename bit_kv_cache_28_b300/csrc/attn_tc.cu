@@ -1352,18 +1352,21 @@ bool tc_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq, const cha
     return true;
 }
 
-int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq) {
+int tc_auto_splits(const kv_cache* cache, int n_q, int n_cur, int Hq, bool pair) {
     const kv_layout& L = cache->layout;
     const int seg = L.kind == KV_UNIFORM4 ? KV_SEG_INT4 : KV_SEG_INT2;
     const int tiles = (cache->n_blocks[seg] + 3) / 4 + (n_cur + kN - 1) / kN;
-    const long long ctas = (long long)L.B * Hq * ((n_q + kM - 1) / kM);
+    const int n_qt = (n_q + kM - 1) / kM;
+    const long long ctas = (long long)L.B * Hq * (pair ? 2 * ((n_qt + 1) / 2) : n_qt);
+    // pipeline fill per CTA, in tiles: longer for a pair, whose halves meet through the cluster
+    const double fill = pair ? 6.0 : 3.0;
     const int sms = num_sms();
     int best = 1;
     double best_cost = 1e30;
     for (int s = 1; s <= 8; ++s) {
         if (s > 1 && tiles / s < 6) break;
         const double waves = (double)((ctas * s + sms - 1) / sms);
-        const double cost = waves * ((double)tiles / s + 3.0);   // +3 tiles of pipeline fill per CTA
+        const double cost = waves * ((double)tiles / s + fill);
         if (cost < best_cost * 0.97) {
             best_cost = cost;
             best = s;
