@@ -25,6 +25,11 @@ head dim d:
                          Vm  float2[d/32][32]
                          Kq  fp16[32][rp]         PSAC coefficients, rp = ceil8(r)
 
+fp16-metadata caches (a layout flag; INT2 / INT4 blocks only): Km is half2[d] and
+Vm half2[d/32][32], each pair (s, z) as two fp16 values, so the block shrinks by
+4 d bytes (d = 128 INT2: 4096 -> 3072 B); the quantiser then takes its codes
+against the fp16 pair (oracle/quant.py).
+
 Within a word, element i (channel for Kc, token for Vc) sits at bit
 b*(i mod 32/b).  Keys are token-major because a key row feeds Q K^T;
 values are channel-major because a value column feeds P V.  Pad slots
@@ -53,23 +58,24 @@ def ceil8(r):
     return (r + 7) // 8 * 8
 
 
-def block_bytes(cls, d, r=0):
+def block_bytes(cls, d, r=0, meta16=False):
     if cls == RAW16:
         return 2 * BLOCK * d * 2
     if cls in (INT2, INT4):
         b = CLASS_BITS[cls]
-        return 2 * (BLOCK * d * b // 8) + 8 * d + BLOCK * (d // 32) * 8
+        pair = 4 if meta16 else 8              # bytes of one (s, z)
+        return 2 * (BLOCK * d * b // 8) + pair * d + BLOCK * (d // 32) * pair
     if cls == CB2:
         return 2 * (BLOCK * d * 2 // 8) + BLOCK * (d // 32) * 8 + BLOCK * ceil8(r) * 2
     raise ValueError(cls)
 
 
-def stream_layout(classes, caps, d, r=0):
+def stream_layout(classes, caps, d, r=0, meta16=False):
     """Segment byte offsets and stream bytes for segments ``classes`` with capacities ``caps``."""
     offs, o = [], 0
     for c, n in zip(classes, caps):
         offs.append(o)
-        o += n * block_bytes(c, d, r)
+        o += n * block_bytes(c, d, r, meta16)
     return offs, o
 
 
@@ -80,11 +86,19 @@ def _bits16(x, dtype):
     return t.view(torch.int16).numpy().view(np.uint8)
 
 
-def encode_int_blocks(Kb, Vb, bits, nvalid):
+def _meta_bytes(sz, meta16):
+    """(s, z) pairs [..., 2] as stored: fp32 pairs, or fp16 pairs under meta16."""
+    if not meta16:
+        return np.ascontiguousarray(sz, F32).view(np.uint8)
+    return _bits16(sz, "f16")
+
+
+def encode_int_blocks(Kb, Vb, bits, nvalid, meta16=False):
     """Quantise and pack N blocks that share one valid length.
 
     Kb, Vb: fp32 [N, 32, d].  Keys: one group per (block, channel) over the
     valid tokens.  Values: one group per (token, 32 consecutive channels).
+    meta16: (s, z) stored as fp16 pairs (see oracle/quant.py).
     Returns a dict with the packed bytes [N, block_bytes] and the unpacked
     codes, steps and zero points, plus the dequantised fp32 entries.
     """
@@ -92,9 +106,9 @@ def encode_int_blocks(Kb, Vb, bits, nvalid):
     Vb = np.asarray(Vb, F32)
     N, T, d = Kb.shape
     assert T == BLOCK and d % 32 == 0
-    kc, ks, kz = quantize_groups(Kb.transpose(0, 2, 1), bits, nvalid)   # [N,d,32]
-    kc = np.ascontiguousarray(kc.transpose(0, 2, 1))                     # [N,32,d]
-    vc, vs, vz = quantize_groups(Vb.reshape(N, T, d // 32, 32), bits)   # [N,32,d/32,32]
+    kc, ks, kz = quantize_groups(Kb.transpose(0, 2, 1), bits, nvalid, meta16)   # [N,d,32]
+    kc = np.ascontiguousarray(kc.transpose(0, 2, 1))                             # [N,32,d]
+    vc, vs, vz = quantize_groups(Vb.reshape(N, T, d // 32, 32), bits, None, meta16)   # [N,32,d/32,32]
     vc[:, nvalid:] = 0
     vs[:, nvalid:] = 0
     vz[:, nvalid:] = 0
@@ -102,8 +116,8 @@ def encode_int_blocks(Kb, Vb, bits, nvalid):
     vw = pack_codes(vc.reshape(N, T, d).transpose(0, 2, 1), bits)   # [N,d,b]
     km = np.stack([ks, kz], -1).astype(F32)                    # [N,d,2]
     vm = np.stack([vs, vz], -1).astype(F32).transpose(0, 2, 1, 3)   # [N,d/32,32,2]
-    raw = np.concatenate([kw.reshape(N, -1).view(np.uint8), km.reshape(N, -1).view(np.uint8),
-                          vw.reshape(N, -1).view(np.uint8), vm.reshape(N, -1).view(np.uint8)], axis=1)
+    raw = np.concatenate([kw.reshape(N, -1).view(np.uint8), _meta_bytes(km, meta16).reshape(N, -1),
+                          vw.reshape(N, -1).view(np.uint8), _meta_bytes(vm, meta16).reshape(N, -1)], axis=1)
     khat = dequantize(kc, ks[:, None, :], kz[:, None, :])
     vhat = dequantize(vc, vs[..., None], vz[..., None]).reshape(N, T, d)
     return dict(bytes=raw, kcode=kc, ks=ks, kz=kz, vcode=vc.reshape(N, T, d), vs=vs, vz=vz,
@@ -161,10 +175,10 @@ class Cache:
               key step size), and per block the key step sizes ks [nblk, d].
     """
 
-    def __init__(self, B, H, d, classes, caps, r=0):
+    def __init__(self, B, H, d, classes, caps, r=0, meta16=False):
         self.B, self.H, self.d = B, H, d
-        self.classes, self.caps, self.r = list(classes), list(caps), r
-        self.seg_off, self.stream_bytes = stream_layout(classes, caps, d, r)
+        self.classes, self.caps, self.r, self.meta16 = list(classes), list(caps), r, meta16
+        self.seg_off, self.stream_bytes = stream_layout(classes, caps, d, r, meta16)
         self.data = np.zeros((B, H, self.stream_bytes), np.uint8)
         ncap = int(sum(caps))
         self.blk_len = np.zeros((B, ncap), np.int32)
@@ -177,7 +191,7 @@ class Cache:
 
     def _put(self, b, h, seg, idx, raw):
         cls = self.classes[seg]
-        bb = block_bytes(cls, self.d, self.r)
+        bb = block_bytes(cls, self.d, self.r, self.meta16)
         o = self.seg_off[seg] + idx * bb
         self.data[b, h, o:o + bb] = raw
 
@@ -198,18 +212,19 @@ class Cache:
         return out
 
 
-def build_uniform(K, V, bits, appends, cap_blocks):
+def build_uniform(K, V, bits, appends, cap_blocks, meta16=False):
     """Cache of uniform INT{bits} blocks built by successive chunk appends.
 
     K, V: fp32 [B, H, n_total, d]; ``appends`` lists chunk lengths that sum to
     n_total.  Each chunk starts a new block (groups aligned to the chunk).
+    meta16: blocks store their (s, z) as fp16.
     """
     K = np.asarray(K, F32)
     V = np.asarray(V, F32)
     B, H, n_total, d = K.shape
     assert sum(appends) == n_total
     cls = INT2 if bits == 2 else INT4
-    c = Cache(B, H, d, [cls], [cap_blocks])
+    c = Cache(B, H, d, [cls], [cap_blocks], meta16=meta16)
     t0 = 0
     for n in appends:
         nfull, tail = divmod(n, BLOCK)
@@ -228,7 +243,7 @@ def build_uniform(K, V, bits, appends, cap_blocks):
             segv = V[:, :, a:a + cnt * nv]
             Kb[:, :, :, :nv] = seg.reshape(B, H, cnt, nv, d)
             Vb[:, :, :, :nv] = segv.reshape(B, H, cnt, nv, d)
-            enc = encode_int_blocks(Kb.reshape(-1, BLOCK, d), Vb.reshape(-1, BLOCK, d), bits, nv)
+            enc = encode_int_blocks(Kb.reshape(-1, BLOCK, d), Vb.reshape(-1, BLOCK, d), bits, nv, meta16)
             raw = enc["bytes"].reshape(B, H, cnt, -1)
             kh = enc["khat"].reshape(B, H, cnt, BLOCK, d)
             vh = enc["vhat"].reshape(B, H, cnt, BLOCK, d)
@@ -254,12 +269,13 @@ def build_uniform(K, V, bits, appends, cap_blocks):
     return c
 
 
-def build_mixed(K, V, window_bits, caps, dtype):
+def build_mixed(K, V, window_bits, caps, dtype, meta16=False):
     """Mixed FP16/INT4/INT2 cache of one prefill, one class per 32-token window.
 
     K, V: fp32 [B, H, n, d] holding values exact in ``dtype`` ('f16'/'bf16').
     window_bits: int [B, W] with entries 16, 4 or 2; W = ceil(n / 32).
     Windows of one class are stored in ascending window order in their segment.
+    meta16: INT blocks store their (s, z) as fp16.
     """
     K = np.asarray(K, F32)
     V = np.asarray(V, F32)
@@ -267,7 +283,7 @@ def build_mixed(K, V, window_bits, caps, dtype):
     W = (n + BLOCK - 1) // BLOCK
     window_bits = np.asarray(window_bits)
     assert window_bits.shape == (B, W)
-    c = Cache(B, H, d, [RAW16, INT4, INT2], caps)
+    c = Cache(B, H, d, [RAW16, INT4, INT2], caps, meta16=meta16)
     cls_of = {16: 0, 4: 1, 2: 2}
     counts = None
     for b in range(B):
@@ -285,7 +301,7 @@ def build_mixed(K, V, window_bits, caps, dtype):
                 ks = np.zeros((H, d), F32)
                 kcd = vcd = [None] * H
             else:
-                enc = encode_int_blocks(Kb, Vb, 4 if seg == 1 else 2, nv)
+                enc = encode_int_blocks(Kb, Vb, 4 if seg == 1 else 2, nv, meta16)
                 ks = enc["ks"]
                 kcd, vcd = enc["kcode"], enc["vcode"]
             idx = cnt[seg]

@@ -17,6 +17,18 @@ The decisions that produce integers (t_i and its rounding) are taken in fp32,
 the precision the kernels use, so codes can be compared bit for bit.  ``-0.0``
 as a minimum is canonicalised to ``+0.0`` (``m + 0.0``) so that stored bytes are
 unique.
+
+fp16 metadata (a cache variant that stores s and z as fp16, for the smaller
+caches the WindowQuant note (主な結果) and the QuantWM card (Key Results) report):
+s and z are the fp16 round-to-nearest-even of the fp32 s and m above (a ``-0``
+zero point stored as ``+0``), and the codes are taken against the stored pair,
+
+    t_i = fl32(fl32(x_i - z16) / s16),  code_i = clamp(rint(t_i), 0, 2^b - 1)
+    (code 0 everywhere if s16 == 0),    x_hat_i = fmaf(code_i, s16, z16),
+
+so that each code is the nearest level of the grid the cache actually holds.
+Inputs stay within the fp16 range (|x| <= 65504); beyond it s16 or z16 would
+be infinite.
 """
 
 from __future__ import annotations
@@ -58,15 +70,23 @@ def fma32(a, b, c):
     return out
 
 
-def quantize_groups(x, bits, n_valid=None):
+def f16_rne(x):
+    """fp16 round-to-nearest-even of fp32 values, returned as fp32 (exact widening)."""
+    x = np.asarray(x, dtype=F32)
+    return np.asarray(round_to(x, "f16"), dtype=F32).reshape(x.shape)
+
+
+def quantize_groups(x, bits, n_valid=None, meta16=False):
     """Quantise groups laid out along the last axis.
 
     x       : fp32 array [..., n] (n <= 32 for the cache, any n here).
     bits    : 2 or 4.
     n_valid : members [0, n_valid) are real; the rest are padding (code 0,
               excluded from min/max).  ``None`` means all n are valid.
+    meta16  : store s and z as fp16 and take the codes against them.
 
-    Returns (codes uint8 [..., n], s fp32 [...], z fp32 [...]).
+    Returns (codes uint8 [..., n], s fp32 [...], z fp32 [...]); with meta16
+    s and z hold fp16 values.
     """
     x = np.asarray(x, dtype=F32)
     n = x.shape[-1]
@@ -82,6 +102,9 @@ def quantize_groups(x, bits, n_valid=None):
     m = (m + F32(0.0)).astype(F32)               # -0.0 -> +0.0
     D = (mx - m).astype(F32)
     s = ((D / qmax).astype(F32) + F32(0.0)).astype(F32)   # -0.0 -> +0.0
+    if meta16:
+        s = f16_rne(s)
+        m = (f16_rne(m) + F32(0.0)).astype(F32)
     s_safe = np.where(s > 0, s, F32(1.0)).astype(F32)
     t = ((xv - m[..., None]).astype(F32) / s_safe[..., None]).astype(F32)
     code = np.clip(np.rint(t), 0, qmax)
