@@ -24,7 +24,10 @@ follow the chunk-wise video-diffusion and video-VLM settings of the pages):
 * ``tiny``: 1 head, d 64, fp32, 1024 cached + 64 current tokens.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rollout|chunk|decode|codebook|rollout_decode|tiny]
-                    [--jensen 0|1|2|3]
+                    [--jensen 0|1|2|3] [--meta16]
+
+``--meta16`` stores the INT blocks' step and zero point as fp16 pairs (not for codebook):
+an INT2 block at d 128 is 3072 bytes instead of 4096.
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 N > 1 runs independent replicas (weak scaling): every rank owns its own
@@ -280,7 +283,8 @@ class ChunkRunner:
         r = spec.get("r", 0)
         kind = B.KV_CODEBOOK2 if spec["name"] == "codebook" else B.KV_UNIFORM2
         self.tc = B.TorchCache(spec["B"], spec["Hkv"], spec["d"], kind, (0, 0, nb_cache + nb_cur),
-                               raw_dtype=B.KV_BF16, psac_rank=r, device=dev)
+                               raw_dtype=B.KV_BF16, psac_rank=r, device=dev,
+                               meta_dtype=B.KV_F16 if spec.get("meta16") else B.KV_F32)
         self.calib_ms = None
         if kind == B.KV_CODEBOOK2:
             # calibration of the prefill on the device: per-channel centroids of the cached keys,
@@ -352,18 +356,22 @@ class DecodeRunner:
         for b in range(Bn):
             B.kv_window_plan(np.ascontiguousarray(inputs["sim"][b], np.float32), W, th, bits[b])
         caps = [int((bits[0] == k).sum()) for k in (16, 4, 2)]
-        self.tc = B.TorchCache(Bn, Hkv, d, B.KV_MIXED, caps, raw_dtype=B.KV_F16, device=dev)
+        m16 = bool(spec.get("meta16"))
+        self.tc = B.TorchCache(Bn, Hkv, d, B.KV_MIXED, caps, raw_dtype=B.KV_F16, device=dev,
+                               meta_dtype=B.KV_F16 if m16 else B.KV_F32)
         bits_dev = torch.from_numpy(bits).to(dev)
         self.K_cache = to(inputs["K_cache"])
         B.kv_quantize_append(self.K_cache, to(inputs["V_cache"]), self.dt, n, self.tc.c,
                              B.kv_append_opts(bits.ctypes.data, bits_dev.data_ptr()))
         torch.cuda.synchronize(dev)
-        # algorithmic cache bytes: codes of valid tokens + all metadata; 16-bit windows' valid rows
+        # algorithmic cache bytes: codes of valid tokens + all metadata (key and value pairs,
+        # 2 d of each per block); 16-bit windows' valid rows
         bl = self.tc.blk_len.cpu().numpy().reshape(Bn, -1)
         nb = list(self.tc.c.n_blocks)
         lens = [bl[:, :nb[0]], bl[:, nb[0]:nb[0] + nb[1]], bl[:, nb[0] + nb[1]:nb[0] + nb[1] + nb[2]]]
-        per_b = (lens[0].sum(1) * 2 * d * 2 + lens[1].sum(1) * 2 * d * 4 / 8 + nb[1] * 16 * d
-                 + lens[2].sum(1) * 2 * d * 2 / 8 + nb[2] * 16 * d)
+        meta = (8 if m16 else 16) * d
+        per_b = (lens[0].sum(1) * 2 * d * 2 + lens[1].sum(1) * 2 * d * 4 / 8 + nb[1] * meta
+                 + lens[2].sum(1) * 2 * d * 2 / 8 + nb[2] * meta)
         self.cache_bytes = float(per_b.sum() * Hkv)
         self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
         self.Q, self.Kc, self.Vc = self.inputs
@@ -417,6 +425,27 @@ def with_jensen(spec, jensen):
     return spec
 
 
+def with_meta16(spec, on):
+    """The workload on a cache with fp16 (s, z) metadata: the algorithmic cache and append
+    bytes count 4-byte pairs instead of 8-byte ones."""
+    if not on:
+        return spec
+    if spec["name"] == "codebook":
+        raise SystemExit("--meta16: codebook caches keep fp32 metadata")
+    spec = dict(spec, meta16=True)
+    if spec["kind"] in ("chunk", "chunkdecode"):
+        H, d, chunks = spec["Hkv"], spec["d"], spec["chunks"]
+        n_cache = sum(chunks)
+        groups = sum((n + 31) // 32 for n in chunks)
+        spec["cache_bytes"] = H * n_cache * d * 2 * 2 / 8 + H * groups * d * 4 + H * n_cache * (d // 32) * 4
+        if spec["kind"] == "chunk":
+            n = spec["n_cur"]
+            spec["append_bytes"] = (2 * H * n * d * (4 if spec["dtype"] == "f32" else 2)
+                                    + H * ((n + 31) // 32) * (32 * d * 2 * 2 // 8 + 8 * d))
+    spec["label"] += ", fp16 (s, z) metadata"
+    return spec
+
+
 def max_over_ranks(times, dist, device):
     """Each timing (seconds) as the slowest rank measured it: the job's step ends when its
     last replica does."""
@@ -436,7 +465,7 @@ def run_own(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec = with_jensen(workload_spec(args.workload), args.jensen)
+    spec = with_meta16(with_jensen(workload_spec(args.workload), args.jensen), args.meta16)
     inputs = make_inputs(spec)
     r = (DecodeRunner if spec["kind"] == "decode" else ChunkRunner)(spec, inputs, dev)
     if spec["kind"] == "chunkdecode":
@@ -513,7 +542,8 @@ def run_own(args, rank, world, dist):
         if peaks.get("bf16_tflops_sustained"):
             # the kernel is timed alone (burst peak above); the power-capped figure for context
             roof["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
-    roof.update({"traffic": traffic_for(kernel, spec["name"]), "kernel": kernel, "splits": r.splits,
+    tkey = spec["name"] + ("+meta16" if spec.get("meta16") else "")
+    roof.update({"traffic": traffic_for(kernel, tkey), "kernel": kernel, "splits": r.splits,
                  "peak_source": peaks["source"],
                  "algorithmic": ("cache bytes (codes of valid tokens + all metadata) per launch"
                                  if spec["kind"] in ("decode", "chunkdecode")
@@ -584,12 +614,13 @@ def oracle_sample_step(spec, inputs, heads):
     decode: `heads` kv heads of sequence 0 (cache build + attention of their query heads).
     """
     from oracle import layout as OL, attention as OA, window as OW
+    m16 = bool(spec.get("meta16"))
     if spec["kind"] == "decode":
         sl = slice(0, heads)
         b = slice(0, 1)
         bits, _ = OW.window_plan(inputs["sim"][0], 0.2, 0.3)
         caps = [int((bits == k).sum()) for k in (16, 4, 2)]
-        oc = OL.build_mixed(inputs["K_cache"][b, sl], inputs["V_cache"][b, sl], bits[None], caps, "f16")
+        oc = OL.build_mixed(inputs["K_cache"][b, sl], inputs["V_cache"][b, sl], bits[None], caps, "f16", m16)
         g = spec["Hq"] // spec["Hkv"]
         OA.attention_over_cache(oc, inputs["Q"][b, :heads * g], inputs["K_cur"][b, sl], inputs["V_cur"][b, sl],
                                 "f16")
@@ -597,7 +628,7 @@ def oracle_sample_step(spec, inputs, heads):
     sl = slice(0, heads)
     if spec["kind"] == "chunkdecode":
         oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
-                              sum((n + 31) // 32 for n in spec["chunks"]))
+                              sum((n + 31) // 32 for n in spec["chunks"]), m16)
         OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
                                 spec["dtype"], jensen=spec["jensen"])
         return spec["B"] * heads
@@ -613,11 +644,11 @@ def oracle_sample_step(spec, inputs, heads):
         OC.build_codebook(inputs["K_cur"][:, sl], inputs["V_cur"][:, sl], cent, U, (spec["n_cur"] + 31) // 32)
         return spec["B"] * heads * spec["n_q"]
     oc = OL.build_uniform(inputs["K_cache"][:, sl], inputs["V_cache"][:, sl], 2, spec["chunks"],
-                          sum((n + 31) // 32 for n in spec["chunks"]))
+                          sum((n + 31) // 32 for n in spec["chunks"]), m16)
     OA.attention_over_cache(oc, inputs["Q"][:, sl], inputs["K_cur"][:, sl], inputs["V_cur"][:, sl],
                             spec["dtype"], jensen=spec["jensen"])
     OL.build_uniform(inputs["K_cur"][:, sl], inputs["V_cur"][:, sl], 2, [spec["n_cur"]],
-                     (spec["n_cur"] + 31) // 32)
+                     (spec["n_cur"] + 31) // 32, m16)
     return spec["B"] * heads * spec["n_q"]
 
 
@@ -661,7 +692,7 @@ def cpu_baseline(spec, inputs):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    spec = with_jensen(workload_spec(args.workload), args.jensen)
+    spec = with_meta16(with_jensen(workload_spec(args.workload), args.jensen), args.meta16)
     inputs = make_inputs(spec)
     heads = 1
     for _ in range(args.warmup):
@@ -693,6 +724,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--jensen", type=int, default=None, choices=[0, 1, 2, 3],
                     help="override the workload's Jensen mode (0 off, 1 TAYLOR2, 2 EXACT, 3 ISOTROPIC)")
+    ap.add_argument("--meta16", action="store_true",
+                    help="fp16 step / zero-point metadata in the INT blocks (not for codebook)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "own" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -41,7 +41,7 @@ EXPORTS = ["kv_layout_init", "kv_layout_bytes", "kv_cache_init", "kv_quantize_ap
 class kv_layout(C.Structure):
     _fields_ = [("B", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32), ("kind", C.c_int32),
                 ("raw_dtype", C.c_int32), ("psac_rank", C.c_int32), ("cap_blocks", C.c_int32 * 3),
-                ("block_bytes", C.c_int64 * 3), ("seg_offset", C.c_int64 * 3), ("stream_bytes", C.c_int64)]
+                ("meta_dtype", C.c_int32), ("block_bytes", C.c_int64 * 3), ("seg_offset", C.c_int64 * 3), ("stream_bytes", C.c_int64)]
 
 
 class kv_cache(C.Structure):
@@ -81,7 +81,7 @@ def lib():
         L = C.CDLL(_LIB_PATH)
         P, I, S = C.c_void_p, C.c_int, C.c_size_t
         sig = {
-            "kv_layout_init": (C.c_int, [C.POINTER(kv_layout), I, I, I, I, I, C.POINTER(C.c_int32), I]),
+            "kv_layout_init": (C.c_int, [C.POINTER(kv_layout), I, I, I, I, I, C.POINTER(C.c_int32), I, I]),
             "kv_layout_bytes": (S, [C.POINTER(kv_layout), I]),
             "kv_cache_init": (C.c_int, [C.POINTER(kv_cache), C.POINTER(kv_layout), P, P, P, P, P]),
             "kv_quantize_append": (C.c_int, [P, P, I, I, C.POINTER(kv_cache), C.POINTER(kv_append_opts), P]),
@@ -143,10 +143,11 @@ def _stream(stream):
 
 # ----------------------------------------------------------------- calls ----
 
-def kv_layout_init(B, Hkv, d, kind, raw_dtype=KV_F16, cap_blocks=(0, 0, 0), psac_rank=0) -> kv_layout:
+def kv_layout_init(B, Hkv, d, kind, raw_dtype=KV_F16, cap_blocks=(0, 0, 0), psac_rank=0,
+                   meta_dtype=KV_F32) -> kv_layout:
     L = kv_layout()
     caps = (C.c_int32 * 3)(*cap_blocks)
-    _check(lib().kv_layout_init(C.byref(L), B, Hkv, d, kind, raw_dtype, caps, psac_rank))
+    _check(lib().kv_layout_init(C.byref(L), B, Hkv, d, kind, raw_dtype, caps, psac_rank, meta_dtype))
     return L
 
 
@@ -269,9 +270,10 @@ def torch_dtype_code(t):
 class TorchCache:
     """A cache whose regions are torch tensors on one CUDA device (allocation only)."""
 
-    def __init__(self, B, Hkv, d, kind, cap_blocks, raw_dtype=KV_F16, psac_rank=0, device="cuda", resid_var=False):
+    def __init__(self, B, Hkv, d, kind, cap_blocks, raw_dtype=KV_F16, psac_rank=0, device="cuda", resid_var=False,
+                 meta_dtype=KV_F32):
         import torch
-        self.layout = kv_layout_init(B, Hkv, d, kind, raw_dtype, cap_blocks, psac_rank)
+        self.layout = kv_layout_init(B, Hkv, d, kind, raw_dtype, cap_blocks, psac_rank, meta_dtype)
         nb = lambda r: kv_layout_bytes(self.layout, r)
         self.data = torch.zeros(nb(KV_REGION_DATA), dtype=torch.uint8, device=device)
         self.blk_len = torch.zeros(max(1, nb(KV_REGION_BLK_LEN) // 4), dtype=torch.int32, device=device)

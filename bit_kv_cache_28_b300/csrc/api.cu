@@ -105,11 +105,12 @@ kv_status set_smem_limit(const void* kernel, size_t bytes, const char* name) {
 
 static int ceil8(int r) { return (r + 7) / 8 * 8; }
 
-static long long block_bytes_of(int cls, int d, int r) {
+static long long block_bytes_of(int cls, int d, int r, int meta16) {
+    const long long pair = meta16 ? 4 : 8;    // bytes of one (s, z)
     switch (cls) {
         case CLS_RAW16: return 2LL * kBlockTokens * d * 2;
-        case CLS_INT4: return 2LL * (kBlockTokens * d * 4 / 8) + 8LL * d + 8LL * d;
-        case CLS_INT2: return 2LL * (kBlockTokens * d * 2 / 8) + 8LL * d + 8LL * d;
+        case CLS_INT4: return 2LL * (kBlockTokens * d * 4 / 8) + 2 * pair * d;
+        case CLS_INT2: return 2LL * (kBlockTokens * d * 2 / 8) + 2 * pair * d;
         case CLS_CB2: return 2LL * (kBlockTokens * d * 2 / 8) + 8LL * d + kBlockTokens * ceil8(r) * 2LL;
     }
     return 0;
@@ -131,6 +132,7 @@ DevCache make_dev_cache(const kv_cache* cc) {
     c.raw_dtype = L.raw_dtype;
     c.r = L.psac_rank;
     c.rp = ceil8(L.psac_rank);
+    c.meta16 = L.meta_dtype == KV_F16;
     c.cap_total = L.cap_blocks[0] + L.cap_blocks[1] + L.cap_blocks[2];
     int base = 0;
     for (int s = 0; s < KV_NUM_SEG; ++s) {
@@ -170,7 +172,7 @@ const char* kv_last_error(void) { return g_err.c_str(); }
 const char* kv_version(void) { return "bitkv 0.1 (sm_103a)"; }
 
 kv_status kv_layout_init(kv_layout* out, int B, int Hkv, int d, kv_kind kind, kv_dtype raw_dtype,
-                         const int32_t cap_blocks[KV_NUM_SEG], int psac_rank) {
+                         const int32_t cap_blocks[KV_NUM_SEG], int psac_rank, kv_dtype meta_dtype) {
     if (!out || !cap_blocks) return set_error(KV_ERR_INVALID_ARG, "layout or cap_blocks is NULL");
     if (B <= 0 || Hkv <= 0) return set_error(KV_ERR_INVALID_ARG, "B=%d Hkv=%d must be positive", B, Hkv);
     if (d <= 0 || d % 32 != 0 || d > 256) return set_error(KV_ERR_UNSUPPORTED, "d=%d must be a multiple of 32 <= 256", d);
@@ -179,6 +181,10 @@ kv_status kv_layout_init(kv_layout* out, int B, int Hkv, int d, kv_kind kind, kv
     if (kind != KV_CODEBOOK2 && psac_rank != 0) return set_error(KV_ERR_INVALID_ARG, "psac_rank needs a CODEBOOK2 cache");
     if (kind == KV_MIXED && raw_dtype != KV_F16 && raw_dtype != KV_BF16)
         return set_error(KV_ERR_INVALID_ARG, "MIXED caches store 16-bit windows: raw_dtype must be F16 or BF16");
+    if (meta_dtype != KV_F32 && meta_dtype != KV_F16)
+        return set_error(KV_ERR_INVALID_ARG, "meta_dtype must be KV_F32 or KV_F16");
+    if (meta_dtype == KV_F16 && kind == KV_CODEBOOK2)
+        return set_error(KV_ERR_UNSUPPORTED, "fp16 metadata is for UNIFORM2 / UNIFORM4 / MIXED caches");
     for (int s = 0; s < KV_NUM_SEG; ++s)
         if (cap_blocks[s] < 0) return set_error(KV_ERR_INVALID_ARG, "negative capacity");
     const bool used[3] = {kind == KV_MIXED, kind == KV_MIXED || kind == KV_UNIFORM4,
@@ -194,10 +200,11 @@ kv_status kv_layout_init(kv_layout* out, int B, int Hkv, int d, kv_kind kind, kv
     L.kind = kind;
     L.raw_dtype = raw_dtype;
     L.psac_rank = psac_rank;
+    L.meta_dtype = meta_dtype;
     long long off = 0;
     for (int s = 0; s < KV_NUM_SEG; ++s) {
         L.cap_blocks[s] = cap_blocks[s];
-        L.block_bytes[s] = block_bytes_of(seg_class(kind, s), d, psac_rank);
+        L.block_bytes[s] = block_bytes_of(seg_class(kind, s), d, psac_rank, meta_dtype == KV_F16);
         L.seg_offset[s] = off;
         off += (long long)cap_blocks[s] * L.block_bytes[s];
     }

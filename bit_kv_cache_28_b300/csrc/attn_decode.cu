@@ -18,8 +18,10 @@
 // and the per-token value step and zero into the probability side,
 // sum_t p_t v_hat_t = sum_t (p_t s_t) code_t + sum_t p_t z_t, so the B operands
 // are the raw codes, turned into exact fp16 integers three instructions per
-// pair (byte permute, mask-or of the fp16 exponent, fp16x2 FMA).  RAW16 blocks
-// are read with ldmatrix (their chunk-permuted rows are bank-conflict free).
+// pair (byte permute, mask-or of the fp16 exponent, fp16x2 FMA).  Blocks with fp16
+// metadata hold fp16 entries, fp16(code s + z): one more fp16x2 FMA forms them exactly
+// and they enter the MMAs directly (queries as fp16, the probabilities unscaled).
+// RAW16 blocks are read with ldmatrix (their chunk-permuted rows are bank-conflict free).
 // Products accumulate in fp32.  The Jensen term of "Quantized Keys Steal
 // Attention" (abstract) is a per-(block, head) scalar, sum_c q_c^2 s_c^2.
 // Current-chunk tokens run on CUDA cores.
@@ -206,11 +208,10 @@ __device__ __forceinline__ void online_softmax(DecState<D, NT>& st, float (&x)[N
 template <int D, int BITS, int NT, int JENSEN>
 __device__ __forceinline__ void int_block(const unsigned char* blk, int len, const LaneConst& lc,
                                           const float (&q)[NT][D / 4], float c1, float tau, DecState<D, NT>& st) {
-    const IntBlockOffsets o = int_offsets(D, BITS);
+    const IntBlockOffsets o = int_offsets(D, BITS, 0);
     // B = (q o s)^T as an fp16 pair hi + lo (hi = fp16(q s), lo = fp16(q s - hi):
     // the product keeps ~22 bits, enough for outlier channels with large steps),
     // the zero-point term q.z and the Jensen sum of head g + 8 nt
-    const float4* km4 = reinterpret_cast<const float4*>(blk + o.km);
     uint32_t bh[NT][D / 16][2], bl[NT][D / 16][2];
     float qz[NT], jd[NT];
     float ss2 = 0.0f;   // ISOTROPIC: sum_c s_c^2 (jd then holds |q|^2)
@@ -218,8 +219,8 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
     for (int nt = 0; nt < NT; ++nt) qz[nt] = jd[nt] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const float4 A = km4[(16 * kk + 2 * lc.tig) >> 1];
-        const float4 Bq = km4[(16 * kk + 8 + 2 * lc.tig) >> 1];
+        const float4 A = meta2_at<false>(blk + o.km, 16 * kk + 2 * lc.tig);
+        const float4 Bq = meta2_at<false>(blk + o.km, 16 * kk + 8 + 2 * lc.tig);
         const float s[4] = {A.x, A.z, Bq.x, Bq.z}, z[4] = {A.y, A.w, Bq.y, Bq.w};
         if (JENSEN == KV_JENSEN_ISOTROPIC) {
 #pragma unroll
@@ -312,7 +313,6 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
 
     // B = (p o s_v) per value group, transposed to [keys x heads] by movmatrix,
     // and the zero-point term sum p z_v
-    const float2* vm = reinterpret_cast<const float2*>(blk + o.vm);
     uint32_t bpv[D / 32][NT][2][2];
 #pragma unroll
     for (int vg = 0; vg < D / 32; ++vg)
@@ -320,7 +320,7 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const float2 sz = vm[vg * 32 + 16 * mt + 8 * r + lc.g];
+                const float2 sz = meta_at<false>(blk + o.vm, vg * 32 + 16 * mt + 8 * r + lc.g);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float p0 = p[nt][mt][2 * r], p1 = p[nt][mt][2 * r + 1];
@@ -355,6 +355,172 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
             for (int nt = 0; nt < NT; ++nt) mma_f16(st.o[cm][nt], a, bpv[vg][nt][kk][0], bpv[vg][nt][kk][1]);
         }
     }
+}
+
+// ---- one quantised block with fp16 metadata ---------------------------------------
+// The cache's entries are fp16 numbers, x_hat = fp16(code s + z) with one rounding, so
+// they are formed here exactly (fp16x2 FMA of the exact fp16 codes with the channel or
+// token (s, z) pairs) and enter the MMAs as they are: S^T = K_hat q^T with the queries as
+// fp16 (exact for fp16 I/O and for bf16 values in the fp16 normal range), and
+// O^T += V_hat^T p.  The Jensen sum still reads the key steps.
+template <int D, int BITS, int NT, int JENSEN>
+__device__ __forceinline__ void int_block_h(const unsigned char* blk, int len, const LaneConst& lc,
+                                            const float (&q)[NT][D / 4], float c1, float tau, DecState<D, NT>& st) {
+    const IntBlockOffsets o = int_offsets(D, BITS, 1);
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(blk + o.km);   // channel c: (s_c, z_c)
+    // per k-step: (s, s) and (z, z) of the lane's channel pairs 2 tig and 8 + 2 tig
+    uint32_t sp[D / 16][2], zp[D / 16][2];
+    uint32_t bq[NT][D / 16][2];
+    float jd[NT];
+    float ss2 = 0.0f;   // ISOTROPIC: sum_c s_c^2 (jd then holds |q|^2)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) jd[nt] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint2 m = *reinterpret_cast<const uint2*>(km + 16 * kk + 8 * hf + 2 * lc.tig);
+            sp[kk][hf] = __byte_perm(m.x, m.y, 0x5410);
+            zp[kk][hf] = __byte_perm(m.x, m.y, 0x7632);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            bq[nt][kk][0] = pack_f16(q[nt][4 * kk], q[nt][4 * kk + 1]);
+            bq[nt][kk][1] = pack_f16(q[nt][4 * kk + 2], q[nt][4 * kk + 3]);
+        }
+        if (JENSEN != KV_JENSEN_OFF) {
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sp[kk][0]));
+            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sp[kk][1]));
+            const float s[4] = {s01.x, s01.y, s23.x, s23.y};
+            if (JENSEN == KV_JENSEN_ISOTROPIC) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ss2 = fmaf(s[e], s[e], ss2);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float qs = q[nt][4 * kk + e] * s[e];
+                    if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs, qs, jd[nt]);
+                    else if (JENSEN == KV_JENSEN_EXACT) jd[nt] += log_sinhc(0.5f * tau * qs);
+                    else if (JENSEN == KV_JENSEN_ISOTROPIC) jd[nt] = fmaf(q[nt][4 * kk + e], q[nt][4 * kk + e], jd[nt]);
+                }
+        }
+    }
+    // the Jensen bias of head g + 8 nt, gathered for the fragment's heads 2 tig, 2 tig + 1
+    float bias[NT][2];
+    const float ms2 = JENSEN == KV_JENSEN_ISOTROPIC ? quad_sum(ss2) * (1.0f / D) : 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float dl = 0.0f;
+        if (JENSEN != KV_JENSEN_OFF) {
+            dl = quad_sum(jd[nt]);
+            if (JENSEN == KV_JENSEN_TAYLOR2) dl *= tau * tau * (1.0f / 24.0f);
+            else if (JENSEN == KV_JENSEN_ISOTROPIC) dl = tau * tau * (1.0f / 24.0f) * dl * ms2;
+        }
+        const float bq0 = -dl * kLog2e;
+        bias[nt][0] = __shfl_sync(0xffffffffu, bq0, (2 * lc.tig) << 2);
+        bias[nt][1] = __shfl_sync(0xffffffffu, bq0, (2 * lc.tig + 1) << 2);
+    }
+
+    constexpr int KW = D * BITS / 32;   // code words per key row
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
+    float acc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        uint32_t wa[KW], wb[KW];
+        const uint4* sa = reinterpret_cast<const uint4*>(kc + (16 * mt + lc.g) * KW);
+        const uint4* sb = reinterpret_cast<const uint4*>(kc + (16 * mt + 8 + lc.g) * KW);
+#pragma unroll
+        for (int i = 0; i < KW / 4; ++i) {
+            const uint4 va = sa[i], vb = sb[i];
+            wa[4 * i] = va.x; wa[4 * i + 1] = va.y; wa[4 * i + 2] = va.z; wa[4 * i + 3] = va.w;
+            wb[4 * i] = vb.x; wb[4 * i + 1] = vb.y; wb[4 * i + 2] = vb.z; wb[4 * i + 3] = vb.w;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4];
+            if (BITS == 2) {
+                a[0] = code_pair(wa[kk], lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[1] = code_pair(wb[kk], lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                a[2] = code_pair(wa[kk], lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                a[3] = code_pair(wb[kk], lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+            } else {
+                a[0] = code_pair(wa[2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[1] = code_pair(wb[2 * kk], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[2] = code_pair(wa[2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                a[3] = code_pair(wb[2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+            }
+            a[0] = hfma2_u32(a[0], sp[kk][0], zp[kk][0]);
+            a[1] = hfma2_u32(a[1], sp[kk][0], zp[kk][0]);
+            a[2] = hfma2_u32(a[2], sp[kk][1], zp[kk][1]);
+            a[3] = hfma2_u32(a[3], sp[kk][1], zp[kk][1]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[mt][nt], a, bq[nt][kk][0], bq[nt][kk][1]);
+        }
+    }
+    float x[NT][2][4], p[NT][2][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = 16 * mt + 8 * (e >> 1) + lc.g < len;
+                x[nt][mt][e] = valid ? fmaf(acc[mt][nt][e], c1, bias[nt][e & 1]) : -INFINITY;
+            }
+    online_softmax<D, NT>(st, x, p);
+
+    // B = p transposed to [keys x heads] by movmatrix (pad keys: p = 0)
+    uint32_t bp[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) bp[nt][mt][r] = movmatrix_t(pack_f16(p[nt][mt][2 * r], p[nt][mt][2 * r + 1]));
+    // O^T += V_hat [16 channels x 16 keys] p: tokens 16 kk + 2 tig (+ 8) of value group vg
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + o.vc);
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(blk + o.vm);   // (group, token): (s, z)
+#pragma unroll
+    for (int vg = 0; vg < D / 32; ++vg)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t vs[2], vz[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint2 m = *reinterpret_cast<const uint2*>(vm + vg * 32 + 16 * kk + 8 * hf + 2 * lc.tig);
+                vs[hf] = __byte_perm(m.x, m.y, 0x5410);
+                vz[hf] = __byte_perm(m.x, m.y, 0x7632);
+            }
+#pragma unroll
+            for (int cm = 2 * vg; cm < 2 * vg + 2; ++cm) {
+                const int ca = 16 * cm + lc.g, cb = ca + 8;
+                uint32_t a[4];
+                if (BITS == 2) {
+                    const uint32_t wa = vc[ca * 2 + kk], wb = vc[cb * 2 + kk];
+                    a[0] = code_pair(wa, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                    a[1] = code_pair(wb, lc.sel2a, lc.mask2, lc.scale2, lc.bias2);
+                    a[2] = code_pair(wa, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                    a[3] = code_pair(wb, lc.sel2b, lc.mask2, lc.scale2, lc.bias2);
+                } else {
+                    const uint2 wa = *reinterpret_cast<const uint2*>(vc + ca * 4 + 2 * kk);
+                    const uint2 wb = *reinterpret_cast<const uint2*>(vc + cb * 4 + 2 * kk);
+                    a[0] = code_pair(wa.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                    a[1] = code_pair(wb.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                    a[2] = code_pair(wa.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                    a[3] = code_pair(wb.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+                }
+                a[0] = hfma2_u32(a[0], vs[0], vz[0]);
+                a[1] = hfma2_u32(a[1], vs[0], vz[0]);
+                a[2] = hfma2_u32(a[2], vs[1], vz[1]);
+                a[3] = hfma2_u32(a[3], vs[1], vz[1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16(st.o[cm][nt], a, bp[nt][kk][0], bp[nt][kk][1]);
+            }
+        }
 }
 
 // ---- one RAW16 block (16-bit K and V kept as given) ------------------------------
@@ -469,7 +635,7 @@ struct DecShape {
     int rows;         // merge rows per warp (8 or 16)
 };
 
-template <typename T, int D, int NT, int JENSEN>
+template <typename T, int D, int NT, int JENSEN, bool M16>
 __global__ void __launch_bounds__(kDThreads, (D == 64 && NT == 1) ? 4 : ((D == 128 && NT == 2) ? 1 : 2))
 attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* __restrict__ Vcur, int n_cur, int Hq,
                    DevCache c, float tau, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
@@ -523,6 +689,15 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
             aq[nt][kk][0] = wa;
             aq[nt][kk][1] = wb;
         }
+    }
+    if constexpr (M16 && !std::is_same<T, __half>::value) {
+        // fp16-metadata blocks take the queries as fp16: flag any beyond its range
+        bool bad = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < D / 4; ++e) bad |= !(fabsf(q[nt][e]) < 65520.0f);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(err + 1, 1);
     }
     const float c1 = tau * kLog2e;
 
@@ -579,7 +754,9 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
         const int len = __shfl_sync(0xffffffffu, len_next, k & 31);
         const unsigned char* blk = slots + (warp * nsw + k % nsw) * slot_bytes;
         const int cls = seg_class(c.kind, seg);
-        if (cls == CLS_INT2) int_block<D, 2, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
+        if (M16 && cls == CLS_INT2) int_block_h<D, 2, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
+        else if (M16 && cls == CLS_INT4) int_block_h<D, 4, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
+        else if (cls == CLS_INT2) int_block<D, 2, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
         else if (cls == CLS_INT4) int_block<D, 4, NT, JENSEN>(blk, len, lc, q, c1, tau, st);
         else raw_block<T, D, NT>(smem_u32(blk), len, lc, aq, c1, st);
         __syncwarp();
@@ -820,14 +997,16 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
 }
 
 // ------------------------------------------------------- operand dump -----
-// Debug view of this kernel's own operands.  The kernel forms no dequantised key
-// or value: the B/A operands of its quantised-block MMAs are the integer codes,
+// Debug view of this kernel's own operands.  With fp32 metadata the kernel forms no
+// dequantised key or value: the B/A operands of its quantised-block MMAs are the codes,
 // turned into exact fp16 values by code_pair() with the lane constants above, and
-// the steps and zeros enter through the query and probability sides.  This kernel
-// runs that same extraction, per warp one block, on the block's code words in
-// global memory, and writes every fragment's fp16 codes at their (token, channel)
-// place: Kout/Vout fp16 [B][Hkv][32 n_total][d] in stream slot order (all segments'
-// blocks in memory order).  RAW16 slots are not written (they enter as stored).
+// the steps and zeros enter through the query and probability sides; with fp16
+// metadata the operands are the fp16 entries, one fp16x2 FMA of those codes with the
+// (s, z) pairs.  This kernel runs that same extraction, per warp one block, on the
+// block's words in global memory, and writes every fragment's fp16 values at their
+// (token, channel) place: Kout/Vout fp16 [B][Hkv][32 n_total][d] in stream slot order
+// (all segments' blocks in memory order).  RAW16 slots are not written (they enter as
+// stored).
 template <int D, int BITS>
 __global__ void __launch_bounds__(32)
 dec_operands_kernel(DevCache c, int seg, int slot0, int n_total, __half* __restrict__ Kout,
@@ -835,7 +1014,7 @@ dec_operands_kernel(DevCache c, int seg, int slot0, int n_total, __half* __restr
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, lane = threadIdx.x;
     const LaneConst lc = lane_const(lane);
     const unsigned char* blk = block_ptr(c, b, h, seg, i);
-    const IntBlockOffsets o = int_offsets(D, BITS);
+    const IntBlockOffsets o = int_offsets(D, BITS, c.meta16);
     const long long base = (((long long)b * c.Hkv + h) * n_total + slot0 + i) * kBlockTokens;
     auto put = [&](__half* out, int tok, int ch, uint32_t pair) {
         *reinterpret_cast<uint32_t*>(out + (base + tok) * D + ch) = pair;
@@ -866,6 +1045,15 @@ dec_operands_kernel(DevCache c, int seg, int slot0, int n_total, __half* __restr
                 a[2] = code_pair(kc[ka * KW + 2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
                 a[3] = code_pair(kc[kb * KW + 2 * kk + 1], lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
             }
+            if (c.meta16) {   // fp16 metadata: the kernel's operands are the entries themselves
+                const uint32_t* km = reinterpret_cast<const uint32_t*>(blk + o.km);
+                const uint2 m0 = *reinterpret_cast<const uint2*>(km + c0);
+                const uint2 m1 = *reinterpret_cast<const uint2*>(km + c0 + 8);
+                a[0] = hfma2_u32(a[0], __byte_perm(m0.x, m0.y, 0x5410), __byte_perm(m0.x, m0.y, 0x7632));
+                a[1] = hfma2_u32(a[1], __byte_perm(m0.x, m0.y, 0x5410), __byte_perm(m0.x, m0.y, 0x7632));
+                a[2] = hfma2_u32(a[2], __byte_perm(m1.x, m1.y, 0x5410), __byte_perm(m1.x, m1.y, 0x7632));
+                a[3] = hfma2_u32(a[3], __byte_perm(m1.x, m1.y, 0x5410), __byte_perm(m1.x, m1.y, 0x7632));
+            }
             // m16n8k16 A fragment: rows (keys) g, g + 8; columns (channels) 2 tig, 2 tig + 8
             put(Kout, ka, c0, a[0]);
             put(Kout, kb, c0, a[1]);
@@ -894,6 +1082,15 @@ dec_operands_kernel(DevCache c, int seg, int slot0, int n_total, __half* __restr
                 a[1] = code_pair(wb.x, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
                 a[2] = code_pair(wa.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
                 a[3] = code_pair(wb.y, lc.sel4, 0x00F0000Fu, lc.scale4, lc.bias4);
+            }
+            if (c.meta16) {
+                const uint32_t* vm = reinterpret_cast<const uint32_t*>(blk + o.vm) + (cm >> 1) * 32;
+                const uint2 m0 = *reinterpret_cast<const uint2*>(vm + t0);
+                const uint2 m1 = *reinterpret_cast<const uint2*>(vm + t0 + 8);
+                a[0] = hfma2_u32(a[0], __byte_perm(m0.x, m0.y, 0x5410), __byte_perm(m0.x, m0.y, 0x7632));
+                a[1] = hfma2_u32(a[1], __byte_perm(m0.x, m0.y, 0x5410), __byte_perm(m0.x, m0.y, 0x7632));
+                a[2] = hfma2_u32(a[2], __byte_perm(m1.x, m1.y, 0x5410), __byte_perm(m1.x, m1.y, 0x7632));
+                a[3] = hfma2_u32(a[3], __byte_perm(m1.x, m1.y, 0x5410), __byte_perm(m1.x, m1.y, 0x7632));
             }
             // rows (channels) g, g + 8; columns (tokens) 2 tig, 2 tig + 8
             put_t(Vout, ca, t0, a[0]);
@@ -960,13 +1157,13 @@ size_t dec_ticket_bytes(const kv_cache* cache) {
     return ((size_t)cache->layout.B * cache->layout.Hkv * sizeof(int) + 255) / 256 * 256;
 }
 
-template <typename T, int D, int NT, int JENSEN>
+template <typename T, int D, int NT, int JENSEN, bool M16>
 kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur, int Hq, const kv_cache* cache,
                        float tau, int n_splits, void* out, int out_f32, float* lse, void* ws, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     const DecShape sh = dec_shape(cache, Hq);
     const size_t smem = dec_smem_bytes(sh, D);
-    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(attn_decode_kernel<T, D, NT, JENSEN>), smem,
+    const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(attn_decode_kernel<T, D, NT, JENSEN, M16>), smem,
                                         "attn_decode_kernel");
     if (sa != KV_OK) return sa;
     unsigned char* w = static_cast<unsigned char*>(ws);
@@ -977,7 +1174,7 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     const kv_status sc = clear_device(w, kStatusBytes + dec_ticket_bytes(cache), st, "attn_decode_kernel");
     if (sc != KV_OK) return sc;
     dim3 grid(n_splits, c.Hkv, c.B);
-    attn_decode_kernel<T, D, NT, JENSEN><<<grid, kDThreads, smem, st>>>(
+    attn_decode_kernel<T, D, NT, JENSEN, M16><<<grid, kDThreads, smem, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
         sh, out, out_f32, lse, part, tickets, err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
     return check_launch("attn_decode_kernel");
@@ -1022,21 +1219,27 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
                              float* lse, void* ws, cudaStream_t st) {
     const int d = cache->layout.d;
     const bool two = Hq / cache->layout.Hkv > 8;
+    const bool m16 = cache->layout.meta_dtype == KV_F16;
     using F16 = __half;
     using BF16 = __nv_bfloat16;
-#define BITKV_DEC(T, D, NT)                                                                                    \
+#define BITKV_DEC_M(T, D, NT, M16)                                                                             \
     do {                                                                                                        \
         if (jensen == KV_JENSEN_TAYLOR2)                                                                        \
-            return launch_dec_t<T, D, NT, KV_JENSEN_TAYLOR2>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,  \
-                                                              out_f32, lse, ws, st);                            \
+            return launch_dec_t<T, D, NT, KV_JENSEN_TAYLOR2, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, \
+                                                                   out, out_f32, lse, ws, st);                  \
         if (jensen == KV_JENSEN_EXACT)                                                                          \
-            return launch_dec_t<T, D, NT, KV_JENSEN_EXACT>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
-                                                            out_f32, lse, ws, st);                              \
+            return launch_dec_t<T, D, NT, KV_JENSEN_EXACT, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits,   \
+                                                                 out, out_f32, lse, ws, st);                    \
         if (jensen == KV_JENSEN_ISOTROPIC)                                                                      \
-            return launch_dec_t<T, D, NT, KV_JENSEN_ISOTROPIC>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits,     \
-                                                                out, out_f32, lse, ws, st);                     \
-        return launch_dec_t<T, D, NT, KV_JENSEN_OFF>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out, out_f32, \
-                                                      lse, ws, st);                                             \
+            return launch_dec_t<T, D, NT, KV_JENSEN_ISOTROPIC, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau,         \
+                                                                     n_splits, out, out_f32, lse, ws, st);      \
+        return launch_dec_t<T, D, NT, KV_JENSEN_OFF, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
+                                                           out_f32, lse, ws, st);                               \
+    } while (0)
+#define BITKV_DEC(T, D, NT)                                                                                    \
+    do {                                                                                                        \
+        if (m16) BITKV_DEC_M(T, D, NT, true);                                                                   \
+        BITKV_DEC_M(T, D, NT, false);                                                                           \
     } while (0)
     if (dt == KV_F16) {
         if (d == 64) { if (two) BITKV_DEC(F16, 64, 2); else BITKV_DEC(F16, 64, 1); }
@@ -1046,6 +1249,7 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
         else { if (two) BITKV_DEC(BF16, 128, 2); else BITKV_DEC(BF16, 128, 1); }
     }
 #undef BITKV_DEC
+#undef BITKV_DEC_M
 }
 
 kv_status launch_dec_operands(const kv_cache* cache, void* Kout, void* Vout, cudaStream_t st) {

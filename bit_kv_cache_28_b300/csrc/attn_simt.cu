@@ -133,14 +133,15 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
             const int cls = seg_class(c.kind, seg);
             for (int e = tid; e < kSK * D; e += kSimtThreads) {
                 const int t = e / D, ch = e % D;
-                const float2 kv = t < len ? block_entry(cls, blk, D, c.raw_dtype, cent, t, ch) : make_float2(0.f, 0.f);
+                const float2 kv =
+                    t < len ? block_entry(cls, blk, D, c.raw_dtype, c.meta16, cent, t, ch) : make_float2(0.f, 0.f);
                 Ks[t * ld + ch] = kv.x;     // the exact dequantised entries
                 Vs[t * ld + ch] = kv.y;
             }
             if (cls == CLS_INT2 || cls == CLS_INT4) {
                 quantised = 1;
-                const float2* km = reinterpret_cast<const float2*>(blk + int_offsets(D, cls == CLS_INT4 ? 4 : 2).km);
-                for (int ch = tid; ch < D; ch += kSimtThreads) Sk[ch] = km[ch].x;
+                const unsigned char* km = blk + int_offsets(D, cls == CLS_INT4 ? 4 : 2, c.meta16).km;
+                for (int ch = tid; ch < D; ch += kSimtThreads) Sk[ch] = meta_at(km, ch, c.meta16).x;
             }
             codebook = cls == CLS_CB2;
             if (cls == CLS_CB2 && r > 0) {

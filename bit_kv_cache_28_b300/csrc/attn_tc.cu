@@ -107,18 +107,25 @@ template <bool PAIR> struct Geo {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Cache block formats the kernel reads (one template instance each).
-enum { FMT_INT2 = 0, FMT_INT4 = 1, FMT_CB2 = 2 };
-template <int FMT> constexpr int vbits() { return FMT == FMT_INT4 ? 4 : 2; }
+// Cache block formats the kernel reads (one template instance each): INT2 / INT4 with
+// fp32 (s, z) pairs, the same with fp16 pairs (H), and codebook blocks.
+enum { FMT_INT2 = 0, FMT_INT4 = 1, FMT_CB2 = 2, FMT_INT2H = 3, FMT_INT4H = 4 };
+template <int FMT> constexpr int vbits() { return (FMT == FMT_INT4 || FMT == FMT_INT4H) ? 4 : 2; }
+template <int FMT> constexpr bool meta_h() { return FMT == FMT_INT2H || FMT == FMT_INT4H; }
+template <int FMT> constexpr int pair_bytes() { return meta_h<FMT>() ? 4 : 8; }   // one (s, z)
 // bytes of one block (CB2: the largest, PSAC rank 32; the actual stride is the layout's)
 template <int FMT> constexpr int max_block_bytes() {
-    return FMT == FMT_CB2 ? 24 * kD + kBlockTokens * 32 * 2 : 8 * kD * vbits<FMT>() + 16 * kD;
+    return FMT == FMT_CB2 ? 24 * kD + kBlockTokens * 32 * 2 : 8 * kD * vbits<FMT>() + 2 * pair_bytes<FMT>() * kD;
 }
-// byte offsets of the value codes and the value (step, zero) pairs inside a block
-template <int FMT> constexpr int voff_codes() { return FMT == FMT_CB2 ? 8 * kD : 4 * kD * vbits<FMT>() + 8 * kD; }
+// byte offsets of the key (step, zero) pairs, the value codes and the value pairs inside a block
+template <int FMT> constexpr int koff_meta() { return 4 * kD * vbits<FMT>(); }
+template <int FMT> constexpr int voff_codes() {
+    return FMT == FMT_CB2 ? 8 * kD : koff_meta<FMT>() + pair_bytes<FMT>() * kD;
+}
 template <int FMT> constexpr int voff_meta() {
     return FMT == FMT_CB2 ? 16 * kD : voff_codes<FMT>() + 4 * kD * vbits<FMT>();
 }
+template <int FMT> constexpr int seg_of() { return vbits<FMT>() == 4 ? KV_SEG_INT4 : KV_SEG_INT2; }
 constexpr int kCbCoeffOff = 24 * kD;        // CB2: fp16 PSAC coefficients [32][rp]
 
 constexpr int kTile = kM * kD * 2;          // 32 KB: one 16-bit 128 x 128 operand tile
@@ -223,8 +230,10 @@ __device__ __forceinline__ void dequant2(float& v0, float& v1, float m0, float m
 // K-major along the 128 keys).  Single CTA: warp pw expands value group g = pw & 3
 // (channels 32 g .. 32 g + 31, one per lane) of blocks 2 (pw >> 2) and 2 (pw >> 2) + 1.
 // CTA pair of rank r: channels 64 r .. 64 r + 63, warp pw takes group 2 r + (pw & 1) of
-// block pw >> 1.  The group's per-token steps are first pre-scaled in the staging copy
-// by 2^(-b i), i = the token's slot in its half word.
+// block pw >> 1.  fp32 pairs: the group's per-token steps are first pre-scaled in the
+// staging copy by 2^(-b i), i = the token's slot in its half word, and each entry is one
+// fp32 FMA rounded to fp16.  fp16 pairs: each token pair is one fp16x2 FMA of the exact
+// fp16 codes with the tokens' (s, s) and (z, z) pairs -- the entries themselves.
 template <int FMT, bool PAIR>
 __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned char* stg, int stride, int nb, int pw,
                                                   int lane, int rank) {
@@ -240,6 +249,27 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned ch
         const int q = qb + k2;
         if (q < nb) {
             unsigned char* blk = stg + q * stride;
+            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + voff_codes<FMT>()) + c * BITS;
+            if constexpr (meta_h<FMT>()) {
+                uint32_t w[BITS];
+#pragma unroll
+                for (int k = 0; k < BITS; ++k) w[k] = vc[k];
+                const uint32_t* vm = reinterpret_cast<const uint32_t*>(blk + voff_meta<FMT>()) + g * 32;
+#pragma unroll
+                for (int k8 = 0; k8 < 4; ++k8) {     // tokens 8 k8 .. 8 k8 + 7
+                    uint32_t h[4];
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int t = 8 * k8 + i;
+                        const uint2 mm = *reinterpret_cast<const uint2*>(vm + t);   // (s, z) of t and t + 1
+                        const uint32_t cp = BITS == 2 ? code_pair_f16<2>(w[t >> 4], t & 15)
+                                                      : code_pair_f16<4>(w[t >> 3], t & 7);
+                        h[i >> 1] = hfma2_u32(cp, __byte_perm(mm.x, mm.y, 0x5410), __byte_perm(mm.x, mm.y, 0x7632));
+                    }
+                    *reinterpret_cast<uint4*>(Vt + sw_off(row, 4 * q + k8, kRows)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+                continue;
+            }
             float* vm = reinterpret_cast<float*>(blk + voff_meta<FMT>()) + g * 64;
             // token t's (s, z) -> (s 2^(-b slot), z), stored per token pair as
             // (s'_t, s'_t+1, z_t, z_t+1) so that pairs load into adjacent registers
@@ -248,7 +278,6 @@ __device__ __forceinline__ void fill_cache_values(unsigned char* Vt, unsigned ch
             vm[4 * (lane >> 1) + (lane & 1)] = e.x * pow2i(-BITS * (lane % kSlots));
             vm[4 * (lane >> 1) + 2 + (lane & 1)] = e.y;
             __syncwarp();
-            const uint32_t* vc = reinterpret_cast<const uint32_t*>(blk + voff_codes<FMT>()) + c * BITS;
             uint32_t w[BITS];
 #pragma unroll
             for (int k = 0; k < BITS; ++k) w[k] = vc[k];
@@ -298,10 +327,10 @@ __device__ __forceinline__ void key_rows(int p, int rank, int* q, int* t0, int* 
     }
 }
 
-template <int BITS, bool PAIR>
+template <int FMT, bool PAIR>
 __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigned char* stg, int nb, int p, int rank) {
+    constexpr int BITS = vbits<FMT>();
     constexpr int NR = PAIR ? 4 : 8, kRows = Geo<PAIR>::kNK;
-    const IntBlockOffsets o = int_offsets(kD, BITS);
     const int jc = p & 15;
     int q, t0, row0;
     key_rows<PAIR>(p, rank, &q, &t0, &row0);
@@ -310,13 +339,38 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigne
         for (int r = 0; r < NR; ++r) *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = make_uint4(0, 0, 0, 0);
         return;
     }
-    const unsigned char* blk = stg + q * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>();
+    const unsigned char* blk = stg + q * max_block_bytes<FMT>();
+    constexpr int KW = kD * BITS / 32;   // code words per key
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk);
+    if constexpr (meta_h<FMT>()) {
+        // fp16 pairs: channel pairs' (s, s) and (z, z), then one fp16x2 FMA per entry pair
+        const uint4* km = reinterpret_cast<const uint4*>(blk + koff_meta<FMT>()) + 2 * jc;
+        const uint4 m0 = km[0], m1 = km[1];
+        const uint32_t m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        uint32_t sp[4], zp[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sp[i] = __byte_perm(m[2 * i], m[2 * i + 1], 0x5410);
+            zp[i] = __byte_perm(m[2 * i], m[2 * i + 1], 0x7632);
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const int t = t0 + r;
+            const uint32_t x = BITS == 2 ? kc[t * KW + (jc >> 1)] >> (16 * (jc & 1)) : kc[t * KW + jc];
+            uint4 rr;
+            rr.x = hfma2_u32(code_pair_f16<BITS>(x, 0), sp[0], zp[0]);
+            rr.y = hfma2_u32(code_pair_f16<BITS>(x, 2), sp[1], zp[1]);
+            rr.z = hfma2_u32(code_pair_f16<BITS>(x, 4), sp[2], zp[2]);
+            rr.w = hfma2_u32(code_pair_f16<BITS>(x, 6), sp[3], zp[3]);
+            *reinterpret_cast<uint4*>(Kt + sw_off(row0 + r, jc, kRows)) = rr;
+        }
+        return;
+    }
     constexpr int kSlots = 16 / BITS;
-    const float4* km4 = reinterpret_cast<const float4*>(blk + o.km) + jc * 4;
     float s[8], z[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float4 v = km4[k];
+        const float4 v = meta2_at<meta_h<FMT>()>(blk + koff_meta<FMT>(), 8 * jc + 2 * k);
         s[2 * k] = v.x;
         z[2 * k] = v.y;
         s[2 * k + 1] = v.z;
@@ -324,8 +378,6 @@ __device__ __forceinline__ void fill_cache_keys(unsigned char* Kt, const unsigne
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i] *= pow2i(-BITS * (i % kSlots));
-    constexpr int KW = kD * BITS / 32;   // code words per key
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(blk + o.kc);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         const int t = t0 + r;
@@ -442,15 +494,13 @@ __device__ __forceinline__ void fill_coeff(unsigned char* Ct, const unsigned cha
 // other rows stay zero (`wrows` rows in the tile).  EXACT: the block steps s_c as fp32 [4][128].
 // ISOTROPIC: the two warps of block g each sum s_c^2 over their 64 channels into
 // ss2[g][w] (the softmax adds the two in a fixed order).
-template <int BITS, int JENSEN>
+template <int FMT, int JENSEN>
 __device__ __forceinline__ void fill_weights(unsigned char* W, const unsigned char* stg, int nb, int p, float coef,
                                              int wrows, float (*ss2)[2] = nullptr) {
-    const IntBlockOffsets o = int_offsets(kD, BITS);
     const int g = p >> 6, c = 2 * (p & 63);
     float2 s = make_float2(0.0f, 0.0f);
     if (g < nb) {
-        const float4 v = *reinterpret_cast<const float4*>(stg + g * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>() +
-                                                          o.km + c * 8);
+        const float4 v = meta2_at<meta_h<FMT>()>(stg + g * max_block_bytes<FMT>() + koff_meta<FMT>(), c);
         s = make_float2(v.x, v.z);
     }
     if (JENSEN == KV_JENSEN_TAYLOR2) {
@@ -533,14 +583,12 @@ __device__ __forceinline__ bool fill_current_keys(unsigned char* Kt, const __nv_
 // The cached keys of a staged INT tile stay inside the fp16 range: every entry of a
 // (block, channel) lies between z and fmaf(2^b - 1, s, z), so checking those two
 // bounds for each of the thread's two channels covers the tile.
-template <int BITS>
+template <int FMT>
 __device__ __forceinline__ bool cache_keys_in_f16_range(const unsigned char* stg, int nb, int p) {
     const int g = p >> 6, c = 2 * (p & 63);
     if (g >= nb) return true;
-    const IntBlockOffsets o = int_offsets(kD, BITS);
-    const float4 v = *reinterpret_cast<const float4*>(stg + g * max_block_bytes<BITS == 4 ? FMT_INT4 : FMT_INT2>() +
-                                                      o.km + c * 8);
-    constexpr float kTop = (float)((1 << BITS) - 1);
+    const float4 v = meta2_at<meta_h<FMT>()>(stg + g * max_block_bytes<FMT>() + koff_meta<FMT>(), c);
+    constexpr float kTop = (float)((1 << vbits<FMT>()) - 1);
     return f16_finite(v.y) && f16_finite(fmaf(kTop, v.x, v.y)) && f16_finite(v.w) && f16_finite(fmaf(kTop, v.z, v.w));
 }
 
@@ -570,7 +618,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     const int hq = blockIdx.y, b = blockIdx.z;
     const int h = hq / (Hq / c.Hkv);
     const int q0 = qt * kM;
-    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int seg = seg_of<FMT>();
     // staging stride of one block (a CB2 block's size depends on the PSAC rank)
     const int bb = kCb ? (int)c.block_bytes[seg] : max_block_bytes<FMT>();
     const int n_cache_tiles = (c.n_blocks[seg] + 3) / 4;
@@ -940,18 +988,18 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 fill_cb_keys<PAIR>(Kt, stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p, rank);
                 if (r16 > 0) fill_coeff<PAIR>(Ct, stg, bb, nb, c.rp, r16 / 8, p, rank);
             } else if (cached) {
-                fill_cache_keys<vbits<FMT>(), PAIR>(Kt, stg, nb, p, rank);
-                if (!cache_keys_in_f16_range<vbits<FMT>()>(stg, nb, p)) atomicExch(err + 1, 1);
+                fill_cache_keys<FMT, PAIR>(Kt, stg, nb, p, rank);
+                if (!cache_keys_in_f16_range<FMT>(stg, nb, p)) atomicExch(err + 1, 1);
                 // TAYLOR2: bf16 weights read by the Jensen MMA with Q K^T (stage s, free
                 // since Q K^T of tile j - 2 completed; in a pair the even CTA holds the
                 // weight rows, the odd CTA's rows stay zero); EXACT: fp32 steps read by the
                 // softmax, in a ring of 4 like the tile info
                 if (JENSEN == KV_JENSEN_TAYLOR2) {
-                    if (rank == 0) fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef, G::kWR);
+                    if (rank == 0) fill_weights<FMT, JENSEN>(sm + M::w + s * kWBytes, stg, nb, p, jcoef, G::kWR);
                 } else if (JENSEN == KV_JENSEN_EXACT) {
-                    fill_weights<vbits<FMT>(), JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef, G::kWR);
+                    fill_weights<FMT, JENSEN>(sm + M::w + (j & 3) * kExactW, stg, nb, p, jcoef, G::kWR);
                 } else if (JENSEN == KV_JENSEN_ISOTROPIC) {
-                    fill_weights<vbits<FMT>(), JENSEN>(nullptr, stg, nb, p, jcoef, G::kWR, inf.ss2);
+                    fill_weights<FMT, JENSEN>(nullptr, stg, nb, p, jcoef, G::kWR, inf.ss2);
                 }
             } else {
                 if (!fill_current_keys<PAIR>(Kt, Kcur, row0, cvalid, p, rank)) atomicExch(err + 1, 1);
@@ -1231,7 +1279,7 @@ tc_operands_kernel(DevCache c, __half* __restrict__ Kout, __half* __restrict__ V
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int p = threadIdx.x, pw = p >> 5, lane = p & 31;
     const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int seg = seg_of<FMT>();
     const int nblk = c.n_blocks[seg];
     const int nb = min(4, nblk - tile * 4);
     if (nb <= 0) return;
@@ -1245,7 +1293,7 @@ tc_operands_kernel(DevCache c, __half* __restrict__ Kout, __half* __restrict__ V
     __syncthreads();
     // keys first, then values (the value routine rescales the staged steps in place)
     if (kCb) fill_cb_keys<false>(sm + M::k, sm + M::stg, bb, nb, reinterpret_cast<const uint32_t*>(sm + M::cent), p, 0);
-    else fill_cache_keys<vbits<FMT>(), false>(sm + M::k, sm + M::stg, nb, p, 0);
+    else fill_cache_keys<FMT, false>(sm + M::k, sm + M::stg, nb, p, 0);
     __syncthreads();
     fill_cache_values<FMT, false>(sm + M::v, sm + M::stg, bb, nb, pw, lane, 0);
     __syncthreads();
@@ -1268,7 +1316,7 @@ kv_status launch_tc_operands_t(const DevCache& c, void* Kout, void* Vout, cudaSt
     const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(tc_operands_kernel<FMT>), kSmem,
                                         "tc_operands_kernel");
     if (sa != KV_OK) return sa;
-    const int seg = FMT == FMT_INT4 ? KV_SEG_INT4 : KV_SEG_INT2;
+    const int seg = seg_of<FMT>();
     const int tiles = (c.n_blocks[seg] + 3) / 4;
     if (tiles == 0) return KV_OK;
     tc_operands_kernel<FMT><<<dim3(tiles, c.Hkv, c.B), kProd, kSmem, st>>>(c, static_cast<__half*>(Kout),
@@ -1426,7 +1474,13 @@ kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q,
             s = launch_tc_t<FMT_CB2, KV_JENSEN_OFF>(c, Q, Kc, Vc, n_q, n_cur, Hq, tau, r16, n_splits, out, out_f32,
                                                     lse, ws_o, ws_ml, err, pair, st);
     } else if (c.kind == KV_UNIFORM4) {
-        BITKV_TC(FMT_INT4)
+        if (c.meta16) {
+            BITKV_TC(FMT_INT4H)
+        } else {
+            BITKV_TC(FMT_INT4)
+        }
+    } else if (c.meta16) {
+        BITKV_TC(FMT_INT2H)
     } else {
         BITKV_TC(FMT_INT2)
     }
@@ -1440,8 +1494,12 @@ kv_status launch_tc_operands(const kv_cache* cache, void* Kout, void* Vout, cuda
     const DevCache c = make_dev_cache(cache);
     if (c.d != kD) return set_error(KV_ERR_UNSUPPORTED, "tensor-core operands: needs head dim 128");
     if (c.kind == KV_CODEBOOK2) return launch_tc_operands_t<FMT_CB2>(c, Kout, Vout, st);
-    if (c.kind == KV_UNIFORM4) return launch_tc_operands_t<FMT_INT4>(c, Kout, Vout, st);
-    if (c.kind == KV_UNIFORM2) return launch_tc_operands_t<FMT_INT2>(c, Kout, Vout, st);
+    if (c.kind == KV_UNIFORM4)
+        return c.meta16 ? launch_tc_operands_t<FMT_INT4H>(c, Kout, Vout, st)
+                        : launch_tc_operands_t<FMT_INT4>(c, Kout, Vout, st);
+    if (c.kind == KV_UNIFORM2)
+        return c.meta16 ? launch_tc_operands_t<FMT_INT2H>(c, Kout, Vout, st)
+                        : launch_tc_operands_t<FMT_INT2>(c, Kout, Vout, st);
     return set_error(KV_ERR_UNSUPPORTED, "tensor-core operands: needs a UNIFORM2, UNIFORM4 or CODEBOOK2 cache");
 }
 

@@ -7,10 +7,14 @@
 //   RAW16:              K 16-bit[32][d] | V 16-bit[32][d], 16-byte chunk j of row t
 //                       stored at chunk position j ^ (t mod min(8, d/8))
 //   CODEBOOK2:          Kc u32[32][d/16] | Vc u32[d][2] | Vm float2[d/32][32] | Kq fp16[32][rp]
+// fp16-metadata layouts store Km as half2[d] and Vm as half2[d/32][32] (INT blocks only).
 // Quantiser (step sizes of "Quantized Keys Steal Attention", abstract; INT2/INT4
 // of the WindowQuant note, table in 何が新しいのか):
 //   s = fl32(fl32(M-m)/(2^b-1)), code = clamp(rint(fl32(fl32(x-m)/s))), z = m,
 //   x_hat = fmaf(code, s, z).
+// With fp16 metadata s and z are first rounded to fp16 (a -0 zero point as +0), the
+// codes are taken against the rounded pair, and x_hat = fp16(code * s + z) with one
+// rounding (an fp16 FMA).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,6 +39,7 @@ struct DevCache {
     const float* psac_u;
     const float* resid_var;        // CODEBOOK2 residual variances [B][Hkv][d], or NULL
     int B, Hkv, d, kind, raw_dtype, r, rp;
+    int meta16;                    // INT blocks store (s, z) as fp16 pairs
     int cap_total;
     int seg_base[KV_NUM_SEG];      // index of a segment's first block in blk_len / blk_pos rows
     int n_blocks[KV_NUM_SEG];
@@ -60,13 +65,35 @@ __host__ __device__ inline unsigned char* block_ptr(const DevCache& c, int b, in
 struct IntBlockOffsets {
     int kc, km, vc, vm;
 };
-__host__ __device__ inline IntBlockOffsets int_offsets(int d, int bits) {
+__host__ __device__ inline IntBlockOffsets int_offsets(int d, int bits, int meta16) {
     IntBlockOffsets o;
     o.kc = 0;
     o.km = 4 * d * bits;
-    o.vc = o.km + 8 * d;
+    o.vc = o.km + (meta16 ? 4 : 8) * d;
     o.vm = o.vc + 4 * d * bits;
     return o;
+}
+
+// (s, z) pair i of a metadata array: fp32 pairs, or fp16 pairs widened exactly.
+template <bool M16>
+__device__ __forceinline__ float2 meta_at(const unsigned char* base, int i) {
+    if constexpr (M16) return __half22float2(reinterpret_cast<const __half2*>(base)[i]);
+    else return reinterpret_cast<const float2*>(base)[i];
+}
+__device__ __forceinline__ float2 meta_at(const unsigned char* base, int i, int meta16) {
+    return meta16 ? meta_at<true>(base, i) : meta_at<false>(base, i);
+}
+// Pairs i and i + 1 (i even) as (s_i, z_i, s_i+1, z_i+1), one 16- or 8-byte load.
+template <bool M16>
+__device__ __forceinline__ float4 meta2_at(const unsigned char* base, int i) {
+    if constexpr (M16) {
+        const uint2 u = reinterpret_cast<const uint2*>(base)[i >> 1];
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return reinterpret_cast<const float4*>(base)[i >> 1];
+    }
 }
 struct CbBlockOffsets {
     int kc, vc, vm, kq;
@@ -83,6 +110,45 @@ __host__ __device__ inline CbBlockOffsets cb_offsets(int d) {
 // The one dequantisation rule: one fp32 rounding of code*s + z.
 __device__ __forceinline__ float dequant(uint32_t code, float s, float z) {
     return __fmaf_rn(__uint2float_rn(code), s, z);
+}
+
+// fp16 dequantisation of blocks with fp16 metadata: one rounding of code * s + z, where
+// sz holds (s, z) as an fp16 pair; the code (< 16) is exact in fp16.
+__device__ __forceinline__ float dequant_h(uint32_t code, __half2 sz) {
+    return __half2float(__hfma(__uint2half_rn(code), __low2half(sz), __high2half(sz)));
+}
+
+// Codes i and i + 1 (i even) of a b-bit packed word as an exact fp16 pair (code i in the
+// low half).  The byte holding both codes goes into both halves, a mask keeps code i in
+// the low half and code i + 1 (times 2^b) in the high half, the fp16 exponent of 1024 is
+// or-ed in (values 1024 + code 2^p), and one fp16x2 FMA takes off the 1024 and the 2^p;
+// every step is exact.  With i known at compile time the constants fold.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair_f16(uint32_t w, int i) {
+    const uint32_t byte = BITS == 2 ? (uint32_t)(i >> 2) : (uint32_t)(i >> 1);
+    const uint32_t sel = byte | 0x40u | (byte << 8) | 0x4000u;
+    uint32_t mask, scale, bias;
+    if (BITS == 2) {
+        const bool hi = (i >> 1) & 1;      // codes in bits 4-7 of the byte
+        mask = hi ? 0x00C00030u : 0x000C0003u;
+        scale = hi ? 0x24002C00u : 0x34003C00u;   // (2^-4, 2^-6) : (1, 2^-2)
+        bias = hi ? 0xCC00D400u : 0xDC00E400u;    // (-64, -16) : (-1024, -256)
+    } else {
+        mask = 0x00F0000Fu;
+        scale = 0x2C003C00u;                      // (1, 2^-4)
+        bias = 0xD400E400u;                       // (-1024, -64)
+    }
+    const uint32_t x = (__byte_perm(w, 0u, sel) & mask) | 0x64006400u;
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(scale), "r"(bias));
+    return r;
+}
+
+// fp16x2 FMA a * b + c, one rounding per half.
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
 }
 
 // Key code of (token t, channel c) in a token-major code array.
@@ -112,7 +178,7 @@ __device__ __forceinline__ float raw16_to_f32(uint16_t bits, int raw_dtype);
 // Dequantised (key, value) of token t, channel ch of one block, in fp32 before
 // any rounding to the I/O dtype.  `cent` is the [d][4] centroid table of the
 // block's (batch, kv head) for codebook blocks, else unused.
-__device__ __forceinline__ float2 block_entry(int cls, const unsigned char* blk, int d, int raw_dtype,
+__device__ __forceinline__ float2 block_entry(int cls, const unsigned char* blk, int d, int raw_dtype, int meta16,
                                               const float* cent, int t, int ch) {
     if (cls == CLS_RAW16) {
         const uint16_t* r = reinterpret_cast<const uint16_t*>(blk);
@@ -127,11 +193,14 @@ __device__ __forceinline__ float2 block_entry(int cls, const unsigned char* blk,
         return make_float2(cent[ch * 4 + ki], dequant(vq, sv.x, sv.y));
     }
     const int bits = cls == CLS_INT4 ? 4 : 2;
-    const IntBlockOffsets o = int_offsets(d, bits);
-    const float2 sk = reinterpret_cast<const float2*>(blk + o.km)[ch];
-    const float2 sv = reinterpret_cast<const float2*>(blk + o.vm)[(ch / 32) * 32 + t];
+    const IntBlockOffsets o = int_offsets(d, bits, meta16);
     const uint32_t kq = key_code(reinterpret_cast<const uint32_t*>(blk + o.kc), t, ch, d, bits);
     const uint32_t vq = val_code(reinterpret_cast<const uint32_t*>(blk + o.vc), t, ch, bits);
+    if (meta16)
+        return make_float2(dequant_h(kq, reinterpret_cast<const __half2*>(blk + o.km)[ch]),
+                           dequant_h(vq, reinterpret_cast<const __half2*>(blk + o.vm)[(ch / 32) * 32 + t]));
+    const float2 sk = meta_at<false>(blk + o.km, ch);
+    const float2 sv = meta_at<false>(blk + o.vm, (ch / 32) * 32 + t);
     return make_float2(dequant(kq, sk.x, sk.y), dequant(vq, sv.x, sv.y));
 }
 

@@ -53,6 +53,20 @@ __device__ __forceinline__ void step_and_zero(float mn, float mx, float qmax, fl
     s = __fadd_rn(__fdiv_rn(__fsub_rn(mx, z), qmax), 0.0f);
 }
 
+// The stored (s, z) of a group: the fp32 pair, or its fp16 rounding (RNE; a -0 zero
+// point becomes +0) whose exact widening then serves for the codes.
+__device__ __forceinline__ void store_meta(unsigned char* base, int i, int meta16, float& s, float& z, bool write) {
+    if (meta16) {
+        const __half2 h = __floats2half2_rn(s, __fadd_rn(__half2float(__float2half_rn(z)), 0.0f));
+        const float2 f = __half22float2(h);
+        s = f.x;
+        z = f.y;
+        if (write) reinterpret_cast<__half2*>(base)[i] = h;
+    } else if (write) {
+        reinterpret_cast<float2*>(base)[i] = make_float2(s, z);
+    }
+}
+
 // Code of d = fl32(x - z) for step s with inverse r = 1/s (rounded): rint(fl32(d / s)),
 // clamped.  fl32(d * r) lies within 3 * 2^-24 |d / s| of fl32(d / s) (both quotients
 // carry at most two roundings of 2^-24), so the two round to the same integer
@@ -68,9 +82,9 @@ __device__ __forceinline__ uint32_t code_fast(float x, float s, float r, float z
 
 // Values of one block, INT layout: (token t, 32-channel group g) is shared by
 // tpc = 256 / d adjacent threads, each taking 32 / tpc channels; min / max are
-// combined by shuffles.  Writes Vm[g][t] and the codes into vc8[c][t].
+// combined by shuffles.  Writes Vm[g][t] (fp32 or fp16 pairs) and the codes into vc8[c][t].
 template <int BITS>
-__device__ void encode_values(const float* Vs, int ld, int d, int nv, uint8_t* vc8, float2* vm) {
+__device__ void encode_values(const float* Vs, int ld, int d, int nv, uint8_t* vc8, unsigned char* vm, int meta16) {
     const float qmax = float((1 << BITS) - 1);
     const int tid = threadIdx.x;
     const int tpc = kAppendThreads / d, span = kBlockTokens / tpc, part = tid % tpc;
@@ -89,8 +103,8 @@ __device__ void encode_values(const float* Vs, int ld, int d, int nv, uint8_t* v
     }
     float s = 0.0f, z = 0.0f;
     if (t < nv) step_and_zero(mn, mx, qmax, s, z);
+    store_meta(vm, g * 32 + t, meta16, s, z, part == 0);
     const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    if (part == 0) vm[g * 32 + t] = make_float2(s, z);
     for (int i = 0; i < span; ++i)
         vc8[(c0 + i) * kBlockTokens + t] =
             t < nv ? static_cast<uint8_t>(code_fast(Vs[t * ld + c0 + i], s, r, z, qmax)) : 0;
@@ -122,9 +136,9 @@ __device__ void pack_words(const uint8_t* kc8, const uint8_t* vc8, int nwords, u
 // one thread per output word packs them.
 template <int BITS>
 __device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d, int nv, uint8_t* kc8,
-                                 uint8_t* vc8, unsigned char* blk) {
+                                 uint8_t* vc8, unsigned char* blk, int meta16) {
     const float qmax = float((1 << BITS) - 1);
-    const IntBlockOffsets o = int_offsets(d, BITS);
+    const IntBlockOffsets o = int_offsets(d, BITS, meta16);
     const int tid = threadIdx.x;
     const int tpc = kAppendThreads / d;           // 1, 2, 4 or 8 threads per group
     const int span = kBlockTokens / tpc;          // elements per thread
@@ -147,14 +161,14 @@ __device__ void encode_int_block(const float* Ks, const float* Vs, int ld, int d
         }
         float s = 0.0f, z = 0.0f;
         if (nv > 0) step_and_zero(mn, mx, qmax, s, z);
+        store_meta(blk + o.km, ch, meta16, s, z, part == 0);
         const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
-        if (part == 0) reinterpret_cast<float2*>(blk + o.km)[ch] = make_float2(s, z);
         for (int i = 0; i < span; ++i) {
             const int t = t0 + i;
             kc8[t * d + ch] = t < nv ? static_cast<uint8_t>(code_fast(Ks[t * ld + ch], s, r, z, qmax)) : 0;
         }
     }
-    encode_values<BITS>(Vs, ld, d, nv, vc8, reinterpret_cast<float2*>(blk + o.vm));
+    encode_values<BITS>(Vs, ld, d, nv, vc8, blk + o.vm, meta16);
     __syncthreads();
     pack_words<BITS>(kc8, vc8, kBlockTokens * d * BITS / 32, reinterpret_cast<uint32_t*>(blk + o.kc),
                      reinterpret_cast<uint32_t*>(blk + o.vc));
@@ -326,7 +340,7 @@ __device__ void encode_cb_block(float* Ks, float* Vs, int ld, int d, int nv, uin
         const int c = e / rp, j = e - (e / rp) * rp;
         Us[e] = j < r ? __ldg(U + c * r + j) : 0.0f;
     }
-    encode_values<2>(Vs, ld, d, nv, vc8, reinterpret_cast<float2*>(blk + o.vm));
+    encode_values<2>(Vs, ld, d, nv, vc8, blk + o.vm, 0);
     __syncthreads();     // V is free for the low parts of the residual
     // keys: channel ch by tpc adjacent threads; the residual pair (high, low)
     // overwrites (K, V) in place
@@ -460,9 +474,9 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, De
         }
         __syncthreads();
         if (cls == CLS_INT4) {
-            encode_int_block<4>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk);
+            encode_int_block<4>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk, c.meta16);
         } else if (cls == CLS_INT2) {
-            encode_int_block<2>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk);
+            encode_int_block<2>(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d, blk, c.meta16);
         } else {
             const long long bh = (long long)b * c.Hkv + h;
             encode_cb_block(Ks, Vs, ld, d, nv, codes, codes + kBlockTokens * d,
@@ -494,7 +508,7 @@ __global__ void dequant_kernel(DevCache c, int n_tok, float* __restrict__ Kout, 
     const float* cent = c.centroids ? c.centroids + ((long long)b * c.Hkv + h) * d * 4 : nullptr;
     for (int e = threadIdx.x; e < len * d; e += blockDim.x) {
         const int t = e / d, ch = e % d;
-        const float2 kv = block_entry(cls, blk, d, c.raw_dtype, cent, t, ch);
+        const float2 kv = block_entry(cls, blk, d, c.raw_dtype, c.meta16, cent, t, ch);
         const long long o = (((long long)b * c.Hkv + h) * n_tok + pos + t) * d + ch;
         Kout[o] = kv.x;
         Vout[o] = kv.y;

@@ -86,13 +86,21 @@ typedef enum {
  * s = fl32(fl32(M-m)/(2^b-1)), code = clamp(rint(fl32(fl32(x-m)/s)), 0, 2^b-1),
  * z = m; dequantised x = fmaf(code, s, z).  Key groups are 32 tokens of one
  * channel (one block, aligned to each appended chunk); value groups are 32
- * channels of one token.  Pad slots hold code 0 and zero metadata. */
+ * channels of one token.  Pad slots hold code 0 and zero metadata.
+ * fp16 metadata (meta_dtype KV_F16; the smaller caches of [WQ] 主な結果 and the
+ * QuantWM card's Key Results): Km is half2[d] and Vm half2[d/32][32], each pair
+ * (s, z) as fp16 (d = 128 INT2: 3072 B per block instead of 4096).  s and z are
+ * the fp16 round-to-nearest-even of the fp32 step and minimum (a -0 zero point
+ * stored as +0), and the codes are taken against them:
+ * code = clamp(rint(fl32(fl32(x-z16)/s16))), code 0 where s16 == 0.  The cached
+ * values must lie within the fp16 range (|x| <= 65504). */
 typedef struct {
     int32_t B, Hkv, d;          /* d: multiple of 32, <= 256 */
     int32_t kind;               /* kv_kind */
     int32_t raw_dtype;          /* MIXED: dtype of RAW16 blocks (KV_F16 or KV_BF16) */
     int32_t psac_rank;          /* CODEBOOK2: r in [0, 32] */
     int32_t cap_blocks[KV_NUM_SEG]; /* capacity per segment, in 32-token blocks */
+    int32_t meta_dtype;         /* KV_F32 or KV_F16: dtype of the INT blocks' (s, z) metadata */
     /* derived by kv_layout_init: */
     int64_t block_bytes[KV_NUM_SEG];
     int64_t seg_offset[KV_NUM_SEG];
@@ -151,9 +159,11 @@ typedef struct {
     int32_t force_first; /* 1: window 0 is FP16 regardless of similarity */
 } kv_thresholds;
 
-/* Fill a layout and its derived sizes.  Host only. */
+/* Fill a layout and its derived sizes.  Host only.  meta_dtype: KV_F32, or KV_F16 for
+ * fp16 (s, z) metadata in the INT2 / INT4 blocks of UNIFORM2 / UNIFORM4 / MIXED caches
+ * (KV_ERR_UNSUPPORTED for CODEBOOK2; KV_ERR_INVALID_ARG for another dtype). */
 kv_status kv_layout_init(kv_layout* out, int B, int Hkv, int d, kv_kind kind, kv_dtype raw_dtype,
-                         const int32_t cap_blocks[KV_NUM_SEG], int psac_rank);
+                         const int32_t cap_blocks[KV_NUM_SEG], int psac_rank, kv_dtype meta_dtype);
 
 /* Bytes the caller must allocate for `region` (0 if the region is unused). */
 size_t kv_layout_bytes(const kv_layout* layout, kv_region region);

@@ -27,8 +27,8 @@ head dim d:
 
 fp16-metadata caches (a layout flag; INT2 / INT4 blocks only): Km is half2[d] and
 Vm half2[d/32][32], each pair (s, z) as two fp16 values, so the block shrinks by
-4 d bytes (d = 128 INT2: 4096 -> 3072 B); the quantiser then takes its codes
-against the fp16 pair (oracle/quant.py).
+8 d bytes (d = 128 INT2: 4096 -> 3072 B); the quantiser then takes its codes
+against the fp16 pair and dequantises in fp16 (oracle/quant.py).
 
 Within a word, element i (channel for Kc, token for Vc) sits at bit
 b*(i mod 32/b).  Keys are token-major because a key row feeds Q K^T;
@@ -118,8 +118,8 @@ def encode_int_blocks(Kb, Vb, bits, nvalid, meta16=False):
     vm = np.stack([vs, vz], -1).astype(F32).transpose(0, 2, 1, 3)   # [N,d/32,32,2]
     raw = np.concatenate([kw.reshape(N, -1).view(np.uint8), _meta_bytes(km, meta16).reshape(N, -1),
                           vw.reshape(N, -1).view(np.uint8), _meta_bytes(vm, meta16).reshape(N, -1)], axis=1)
-    khat = dequantize(kc, ks[:, None, :], kz[:, None, :])
-    vhat = dequantize(vc, vs[..., None], vz[..., None]).reshape(N, T, d)
+    khat = dequantize(kc, ks[:, None, :], kz[:, None, :], meta16)
+    vhat = dequantize(vc, vs[..., None], vz[..., None], meta16).reshape(N, T, d)
     return dict(bytes=raw, kcode=kc, ks=ks, kz=kz, vcode=vc.reshape(N, T, d), vs=vs, vz=vz,
                 khat=khat, vhat=vhat)
 

@@ -26,9 +26,15 @@ zero point stored as ``+0``), and the codes are taken against the stored pair,
     t_i = fl32(fl32(x_i - z16) / s16),  code_i = clamp(rint(t_i), 0, 2^b - 1)
     (code 0 everywhere if s16 == 0),    x_hat_i = fmaf(code_i, s16, z16),
 
-so that each code is the nearest level of the grid the cache actually holds.
-Inputs stay within the fp16 range (|x| <= 65504); beyond it s16 or z16 would
-be infinite.
+so that each code is the nearest level of the grid the cache actually holds,
+and the dequantised entry is computed in fp16 arithmetic, one rounding of the
+exact value (an fp16 fused multiply-add):
+
+    x_hat_i = fp16_rne(code_i * s16 + z16).
+
+The entry is then an fp16 number, as are the FP16 windows of a mixed cache
+and the tensor-core operands.  Inputs stay within the fp16 range
+(|x| <= 65504); beyond it s16 or z16 would be infinite.
 """
 
 from __future__ import annotations
@@ -68,6 +74,23 @@ def fma32(a, b, c):
     fix = at_mid & (err != 0) & (np.sign(err) == np.sign(diff))
     out = np.where(fix, nb, r).astype(F32)
     return out
+
+
+def f16_round(x):
+    """fp16 round-to-nearest-even of exact fp64 values, as fp64.
+
+    Written from the format's definition: 11 significant bits, exponents down to
+    -14 (below that the step stays 2^-24: subnormals), largest finite 65504;
+    magnitudes that round beyond it become infinite.  The scaling by a power of
+    two and np.rint (ties to even) are exact, so the result is one rounding.
+    """
+    x = np.asarray(x, dtype=F64)
+    a = np.abs(x)
+    _, e2 = np.frexp(np.where(a > 0, a, 1.0))          # a = m 2^e2, m in [0.5, 1)
+    step = np.ldexp(1.0, np.maximum(e2 - 1, -14) - 10)
+    y = np.rint(a / step) * step
+    y = np.where(y > 65504.0, np.inf, y)
+    return np.copysign(y, x)
 
 
 def f16_rne(x):
@@ -114,11 +137,18 @@ def quantize_groups(x, bits, n_valid=None, meta16=False):
     return codes, s, m
 
 
-def dequantize(codes, s, z):
-    """x_hat = fmaf(code, s, z) in fp32 (single rounding); s, z broadcast against codes."""
+def dequantize(codes, s, z, meta16=False):
+    """x_hat = fmaf(code, s, z) in fp32 (single rounding); s, z broadcast against codes.
+
+    meta16: s and z are fp16 values and x_hat = fp16_rne(code s + z), the value
+    code s + z being exact in fp64 (code < 16 and two fp16 operands); returned as fp32.
+    """
     codes = np.asarray(codes)
     s = np.broadcast_to(np.asarray(s, F32), codes.shape)
     z = np.broadcast_to(np.asarray(z, F32), codes.shape)
+    if meta16:
+        exact = codes.astype(F64) * s.astype(F64) + z.astype(F64)
+        return f16_round(exact).astype(F32)
     return fma32(codes.astype(F32), s, z)
 
 

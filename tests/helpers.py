@@ -24,13 +24,13 @@ def n_blocks_for(chunks):
     return sum((n + 31) // 32 for n in chunks)
 
 
-def gpu_uniform(case, bits, cap_extra=0):
-    """Append every chunk of a chunk-case through kv_quantize_append."""
+def gpu_uniform(case, bits, cap_extra=0, meta16=False):
+    """Append every chunk of a chunk-case through kv_quantize_append (meta16: fp16 (s, z))."""
     dt = case["dtype"]
     cap = n_blocks_for(case["chunks"]) + cap_extra
     kind = B.KV_UNIFORM2 if bits == 2 else B.KV_UNIFORM4
     caps = (0, 0, cap) if bits == 2 else (0, cap, 0)
-    tc = B.TorchCache(case["B"], case["Hkv"], case["d"], kind, caps)
+    tc = B.TorchCache(case["B"], case["Hkv"], case["d"], kind, caps, meta_dtype=B.KV_F16 if meta16 else B.KV_F32)
     t0 = 0
     for n in case["chunks"]:
         K = to_dev(case["K_cache"][:, :, t0:t0 + n], dt)
@@ -40,10 +40,11 @@ def gpu_uniform(case, bits, cap_extra=0):
     return tc
 
 
-def gpu_mixed(case, window_bits, caps):
+def gpu_mixed(case, window_bits, caps, meta16=False):
     import torch
     dt = case["dtype"]
-    tc = B.TorchCache(case["B"], case["Hkv"], case["d"], B.KV_MIXED, caps, raw_dtype=DT[dt])
+    tc = B.TorchCache(case["B"], case["Hkv"], case["d"], B.KV_MIXED, caps, raw_dtype=DT[dt],
+                      meta_dtype=B.KV_F16 if meta16 else B.KV_F32)
     n = case["K_cache"].shape[2]
     wb = np.ascontiguousarray(window_bits, dtype=np.int8)
     wb_dev = torch.from_numpy(wb).cuda()

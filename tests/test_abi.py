@@ -48,6 +48,25 @@ def test_layout_sizes_match_oracle(d):
     assert B.kv_layout_bytes(Lc, B.KV_REGION_PSAC_U) == 2 * d * 8 * 4
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp16_metadata_layout(d):
+    """fp16 (s, z) pairs: the INT segments shrink by 8 d bytes per block, RAW16 stays."""
+    L = B.kv_layout_init(2, 3, d, B.KV_MIXED, B.KV_F16, (5, 7, 11), 0, B.KV_F16)
+    assert L.meta_dtype == B.KV_F16
+    assert list(L.block_bytes) == [OL.block_bytes(OL.RAW16, d), OL.block_bytes(OL.INT4, d, meta16=True),
+                                   OL.block_bytes(OL.INT2, d, meta16=True)]
+    offs, stream = OL.stream_layout([OL.RAW16, OL.INT4, OL.INT2], [5, 7, 11], d, meta16=True)
+    assert list(L.seg_offset) == offs and L.stream_bytes == stream
+    L32 = B.kv_layout_init(2, 3, d, B.KV_MIXED, B.KV_F16, (5, 7, 11))
+    assert L32.stream_bytes - L.stream_bytes == (7 + 11) * 8 * d
+    with pytest.raises(B.BitKVError) as e:
+        B.kv_layout_init(1, 1, d, B.KV_CODEBOOK2, B.KV_BF16, (0, 0, 4), 0, B.KV_F16)
+    assert e.value.status == B.KV_ERR_UNSUPPORTED
+    with pytest.raises(B.BitKVError) as e:
+        B.kv_layout_init(1, 1, d, B.KV_UNIFORM2, B.KV_BF16, (0, 0, 4), 0, B.KV_BF16)
+    assert e.value.status == B.KV_ERR_INVALID_ARG
+
+
 def test_window_plan_matches_oracle():
     c = synth.decode_case()
     for b in range(8):

@@ -30,7 +30,8 @@ def uniform_pair(case, bits):
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 128), ("f16", 64), ("f32", 64), ("bf16", 256),
                                      ("f32", 32), ("f32", 128)])
 def test_uniform_append_ragged(bits, dtype, d):
-    """16-bit inputs of head dim 128 take the warp-per-block kernel, the rest the general one."""
+    """Ragged chunk ends (100 = 3 blocks + 4 tokens, 77, a full block, one token), every input
+    dtype, head dims 32 to 256."""
     case = synth.chunk_case(21, B=2, Hkv=3, d=d, chunks=[100, 77, 32, 1], n_cur=5, dtype=dtype)
     tc, oc = uniform_pair(case, bits)
     assert_same_cache(tc, oc)

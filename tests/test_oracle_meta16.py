@@ -25,9 +25,56 @@ def test_hand_cases(case):
     codes, s, z = quant.quantize_groups(x, case["bits"], meta16=True)
     assert codes.tolist() == case["codes"], case["why"]
     assert float(s) == case["s"] and float(z) == case["z"]
-    assert quant.dequantize(codes, s, z).tolist() == case["xhat"]
+    assert quant.dequantize(codes, s, z, meta16=True).tolist() == case["xhat"]
     if "codes_f32_meta" in case:
         assert quant.quantize_groups(x, case["bits"])[0].tolist() == case["codes_f32_meta"]
+
+
+def _all_f16_nonneg():
+    """Every finite non-negative fp16 value, from its bit patterns."""
+    return np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def test_f16_round_against_every_fp16_value():
+    """Exhaustive: each rounded value is an fp16 value, no fp16 value lies closer, ties go to
+    the even significand; the library's fp64 -> fp16 conversion agrees."""
+    grid = _all_f16_nonneg()
+    rng = np.random.default_rng(21)
+    mids = (grid[1:] + grid[:-1]) / 2                       # exact ties
+    x = np.concatenate([grid, mids, rng.uniform(0, 65504, 3000), np.exp(rng.uniform(-20, 11, 3000)),
+                        rng.uniform(0, 2 ** -14, 500), [65503.9, 65519.99, 65520.0, 1e6]])
+    x = np.concatenate([x, -x])
+    y = quant.f16_round(x)
+    with np.errstate(over="ignore"):
+        assert np.array_equal(y, x.astype(np.float16).astype(np.float64))
+    fin = np.isfinite(y)
+    assert (np.abs(x[~fin]) >= 65520).all() and (np.abs(x[fin]) < 65520).all()
+    idx = np.searchsorted(grid, np.abs(x[fin]))
+    lo = grid[np.maximum(idx - 1, 0)]
+    hi = grid[np.minimum(idx, grid.size - 1)]
+    ay, ax = np.abs(y[fin]), np.abs(x[fin])
+    assert (np.minimum(np.abs(lo - ax), np.abs(hi - ax)) == np.abs(ay - ax)).all()
+    tie = np.abs(lo - ax) == np.abs(hi - ax)
+    bits = ay[tie & (lo != hi)].astype(np.float16).view(np.uint16)
+    assert (bits & 1 == 0).all()
+
+
+def test_fp16_dequantisation_is_one_rounding():
+    """fp16 dequantisation: the fp16 value nearest to the exact code s + z (Fraction), where the
+    fp32 FMA followed by an fp16 rounding may round twice."""
+    rng = np.random.default_rng(22)
+    s = quant.f16_rne(np.exp(rng.uniform(-8, 5, 4000)).astype(np.float32))
+    z = quant.f16_rne((rng.standard_normal(4000) * 50).astype(np.float32))
+    k = rng.integers(0, 16, 4000)
+    got = quant.dequantize(k, s, z, meta16=True)
+    grid = _all_f16_nonneg()
+    for i in range(0, 4000, 7):
+        ex = Fraction(int(k[i])) * Fraction(float(s[i])) + Fraction(float(z[i]))
+        a = abs(ex)
+        j = int(np.searchsorted(grid, float(a)))
+        cands = [grid[max(j - 1, 0)], grid[min(j, grid.size - 1)], grid[min(j + 1, grid.size - 1)]]
+        best = min(abs(Fraction(c) - a) for c in cands)
+        assert abs(Fraction(abs(float(got[i]))) - a) == best
 
 
 def _fp16_neighbours(v):
@@ -122,12 +169,14 @@ def test_dequantised_error_bound():
         qmax = 2 ** bits - 1
         x = (rng.standard_normal((300, 32)) * np.exp(rng.uniform(-3, 3, (300, 1)))).astype(np.float32)
         codes, s, z = quant.quantize_groups(x, bits, meta16=True)
-        xh = quant.dequantize(codes, s[:, None], z[:, None]).astype(np.float64)
+        xh = quant.dequantize(codes, s[:, None], z[:, None], meta16=True).astype(np.float64)
+        assert np.array_equal(xh, xh.astype(np.float16).astype(np.float64))     # fp16 values
         lo = z.astype(np.float64)
         hi = lo + qmax * s.astype(np.float64)
         xc = np.clip(x.astype(np.float64), lo[:, None], hi[:, None])
         err = np.abs(xh - xc)
-        assert (err <= s[:, None] / 2 * (1 + 1e-5) + np.spacing(np.abs(x)) * 2).all()
+        half_f16 = np.abs(np.spacing(np.abs(xh).astype(np.float16)).astype(np.float64)) / 2
+        assert (err <= s[:, None] / 2 * (1 + 1e-5) + half_f16 + np.spacing(np.abs(x)) * 2).all()
         # the spans: |z - m| <= half an fp16 ulp of m, and the top level misses M by at most
         # qmax half-ulps of s plus half an ulp of m
         m, M = x.min(1).astype(np.float64), x.max(1).astype(np.float64)
