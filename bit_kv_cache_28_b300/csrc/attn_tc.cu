@@ -879,9 +879,10 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 commit(bar(BAR_O_DONE));
                 commit(bar(BAR_V_EMPTY + (jj & 1)));
             };
-            // the odd CTA's halves, forwarded by its MMA warp (a pair only)
+            // the odd CTA's halves, forwarded by its MMA warp (a pair only): polled relaxed,
+            // one acquire fence before the MMAs that read them are issued
             auto peer = [&](int base, int j) {
-                return !PAIR || mbar_test_wait_cluster(bar(base + (j & 1)), (j >> 1) & 1);
+                return !PAIR || mbar_test_wait_relaxed_cluster(bar(base + (j & 1)), (j >> 1) & 1);
             };
             // Issue Q K^T of tile j as soon as its operands are staged and P V of
             // tile i as soon as its P is written, whichever is ready first (P V of a
@@ -899,11 +900,13 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 if (np < nq && mbar_test_wait(bar(BAR_P_FULL + (np & 1)), (np >> 1) & 1) &&
                     mbar_test_wait(bar(BAR_V_FULL + (np & 1)), (np >> 1) & 1) && peer(BAR_PP_FULL, np) &&
                     peer(BAR_PV_FULL, np)) {
+                    if (PAIR) fence_acquire_cluster();
                     issue_pv(np++);
                     progressed = true;
                 } else if (nq < T && nq <= np + 1 && mbar_test_wait(bar(BAR_K_FULL + (nq & 1)), (nq >> 1) & 1) &&
                            peer(BAR_PK_FULL, nq) &&
                            (nq < 2 || mbar_test_wait(bar(BAR_V_EMPTY + (nq & 1)), ((nq - 2) >> 1) & 1))) {
+                    if (PAIR) fence_acquire_cluster();
                     issue_qk(nq++);
                     progressed = true;
                 }
@@ -925,8 +928,7 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
         } else if (PAIR && rank == 1 && lane < 3) {
             // the odd CTA of a pair: lanes 0, 1 and 2 forward this CTA's K_FULL, V_FULL and
             // P_FULL phases to the even CTA, whose MMAs read this CTA's halves; one lane per
-            // barrier, so that a forward waits for no other (a cluster-scope release arrive
-            // takes long).  No phase can run two ahead of its forwarding: K_FULL of tile
+            // barrier, so that a forward waits for no other.  No phase can run two ahead of its forwarding: K_FULL of tile
             // j + 2 needs this CTA's P_FULL of tile j, V_FULL of j + 2 the completion of
             // P V of j, P_FULL of j + 2 the Q K^T of j + 2, each issued only after tile j's
             // phase was forwarded.

@@ -267,23 +267,36 @@ __device__ __forceinline__ void mma_commit2(uint32_t bar) {
                  ::"r"(bar), "h"(mask)
                  : "memory");
 }
-// Non-blocking phase test with cluster-scope acquire (the arrivals come from the peer CTA).
-__device__ __forceinline__ uint32_t mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+// Cross-CTA signalling in a pair, the light way: the signalling thread orders what it has
+// observed with a release fence restricted to shared::cta and arrives relaxed on the peer's
+// barrier; the waiting thread polls relaxed and, once its conditions hold, takes one acquire
+// fence restricted to shared::cluster before it acts (issues the MMAs that read the peer's
+// operands).  Release / acquire at cluster scope on every arrive and poll cost about 1 K
+// cycles per hand-off on this part.
+//
+// Non-blocking phase test, relaxed at cluster scope (the arrivals come from the peer CTA);
+// follow a successful set of tests with fence_acquire_cluster().
+__device__ __forceinline__ uint32_t mbar_test_wait_relaxed_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P1;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.relaxed.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
         "selp.b32 %0, 1, 0, P1;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
         : "memory");
     return ok;
 }
-// Arrive (release, cluster scope) on the barrier at the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void fence_acquire_cluster() {
+    asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+}
+// Release fence (shared::cta) and a relaxed arrive on the barrier at the same offset in CTA
+// `rank` of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 // ---- packed fp32 pairs (sm_100+: one instruction for two lanes of fp32 work) -----
