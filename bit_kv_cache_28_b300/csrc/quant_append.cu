@@ -491,6 +491,196 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, De
     }
 }
 
+// ---- uniform INT blocks from 16-bit rows, head dim 128: one CTA (8 warps) per block --------
+// The same quantiser as encode_int_block with less work per element.
+//   keys: the block's rows staged as raw 16-bit pairs in a 32 x 64-word tile whose 16-byte
+//     chunks are XOR-swizzled by row / 8 (the reads below are then conflict-free); pad rows
+//     hold a copy of row 0, so min / max over all 32 rows are those of the valid rows.  Warp w
+//     owns channels 16 w .. 16 w + 15 (8 channel pairs), lane l the pair l / 4 over tokens
+//     8 (l & 3) .. + 7: min / max by fp16x2 / bf16x2 operations (exact), two xor-shuffles, the
+//     codes in registers, and each token's code word OR-reduced across the 8 (4) lanes that hold
+//     its channels and stored directly (zero for pad tokens).
+//   values: lane l of warp w takes token 4 w + l / 8, channels 16 (l & 7) .. + 15 straight from
+//     global memory; a 32-channel group is two lanes (one shuffle); the codes go to a byte tile
+//     [128 channels][32 tokens], from which each thread packs its channel-major words.
+template <typename T> struct Pair16;
+template <> struct Pair16<__half> {
+    using P = __half2;
+    static __device__ __forceinline__ float2 f2(uint32_t w) { return __half22float2(*reinterpret_cast<const P*>(&w)); }
+    static __device__ __forceinline__ uint32_t mn(uint32_t a, uint32_t b) {
+        const P r = __hmin2(*reinterpret_cast<const P*>(&a), *reinterpret_cast<const P*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    static __device__ __forceinline__ uint32_t mx(uint32_t a, uint32_t b) {
+        const P r = __hmax2(*reinterpret_cast<const P*>(&a), *reinterpret_cast<const P*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+};
+template <> struct Pair16<__nv_bfloat16> {
+    using P = __nv_bfloat162;
+    static __device__ __forceinline__ float2 f2(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+    static __device__ __forceinline__ uint32_t mn(uint32_t a, uint32_t b) {
+        const P r = __hmin2(*reinterpret_cast<const P*>(&a), *reinterpret_cast<const P*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    static __device__ __forceinline__ uint32_t mx(uint32_t a, uint32_t b) {
+        const P r = __hmax2(*reinterpret_cast<const P*>(&a), *reinterpret_cast<const P*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+};
+
+constexpr int kFastD = 128;
+
+template <typename T, int BITS>
+__global__ void __launch_bounds__(kAppendThreads)
+append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, DevCache c, int seg, int tok0) {
+    using PP = Pair16<T>;
+    constexpr int D = kFastD;
+    constexpr float qmax = float((1 << BITS) - 1);
+    __shared__ __align__(16) uint32_t kt[kBlockTokens * D / 2];     // 8 KB: key rows, 16-bit pairs
+    __shared__ __align__(16) uint8_t vc8[D * kBlockTokens];         // 4 KB: value codes [c][t]
+    const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = j * kBlockTokens;
+    const int nv = min(kBlockTokens, n_tokens - t0);
+    const int idx = c.n_blocks[seg] + j;
+    unsigned char* blk = block_ptr(c, b, h, seg, idx);
+    const IntBlockOffsets o = int_offsets(D, BITS, c.meta16);
+    const long long row0 = (((long long)b * c.Hkv + h) * n_tokens + t0) * D;
+
+    // key rows -> the swizzled tile (pad rows: a copy of row 0)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int e = tid + k * kAppendThreads, row = e >> 4, ch = e & 15;
+        const int src = row < nv ? row : 0;
+        const uint4 v = *reinterpret_cast<const uint4*>(K + row0 + (long long)src * D + 8 * ch);
+        *reinterpret_cast<uint4*>(kt + row * (D / 2) + 4 * (ch ^ (((row >> 3) & 3) << 1))) = v;
+    }
+
+    // values: token tv, channels 16 jv .. 16 jv + 15 from global memory
+    {
+        const int tv = 4 * warp + (lane >> 3), jv = lane & 7;
+        uint32_t w[8];
+        if (tv < nv) {
+            const uint4* src = reinterpret_cast<const uint4*>(V + row0 + (long long)tv * D + 16 * jv);
+            const uint4 a = src[0], bq = src[1];
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = bq.x; w[5] = bq.y; w[6] = bq.z; w[7] = bq.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = 0u;
+        }
+        uint32_t mnp = w[0], mxp = w[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            mnp = PP::mn(mnp, w[i]);
+            mxp = PP::mx(mxp, w[i]);
+        }
+        float2 fmn = PP::f2(mnp), fmx = PP::f2(mxp);
+        float mn = fminf(fmn.x, fmn.y), mx = fmaxf(fmx.x, fmx.y);
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        float s = 0.0f, z = 0.0f;
+        if (tv < nv) step_and_zero(mn, mx, qmax, s, z);
+        store_meta(blk + o.vm, (jv >> 1) * 32 + tv, c.meta16, s, z, (jv & 1) == 0);
+        const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 f = PP::f2(w[i]);
+            const int ch = 16 * jv + 2 * i;
+            vc8[ch * kBlockTokens + tv] = tv < nv ? (uint8_t)code_fast(f.x, s, r, z, qmax) : 0;
+            vc8[(ch + 1) * kBlockTokens + tv] = tv < nv ? (uint8_t)code_fast(f.y, s, r, z, qmax) : 0;
+        }
+    }
+    __syncthreads();
+
+    // keys: warp w, channel pair cp = 8 w + lane / 4, tokens 8 q .. 8 q + 7 (q = lane & 3)
+    {
+        const int q = lane & 3, pl = lane >> 2, cp = 8 * warp + pl;
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * q + i;
+            w[i] = kt[t * (D / 2) + (cp ^ (q << 3))];
+        }
+        uint32_t mnp = w[0], mxp = w[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            mnp = PP::mn(mnp, w[i]);
+            mxp = PP::mx(mxp, w[i]);
+        }
+        float2 mn = PP::f2(mnp), mx = PP::f2(mxp);
+#pragma unroll
+        for (int x = 1; x < 4; x <<= 1) {
+            mn.x = fminf(mn.x, __shfl_xor_sync(0xffffffffu, mn.x, x));
+            mn.y = fminf(mn.y, __shfl_xor_sync(0xffffffffu, mn.y, x));
+            mx.x = fmaxf(mx.x, __shfl_xor_sync(0xffffffffu, mx.x, x));
+            mx.y = fmaxf(mx.y, __shfl_xor_sync(0xffffffffu, mx.y, x));
+        }
+        float s0, z0, s1, z1;
+        step_and_zero(mn.x, mx.x, qmax, s0, z0);
+        step_and_zero(mn.y, mx.y, qmax, s1, z1);
+        store_meta(blk + o.km, 2 * cp, c.meta16, s0, z0, q == 0);
+        store_meta(blk + o.km, 2 * cp + 1, c.meta16, s1, z1, q == 0);
+        const float r0 = s0 > 0.0f ? __frcp_rn(s0) : 0.0f, r1 = s1 > 0.0f ? __frcp_rn(s1) : 0.0f;
+        // INT2: a word holds 16 channels = this warp's 8 pairs (shift 4 pl);
+        // INT4: 8 channels = 4 pairs, two words per warp (word pl / 4, shift 8 (pl & 3))
+        constexpr int KW = D * BITS / 32;   // code words per key row
+        const int shift = BITS == 2 ? 4 * pl : 8 * (pl & 3);
+        // after the OR-reduction every lane of a word's group holds the word of token 8 q + i;
+        // INT2: lane (pl, q) keeps token 8 q + pl's; INT4: lane (pl, q) keeps tokens
+        // 8 q + (pl & 3) and 8 q + (pl & 3) + 4 of word 2 w + pl / 4
+        uint32_t mine0 = 0u, mine1 = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * q + i;
+            const float2 f = PP::f2(w[i]);
+            uint32_t part = 0u;
+            if (t < nv) part = (code_fast(f.x, s0, r0, z0, qmax) | (code_fast(f.y, s1, r1, z1, qmax) << BITS)) << shift;
+            part |= __shfl_xor_sync(0xffffffffu, part, 4);
+            part |= __shfl_xor_sync(0xffffffffu, part, 8);
+            if (BITS == 2) part |= __shfl_xor_sync(0xffffffffu, part, 16);
+            if (BITS == 2) {
+                if (pl == i) mine0 = part;
+            } else {
+                if ((pl & 3) == i) mine0 = part;
+                if ((pl & 3) + 4 == i) mine1 = part;
+            }
+        }
+        uint32_t* kc = reinterpret_cast<uint32_t*>(blk + o.kc);
+        if (BITS == 2) {
+            kc[(8 * q + pl) * KW + warp] = mine0;
+        } else {
+            kc[(8 * q + (pl & 3)) * KW + 2 * warp + (pl >> 2)] = mine0;
+            kc[(8 * q + (pl & 3) + 4) * KW + 2 * warp + (pl >> 2)] = mine1;
+        }
+    }
+
+    // value code words: channel-major, (32 / BITS) tokens per word
+    {
+        uint32_t* vw = reinterpret_cast<uint32_t*>(blk + o.vc);
+        constexpr int per = 32 / BITS, nw = D * BITS;   // words per block
+        for (int e = tid; e < nw; e += kAppendThreads) {
+            const int ch = e / BITS, part = e % BITS;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc8 + ch * kBlockTokens + part * per);
+            uint32_t word = 0u;
+#pragma unroll
+            for (int k = 0; k < per / 4; ++k) {
+                const uint32_t x = src[k];   // 4 codes, one per byte
+#pragma unroll
+                for (int i = 0; i < 4; ++i) word |= ((x >> (8 * i)) & ((1u << BITS) - 1u)) << (BITS * (4 * k + i));
+            }
+            vw[e] = word;
+        }
+    }
+    if (h == 0 && tid == 0) {
+        const long long gi = (long long)b * c.cap_total + c.seg_base[seg] + idx;
+        c.blk_len[gi] = nv;
+        c.blk_pos[gi] = tok0 + t0;
+    }
+}
+
 __global__ void dequant_kernel(DevCache c, int n_tok, float* __restrict__ Kout, float* __restrict__ Vout) {
     int flat = blockIdx.x;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -527,6 +717,18 @@ template <typename T>
 static kv_status launch_append_t(const void* K, const void* V, int n_tokens, const kv_cache* cache, int mode,
                                  int uni_seg, const int8_t* win_bits, int n_win, int grid_x, cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
+    if constexpr (sizeof(T) == 2) {
+        if (mode == 0 && c.d == kFastD) {
+            dim3 grid(grid_x, c.Hkv, c.B);
+            if (uni_seg == KV_SEG_INT4)
+                append_int128_kernel<T, 4><<<grid, kAppendThreads, 0, st>>>(
+                    static_cast<const T*>(K), static_cast<const T*>(V), n_tokens, c, uni_seg, cache->n_tokens);
+            else
+                append_int128_kernel<T, 2><<<grid, kAppendThreads, 0, st>>>(
+                    static_cast<const T*>(K), static_cast<const T*>(V), n_tokens, c, uni_seg, cache->n_tokens);
+            return check_launch("append_int128_kernel");
+        }
+    }
     const size_t sm = append_smem_bytes(c.d, c.kind == KV_CODEBOOK2 ? c.rp : 0);
     const kv_status sa = set_smem_limit(reinterpret_cast<const void*>(append_kernel<T>), 120 * 1024, "append_kernel");
     if (sa != KV_OK) return sa;
