@@ -585,12 +585,15 @@ append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tok
         if (tv < nv) step_and_zero(mn, mx, qmax, s, z);
         store_meta(blk + o.vm, (jv >> 1) * 32 + tv, c.meta16, s, z, (jv & 1) == 0);
         const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+        // byte tile [c][t] with token t of channel c at t ^ 4 (c / 16): the 8 lanes of a token
+        // (channels 16 jv ..) then store into 8 different banks
+        const int tsw = tv ^ (jv << 2);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float2 f = PP::f2(w[i]);
             const int ch = 16 * jv + 2 * i;
-            vc8[ch * kBlockTokens + tv] = tv < nv ? (uint8_t)code_fast(f.x, s, r, z, qmax) : 0;
-            vc8[(ch + 1) * kBlockTokens + tv] = tv < nv ? (uint8_t)code_fast(f.y, s, r, z, qmax) : 0;
+            vc8[ch * kBlockTokens + tsw] = tv < nv ? (uint8_t)code_fast(f.x, s, r, z, qmax) : 0;
+            vc8[(ch + 1) * kBlockTokens + tsw] = tv < nv ? (uint8_t)code_fast(f.y, s, r, z, qmax) : 0;
         }
     }
     __syncthreads();
@@ -663,13 +666,21 @@ append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tok
         constexpr int per = 32 / BITS, nw = D * BITS;   // words per block
         for (int e = tid; e < nw; e += kAppendThreads) {
             const int ch = e / BITS, part = e % BITS;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(vc8 + ch * kBlockTokens + part * per);
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(vc8 + ch * kBlockTokens);
             uint32_t word = 0u;
 #pragma unroll
             for (int k = 0; k < per / 4; ++k) {
-                const uint32_t x = src[k];   // 4 codes, one per byte
-#pragma unroll
-                for (int i = 0; i < 4; ++i) word |= ((x >> (8 * i)) & ((1u << BITS) - 1u)) << (BITS * (4 * k + i));
+                // tokens 4 k' .. 4 k' + 3 (k' = part per / 4 + k): one byte each, in word k' ^ (c / 16)
+                uint32_t x = row[((part * per / 4) + k) ^ (ch >> 4)];
+                if (BITS == 2) {
+                    x = (x | (x >> 6)) & 0x000F000Fu;   // b0 | b1 << 2 in byte 0, b2 | b3 << 2 in byte 2
+                    x = (x | (x >> 12)) & 0xFFu;        // b0 | b1 << 2 | b2 << 4 | b3 << 6
+                    word |= x << (8 * k);
+                } else {
+                    x = (x | (x >> 4)) & 0x00FF00FFu;   // b0 | b1 << 4 in byte 0, b2 | b3 << 4 in byte 2
+                    x = (x | (x >> 8)) & 0xFFFFu;
+                    word |= x << (16 * k);
+                }
             }
             vw[e] = word;
         }
