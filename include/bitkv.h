@@ -178,7 +178,8 @@ kv_status kv_cache_init(kv_cache* cache, const kv_layout* layout, void* data, in
  * in `dtype`.  UNIFORM*: the chunk starts new blocks (the last may be partial).
  * MIXED: the cache position must be a multiple of 32, each window goes to the
  * segment of its bit-width; per-segment window counts must agree across B.
- * CODEBOOK2: centroids (and psac_u if r > 0) must be filled first.  Fails with
+ * CODEBOOK2: centroids (and psac_u if r > 0) must be filled first.  With fp16
+ * metadata the values must lie within the fp16 range.  Fails with
  * KV_ERR_CAPACITY before launching if a segment would overflow.  Updates
  * cache->n_blocks and cache->n_tokens on the host. */
 kv_status kv_quantize_append(const void* K, const void* V, kv_dtype dtype, int n_tokens, kv_cache* cache,
@@ -208,10 +209,13 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
  * q' = q otherwise, one value per query row ([QWM] PSAC; [JB] second-order
  * correction); EXACT is KV_ERR_UNSUPPORTED there; without resid_var, none.
  * Precision: the result is defined over the exact dequantised entries
- * fmaf(code, s, z) and the inputs as given.  The CUDA-core path (KV_PATH_SIMT)
- * computes that definition in fp32.  The decode path multiplies exact integer
- * codes by the query scaled by the step, split into fp16 high and low parts
- * (about 22 bits), and adds the zero-point term in fp32.  The tensor-core path
+ * fmaf(code, s, z) (fp16 metadata: the fp16 entries fp16(code s + z)) and the
+ * inputs as given.  The CUDA-core path (KV_PATH_SIMT) computes that definition in
+ * fp32.  The decode path multiplies exact integer codes by the query scaled by
+ * the step, split into fp16 high and low parts (about 22 bits), and adds the
+ * zero-point term in fp32; with fp16 metadata it multiplies the fp16 entries by
+ * the query taken as fp16 (a bf16 query beyond the fp16 range raises the range
+ * flag).  The tensor-core path
  * holds the operands of both products in fp16: K_hat and V_hat are the fp16
  * roundings of the dequantised entries, Q and the current keys the fp16
  * conversions of their bf16 values (exact inside the fp16 range), P the fp16
@@ -355,12 +359,14 @@ kv_status kv_dequantize(const kv_cache* cache, float* K_out, float* V_out, void*
  * over all segments in memory order (FP16, INT4, INT2), token t of block i at
  * slot 32 i + t (pad slots included).
  *   path KV_PATH_TC (UNIFORM2 / UNIFORM4 / CODEBOOK2, d 128): the tensor-core
- *     kernel's K_hat and V_hat (the fp16 roundings of the dequantised entries),
- *     expanded by its producer routines from a staged tile and un-swizzled.
- *   path KV_PATH_DECODE (UNIFORM2 / UNIFORM4 / MIXED, d 64 or 128): the decode
- *     kernel forms no dequantised entry; its key and value operands are the codes,
- *     as the exact fp16 integers its extraction routine feeds the MMAs.  FP16
- *     slots are not written (that path reads them as stored).
+ *     kernel's K_hat and V_hat (the fp16 roundings of the dequantised entries; with
+ *     fp16 metadata the entries themselves, which are fp16 numbers), expanded by its
+ *     producer routines from a staged tile and un-swizzled.
+ *   path KV_PATH_DECODE (UNIFORM2 / UNIFORM4 / MIXED, d 64 or 128): with fp32
+ *     metadata the decode kernel forms no dequantised entry: its key and value
+ *     operands are the codes, as the exact fp16 integers its extraction routine
+ *     feeds the MMAs; with fp16 metadata they are the fp16 entries.  FP16 slots are
+ *     not written (that path reads them as stored).
  * Async on `stream`. */
 kv_status kv_debug_operands(const kv_cache* cache, int path, void* K_out, void* V_out, void* stream);
 
