@@ -533,6 +533,29 @@ template <> struct Pair16<__nv_bfloat16> {
 
 constexpr int kFastD = 128;
 
+// Codes of two elements as code_fast() takes them (x0 against s0, r0 = 1/s0, z0; x1 against
+// s1, r1, z1), in packed fp32x2 arithmetic: q = fl32(fl32(x - z) r) is rounded to the nearest
+// integer, ties to even, by adding 1.5 2^23 (exact for |q| < 2^22, which a code's quotient
+// always is) and read out of that sum's low mantissa bits.  e = q - rint(q) is exact, and
+// ||e| - 1/2| equals code_fast()'s |q - floor(q) - 1/2| bit for bit, so the same elements (within
+// 4e-6 of a half-integer, or r not finite) take the IEEE quotient.  Zero steps give code 0.
+__device__ __forceinline__ void code_pair2(float x0, float x1, float s0, float s1, float r0, float r1, float z0,
+                                           float z1, int qmax, uint32_t& c0, uint32_t& c1) {
+    constexpr float kMagic = 12582912.0f;   // 1.5 2^23
+    const f32x2 d = x2_sub(x2(x0, x1), x2(z0, z1));
+    const f32x2 q = x2_mul(d, x2(r0, r1));
+    const f32x2 t = x2_add(q, x2(kMagic, kMagic));
+    const float2 e = x2_split(x2_sub(q, x2_sub(t, x2(kMagic, kMagic))));
+    float2 tf = x2_split(t);
+    if (fabsf(fabsf(e.x) - 0.5f) < 4e-6f || !(r0 < INFINITY))
+        tf.x = __fadd_rn(__fdiv_rn(__fsub_rn(x0, z0), s0), kMagic);
+    if (fabsf(fabsf(e.y) - 0.5f) < 4e-6f || !(r1 < INFINITY))
+        tf.y = __fadd_rn(__fdiv_rn(__fsub_rn(x1, z1), s1), kMagic);
+    const int k0 = (int)__float_as_uint(tf.x) - 0x4B400000, k1 = (int)__float_as_uint(tf.y) - 0x4B400000;
+    c0 = s0 > 0.0f ? (uint32_t)min(max(k0, 0), qmax) : 0u;
+    c1 = s1 > 0.0f ? (uint32_t)min(max(k1, 0), qmax) : 0u;
+}
+
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kAppendThreads)
 append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tokens, DevCache c, int seg, int tok0) {
@@ -592,8 +615,10 @@ append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tok
         for (int i = 0; i < 8; ++i) {
             const float2 f = PP::f2(w[i]);
             const int ch = 16 * jv + 2 * i;
-            vc8[ch * kBlockTokens + tsw] = tv < nv ? (uint8_t)code_fast(f.x, s, r, z, qmax) : 0;
-            vc8[(ch + 1) * kBlockTokens + tsw] = tv < nv ? (uint8_t)code_fast(f.y, s, r, z, qmax) : 0;
+            uint32_t k0, k1;
+            code_pair2(f.x, f.y, s, s, r, r, z, z, (1 << BITS) - 1, k0, k1);
+            vc8[ch * kBlockTokens + tsw] = tv < nv ? (uint8_t)k0 : 0;
+            vc8[(ch + 1) * kBlockTokens + tsw] = tv < nv ? (uint8_t)k1 : 0;
         }
     }
     __syncthreads();
@@ -639,8 +664,10 @@ append_int128_kernel(const T* __restrict__ K, const T* __restrict__ V, int n_tok
         for (int i = 0; i < 8; ++i) {
             const int t = 8 * q + i;
             const float2 f = PP::f2(w[i]);
-            uint32_t part = 0u;
-            if (t < nv) part = (code_fast(f.x, s0, r0, z0, qmax) | (code_fast(f.y, s1, r1, z1, qmax) << BITS)) << shift;
+            uint32_t k0, k1;
+            code_pair2(f.x, f.y, s0, s1, r0, r1, z0, z1, (1 << BITS) - 1, k0, k1);
+            const uint32_t part0 = t < nv ? (k0 | (k1 << BITS)) << shift : 0u;
+            uint32_t part = part0;
             part |= __shfl_xor_sync(0xffffffffu, part, 4);
             part |= __shfl_xor_sync(0xffffffffu, part, 8);
             if (BITS == 2) part |= __shfl_xor_sync(0xffffffffu, part, 16);
