@@ -46,8 +46,9 @@ def mixed_pair(case):
 # ---- append ------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("bits", [2, 4])
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 32), ("bf16", 256)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 128), ("f16", 64), ("f32", 32), ("bf16", 256)])
 def test_uniform_append_bit_exact(bits, dtype, d):
+    """16-bit rows at head dim 128 take the fast append kernel, the rest the general one."""
     case = synth.chunk_case(131, B=2, Hkv=3, d=d, chunks=[100, 77, 32, 1], n_cur=5, dtype=dtype)
     tc = gpu_uniform(case, bits, meta16=True)
     assert tc.layout.block_bytes[2 if bits == 2 else 1] == OL.block_bytes(OL.INT2 if bits == 2 else OL.INT4, d,
