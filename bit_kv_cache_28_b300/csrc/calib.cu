@@ -292,7 +292,7 @@ jacobi_kernel(double* __restrict__ Cws, double* __restrict__ Vws, int d, int r, 
         if (offsum <= 1e-30 * s_done || offsum == 0.0) break;
         __syncthreads();
         for (int rd = 0; rd < m - 1; ++rd) {
-            // rotation angles of this round's d/2 disjoint pairs
+            // rotation angles of this sweep step's d/2 disjoint pairs
             for (int i = tid; i < half; i += kJThreads) {
                 int p = rr_index(i, rd, m), q = rr_index(m - 1 - i, rd, m);
                 if (p > q) { const int t = p; p = q; q = t; }
