@@ -381,7 +381,7 @@ class DecodeRunner:
         self.ws_bytes = B.kv_attention_workspace(self.tc.c, self.dt, 1, 1, spec["Hq"], self.opts)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
         self.path, self.splits = B.kv_attention_plan(self.tc.c, self.dt, 1, 1, spec["Hq"], self.opts)
-        self.launches_per_step = 1   # the decode kernel merges its splits itself
+        self.launches_per_step = 2   # the decode kernel and its split merge
 
     def attention(self, stream):
         s = self.spec

@@ -27,10 +27,11 @@ kv_status launch_attn_simt(const void* Q, const void* Kc, const void* Vc, kv_dty
 size_t simt_workspace(const kv_cache* cache, int n_q, int Hq, int n_splits);
 int simt_units_cache(const kv_cache* c);
 kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_dtype dt, int n_cur, int Hq,
-                             const kv_cache* cache, float tau, int jensen, int n_splits, void* out, int out_f32,
+                             const kv_cache* cache, float tau, int jensen, int n_splits, int n_ctas, void* out, int out_f32,
                              float* lse, void* ws, cudaStream_t st);
 size_t decode_workspace(const kv_cache* cache, int Hq, int n_splits);
 int decode_auto_splits(const kv_cache* cache, int Hq);
+int decode_auto_ctas(const kv_cache* cache, int Hq, int n_splits);
 bool decode_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq);
 kv_status launch_attn_tc(const void* Q, const void* Kc, const void* Vc, int n_q, int n_cur, int Hq,
                          const kv_cache* cache, float tau, int jensen, int psac, int n_splits, void* out, int out_f32,
@@ -397,7 +398,9 @@ kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dty
                 return set_error(KV_ERR_UNSUPPORTED, "decode path: needs n_q == 1, f16/bf16, d in {64,128}, "
                                  "UNIFORM/MIXED cache and at most 16 query heads per kv head");
             if (o->psac) return set_error(KV_ERR_UNSUPPORTED, "decode path has no PSAC term");
-            r = launch_attn_decode(Q, Kcur, Vcur, dtype, n_cur, Hq, cache, tau, o->jensen, sp, out, o->out_f32, lse,
+            // automatic splits: one wave of resident CTAs, some streams one split fewer
+            r = launch_attn_decode(Q, Kcur, Vcur, dtype, n_cur, Hq, cache, tau, o->jensen, sp,
+                                   o->num_splits > 0 ? 0 : decode_auto_ctas(cache, Hq, sp), out, o->out_f32, lse,
                                    workspace, st);
             break;
         case KV_PATH_TC:

@@ -6,8 +6,10 @@
 // mixed FP16 / INT4 / INT2 cache is stored grouped by bit-width so that each
 // class streams contiguously.  This kernel reads every cache byte exactly once.
 //
-// Work split.  Grid (splits, Hkv, B).  A CTA takes a contiguous, byte-balanced
-// range of one (batch, kv head) stream; its 4 warps take blocks w, w+4, ... of
+// Work split.  A 1-D grid of CTAs over the (batch, kv head) streams, by default one
+// wave of resident CTAs (streams past the first (CTAs mod streams) take one split
+// fewer).  A CTA takes a contiguous, cost-balanced range of its stream's blocks
+// (split_begin); its 4 warps take blocks w, w+4, ... of
 // the range, each block bulk-copied (TMA engine, cp.async.bulk) into the
 // warp's own ring of shared-memory slots, several blocks ahead.
 //
@@ -26,9 +28,12 @@
 // Attention" (abstract) is a per-(block, head) scalar, sum_c q_c^2 s_c^2.
 // Current-chunk tokens run on CUDA cores.
 //
-// Merge.  Warps merge (m, l, o) through shared memory, CTAs write partials,
-// and the last CTA of a stream (atomic ticket) merges them:
-// m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l.
+// Merge.  Warps merge (m, l, o) through shared memory, CTAs write partials and
+// a status word each, and a merge kernel (one CTA per stream, launched with
+// programmatic stream serialisation so that it is resident when the decode grid
+// ends) combines them, m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p
+// 2^(m_p - m) / l, and writes the call's status header.  Nothing in the workspace
+// has to be cleared before a call.
 #include <cstdio>
 #include <cstdlib>
 #include <type_traits>
@@ -619,15 +624,66 @@ __device__ __forceinline__ void current_token(const T* kr, const T* vr, const La
     }
 }
 
-// First block of split s of a stream of nb blocks (segment-major: RAW16, INT4,
-// INT2) cut into S ranges of equal block counts.  A block's cost is about the
-// same in every class once both its bytes and its instructions are counted (an
-// 8 KB RAW16 block streams 4x the bytes of a 2 KB INT2 block but issues about a
-// third of its instructions), so equal counts balance the splits.
+// First block of split s of a stream (segment-major: RAW16, INT4, INT2 blocks) cut into
+// S ranges of equal cost.  A warp's time per block, measured with all three classes
+// resident: RAW16 0.7, INT4 1.13 and INT2 1 times that of an INT2 block (an 8 KB RAW16
+// block streams 4x the bytes of a 2 KB INT2 block but issues about a third of its
+// instructions; an INT4 block has twice the codes of an INT2 block).  Hence the weights
+// 7 : 11 : 10 per block; split s starts at the first block where the running cost
+// reaches s / S of the stream's total.
 __device__ __forceinline__ int split_begin(const DevCache& c, int s, int S) {
-    const long long nb = (long long)c.n_blocks[0] + c.n_blocks[1] + c.n_blocks[2];
-    return (int)((long long)s * nb / S);
+    long long w[KV_NUM_SEG], total = 0;
+#pragma unroll
+    for (int g = 0; g < KV_NUM_SEG; ++g) {
+        const int cls = seg_class(c.kind, g);
+        w[g] = cls == CLS_INT2 ? 10 : (cls == CLS_INT4 ? 11 : 7);
+        total += w[g] * c.n_blocks[g];
+    }
+    const long long t = (long long)s * total / S;
+    long long acc = 0;
+    int first = 0;
+#pragma unroll
+    for (int g = 0; g < KV_NUM_SEG; ++g) {
+        const long long span = w[g] * c.n_blocks[g];
+        if (t <= acc + span) return first + (int)((t - acc + w[g] - 1) / w[g]);
+        acc += span;
+        first += c.n_blocks[g];
+    }
+    return first;
 }
+
+// Split of CTA i of a grid of n_ctas CTAs over `streams` (batch, kv head) streams: the
+// first n_ctas % streams streams take one split more than the others, so that a grid of
+// exactly the resident CTA count keeps every SM at the same number of CTAs.
+struct SplitOf {
+    int stream, split, n;
+};
+__device__ __forceinline__ SplitOf split_of(int i, int n_ctas, int streams) {
+    const int base = n_ctas / streams, extra = n_ctas % streams;
+    SplitOf r;
+    if (i < extra * (base + 1)) {
+        r.stream = i / (base + 1);
+        r.split = i % (base + 1);
+        r.n = base + 1;
+    } else {
+        const int k = i - extra * (base + 1);
+        r.stream = extra + k / base;
+        r.split = k % base;
+        r.n = base;
+    }
+    return r;
+}
+
+// Programmatic dependent launch (sm_90 and later): a grid launched with programmatic
+// stream serialisation may start while the previous grid of its stream runs, once every
+// CTA of that grid has executed launch_dependents; griddep_wait() returns when the
+// previous grid has completed and its memory writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+constexpr int kMergeSmemFloats = 12288;   // the merge kernel's shared-memory weights (48 KB at most)
 
 struct DecShape {
     int nsw;          // ring slots per warp
@@ -638,18 +694,19 @@ struct DecShape {
 template <typename T, int D, int NT, int JENSEN, bool M16>
 __global__ void __launch_bounds__(kDThreads, (D == 64 && NT == 1) ? 4 : ((D == 128 && NT == 2) ? 1 : 2))
 attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* __restrict__ Vcur, int n_cur, int Hq,
-                   DevCache c, float tau, int n_splits, DecShape sh, void* __restrict__ out, int out_f32,
-                   float* __restrict__ lse, float* __restrict__ part, int* __restrict__ tickets, int* __restrict__ err,
-                   int stall) {
+                   DevCache c, float tau, int max_splits, int n_ctas, DecShape sh, void* __restrict__ out, int out_f32,
+                   float* __restrict__ lse, float* __restrict__ part, int* __restrict__ cta_status, int stall) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ volatile int abort_flag;
-    __shared__ int s_last;
+    __shared__ int s_code, s_range;
     unsigned char* sm =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // this CTA's stream and split; partial rows are laid out with max_splits per stream
+    const SplitOf so = split_of(blockIdx.x, n_ctas, c.B * c.Hkv);
+    const int split = so.split, n_splits = so.n, stream = so.stream;
+    const int h = stream % c.Hkv, b = stream / c.Hkv;
     const int G = Hq / c.Hkv;
-    const int stream = b * c.Hkv + h;
     const LaneConst lc = lane_const(lane);
     const int nsw = sh.nsw, slot_bytes = sh.slot_bytes;
     unsigned char* slots = sm;
@@ -661,12 +718,15 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
     // (failure tests)
     if (tid == 0) {
         abort_flag = 0;
+        s_code = s_range = 0;
         mbar_init(bar0 + 8u * (uint32_t)(kDW * nsw), 1);
     }
     if (lane == 0)
         for (int i = 0; i < nsw; ++i) mbar_init(bar(i), 1);
     mbar_fence_init();
     __syncthreads();
+    // the merge grid that follows may be scheduled from now on (it waits for this grid)
+    griddep_launch_dependents();
 
     // queries of head g + 8 nt: fp32 copies for quantised blocks, 16-bit B fragments
     // (channel pairs 2 tig, 8 + 2 tig of each k-step) for RAW16 blocks
@@ -697,7 +757,7 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < D / 4; ++e) bad |= !(fabsf(q[nt][e]) < 65520.0f);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(err + 1, 1);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) s_range = 1;
     }
     const float c1 = tau * kLog2e;
 
@@ -746,9 +806,13 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
         // (failure tests: with `stall` the first wait targets a barrier nothing arrives on,
         // with a short limit, so the bounded-wait abort path runs)
         const bool ok = stall && k == 0
-                            ? mbar_wait(bar0 + 8u * (uint32_t)(kDW * nsw), 0, &abort_flag, err, 12, 1LL << 21)
-                            : mbar_wait(bar(k % nsw), (k / nsw) & 1, &abort_flag, err, 1);
-        if (!__all_sync(0xffffffffu, ok)) break;
+                            ? mbar_wait(bar0 + 8u * (uint32_t)(kDW * nsw), 0, &abort_flag, nullptr, 12, 1LL << 21)
+                            : mbar_wait(bar(k % nsw), (k / nsw) & 1, &abort_flag, nullptr, 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+            // a wait gave up here or in another warp: the status word gets the wait's code
+            if (lane == 0) atomicCAS(&s_code, 0, stall && k == 0 ? 12 : 1);
+            break;
+        }
         int seg, idx;
         locate(lo + warp + kDW * k, seg, idx);
         const int len = __shfl_sync(0xffffffffu, len_next, k & 31);
@@ -836,7 +900,7 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
             else static_cast<T*>(out)[orow * D + ch] = from_f32<T>(v);
             if (lse && ch == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         } else {
-            float* pr = part + (((long long)stream * n_splits + split) * G + gi) * (D + 4);
+            float* pr = part + (((long long)stream * max_splits + split) * G + gi) * (D + 4);
             if (ch == 0) {
                 pr[0] = M;
                 pr[1] = L;
@@ -845,21 +909,23 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
         }
     }
     (void)rows_out;
-    if (n_splits == 1) return;
+    // this CTA's status word, written on every call (the merge kernel folds the words of all
+    // CTAs into the status header): the code of a wait that gave up, bit 16 the range flag
+    if (tid == 0) cta_status[blockIdx.x] = s_code | (s_range << 16);
+}
 
-    // the last CTA of this stream merges every split's partial.  All (m, l) pairs come
-    // in with one round of loads into shared memory (the warp-merge area, free now),
-    // the per-split weights are formed once per head, and each output element's
-    // partials are loaded together, so the merge costs a few L2 round trips
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&tickets[stream], 1) == n_splits - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+
+// Merge of the split partials of one (batch, kv head) stream into its G output rows:
+// m = max m_s, l = sum l_s 2^(m_s - m), o = sum o_s 2^(m_s - m) / l.  Partial rows are
+// (m, l, -, -, o[D]) in D + 4 floats (o 16-byte aligned), split-major.  Up to 16 splits
+// every thread loads all (m, l) pairs and its 16-byte partials together; more splits go
+// through shared-memory weights (when smem_floats holds them) or plain loops.
+template <typename T, int D>
+__device__ __forceinline__ void merge_splits(const float* __restrict__ pbase, int n_splits, int G, int b, int h,
+                                             int Hq, float* smem, int smem_floats, void* __restrict__ out,
+                                             int out_f32, float* __restrict__ lse, int tid) {
     // partial rows are (m, l, -, -, o[D]): D + 4 floats, o 16-byte aligned
-    const float* pbase = part + (long long)stream * n_splits * G * (D + 4);
-    float* mls = mrg;                          // [n_splits * G] (m, l)
+    float* mls = smem;                         // [n_splits * G] (m, l)
     float* fws = mls + 2 * n_splits * G;       // [n_splits * G] weights 2^(m_s - m)
     float* hml = fws + n_splits * G;           // [G] (m, l) of the merged rows
     constexpr int kC4 = D / 4;
@@ -917,7 +983,7 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
             }
             if (lse && c4 == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-    } else if (3 * n_splits * G + 2 * G <= kDW * rows * (D + 2)) {
+    } else if (3 * n_splits * G + 2 * G <= smem_floats) {
         for (int e = tid; e < n_splits * G; e += kDThreads) {
             const float2 v = __ldcg(reinterpret_cast<const float2*>(pbase + (long long)e * (D + 4)));
             mls[2 * e] = v.x;
@@ -993,7 +1059,45 @@ attn_decode_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T*
             if (lse && ch == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
     }
-    if (tid == 0) tickets[stream] = 0;
+}
+
+// One CTA per stream, launched after the decode grid with programmatic stream
+// serialisation: it may become resident while the decode grid runs, and waits for that grid
+// to complete before reading.  CTA 0 also writes the call's status header from the decode
+// CTAs' status words (word 0: the first wait code found, word 1: the range flag).
+// Its shared memory is dynamic, and none up to 16 splits, so that its CTAs fit beside
+// the decode CTAs still running on an SM and wait there.
+template <typename T, int D>
+__global__ void __launch_bounds__(kDThreads, 4) dec_merge_kernel(const float* __restrict__ part, int max_splits,
+                                                                 int n_ctas, int Hkv, int B, int Hq,
+                                                                 const int* __restrict__ cta_status,
+                                                                 int* __restrict__ err, void* __restrict__ out,
+                                                                 int out_f32, float* __restrict__ lse,
+                                                                 int smem_floats) {
+    extern __shared__ __align__(16) float msm[];
+    __shared__ int s_code, s_range;
+    const int tid = threadIdx.x;
+    griddep_wait();
+    if (blockIdx.x == 0) {
+        if (tid == 0) s_code = s_range = 0;
+        __syncthreads();
+        for (int i = tid; i < n_ctas; i += kDThreads) {
+            const int w = __ldcg(cta_status + i);
+            if (w & 0xFFFF) atomicCAS(&s_code, 0, w & 0xFFFF);
+            if (w >> 16) s_range = 1;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            err[0] = s_code;
+            err[1] = s_range;
+        }
+    }
+    const int streams = B * Hkv, stream = blockIdx.x;
+    const int n = n_ctas / streams + (stream < n_ctas % streams ? 1 : 0);
+    if (n <= 1) return;
+    const int G = Hq / Hkv;
+    merge_splits<T, D>(part + (long long)stream * max_splits * G * (D + 4), n, G, stream / Hkv, stream % Hkv, Hq,
+                       msm, smem_floats, out, out_f32, lse, tid);
 }
 
 // ------------------------------------------------------- operand dump -----
@@ -1153,13 +1257,15 @@ size_t dec_smem_bytes(const DecShape& sh, int d) {
            (size_t)kDW * sh.nsw * 8 + 8;
 }
 
-size_t dec_ticket_bytes(const kv_cache* cache) {
-    return ((size_t)cache->layout.B * cache->layout.Hkv * sizeof(int) + 255) / 256 * 256;
+// One status word per decode CTA (at most n_splits per stream), in 256-byte units.
+size_t dec_status_bytes(const kv_cache* cache, int n_splits) {
+    return ((size_t)cache->layout.B * cache->layout.Hkv * n_splits * sizeof(int) + 255) / 256 * 256;
 }
 
 template <typename T, int D, int NT, int JENSEN, bool M16>
 kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur, int Hq, const kv_cache* cache,
-                       float tau, int n_splits, void* out, int out_f32, float* lse, void* ws, cudaStream_t st) {
+                       float tau, int n_splits, int n_ctas, void* out, int out_f32, float* lse, void* ws,
+                       cudaStream_t st) {
     const DevCache c = make_dev_cache(cache);
     const DecShape sh = dec_shape(cache, Hq);
     const size_t smem = dec_smem_bytes(sh, D);
@@ -1168,16 +1274,47 @@ kv_status launch_dec_t(const void* Q, const void* Kc, const void* Vc, int n_cur,
     if (sa != KV_OK) return sa;
     unsigned char* w = static_cast<unsigned char*>(ws);
     int* err = reinterpret_cast<int*>(w);
-    int* tickets = reinterpret_cast<int*>(w + kStatusBytes);
-    float* part = reinterpret_cast<float*>(w + kStatusBytes + dec_ticket_bytes(cache));
-    // the status header and the merge tickets start at zero
-    const kv_status sc = clear_device(w, kStatusBytes + dec_ticket_bytes(cache), st, "attn_decode_kernel");
-    if (sc != KV_OK) return sc;
-    dim3 grid(n_splits, c.Hkv, c.B);
-    attn_decode_kernel<T, D, NT, JENSEN, M16><<<grid, kDThreads, smem, st>>>(
+    int* cta_status = reinterpret_cast<int*>(w + kStatusBytes);
+    float* part = reinterpret_cast<float*>(w + kStatusBytes + dec_status_bytes(cache, n_splits));
+    // n_ctas CTAs over the B * Hkv streams, at most n_splits per stream (0: n_splits each)
+    const int streams = c.B * c.Hkv;
+    if (n_ctas <= 0 || n_ctas > streams * n_splits) n_ctas = streams * n_splits;
+    if (n_ctas < streams) n_ctas = streams;
+    attn_decode_kernel<T, D, NT, JENSEN, M16><<<n_ctas, kDThreads, smem, st>>>(
         static_cast<const T*>(Q), static_cast<const T*>(Kc), static_cast<const T*>(Vc), n_cur, Hq, c, tau, n_splits,
-        sh, out, out_f32, lse, part, tickets, err, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
-    return check_launch("attn_decode_kernel");
+        n_ctas, sh, out, out_f32, lse, part, cta_status, getenv("BITKV_TEST_NEVER_ARRIVE") != nullptr ? 1 : 0);
+    const kv_status sk = check_launch("attn_decode_kernel");
+    if (sk != KV_OK) return sk;
+    // the merge grid (and the status header) follows with programmatic stream serialisation
+    const int G = Hq / c.Hkv;
+    int mfloats = 0;
+    if (n_splits > 16) mfloats = 3 * n_splits * G + 2 * G < kMergeSmemFloats ? 3 * n_splits * G + 2 * G : 0;
+    static bool carveout_set = false;
+    if (!carveout_set) {
+        // the decode kernel runs at the largest shared-memory carveout; the same for the
+        // merge kernel lets its CTAs share an SM with decode CTAs
+        for (auto* k : {dec_merge_kernel<__half, 64>, dec_merge_kernel<__half, 128>,
+                        dec_merge_kernel<__nv_bfloat16, 64>, dec_merge_kernel<__nv_bfloat16, 128>})
+            cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        carveout_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(streams);
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = (size_t)mfloats * sizeof(float);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* cpart = part;
+    const int* cstat = cta_status;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_merge_kernel<T, D>, cpart, n_splits, n_ctas, c.Hkv, c.B, Hq,
+                                             cstat, err, out, out_f32, lse, mfloats);
+    if (e != cudaSuccess) return set_error(KV_ERR_CUDA, "dec_merge_kernel launch: %s", cudaGetErrorString(e));
+    return check_launch("dec_merge_kernel");
 }
 
 }  // namespace
@@ -1191,32 +1328,51 @@ bool decode_supported(const kv_cache* cache, kv_dtype dt, int n_q, int Hq) {
     return Hq % L.Hkv == 0 && Hq / L.Hkv <= 16;
 }
 
-int decode_auto_splits(const kv_cache* cache, int Hq) {
-    const kv_layout& L = cache->layout;
+// Resident CTAs of the decode kernel on the whole GPU (shared memory bounds them).
+int decode_resident_ctas(const kv_cache* cache, int Hq) {
     const DecShape sh = dec_shape(cache, Hq);
-    const size_t smem = dec_smem_bytes(sh, L.d);
+    const size_t smem = dec_smem_bytes(sh, cache->layout.d);
     int per_sm = (int)((228 * 1024) / (smem + 1024));
     if (per_sm > 16) per_sm = 16;
     if (per_sm < 1) per_sm = 1;
-    const int streams = L.B * L.Hkv;
+    return per_sm * dec_num_sms();
+}
+
+// Automatic split count: the most splits any stream takes when one wave of resident
+// CTAs is spread over the streams (some streams then take one split fewer; see
+// decode_auto_ctas), with at least two blocks per warp.
+int decode_auto_splits(const kv_cache* cache, int Hq) {
+    const kv_layout& L = cache->layout;
+    const int streams = L.B * L.Hkv > 0 ? L.B * L.Hkv : 1;
     const int nb = cache->n_blocks[0] + cache->n_blocks[1] + cache->n_blocks[2];
-    int s = (per_sm * dec_num_sms()) / (streams > 0 ? streams : 1);
+    const int slots = decode_resident_ctas(cache, Hq);
+    int s = (slots + streams - 1) / streams;
     const int cap = nb / (2 * kDW) > 1 ? nb / (2 * kDW) : 1;   // at least two blocks per warp
     if (s > cap) s = cap;
     return s < 1 ? 1 : s;
 }
 
+// Automatic CTA count: one full wave of resident CTAs (never more than n_splits per
+// stream, never fewer than one per stream).
+int decode_auto_ctas(const kv_cache* cache, int Hq, int n_splits) {
+    const kv_layout& L = cache->layout;
+    const int streams = L.B * L.Hkv;
+    const int slots = decode_resident_ctas(cache, Hq);
+    int n = slots < streams * n_splits ? slots : streams * n_splits;
+    return n < streams ? streams : n;
+}
+
 size_t decode_workspace(const kv_cache* cache, int Hq, int n_splits) {
     const kv_layout& L = cache->layout;
     const int G = Hq / L.Hkv;
-    size_t ws = kStatusBytes + dec_ticket_bytes(cache);
+    size_t ws = kStatusBytes + dec_status_bytes(cache, n_splits);
     if (n_splits > 1) ws += (size_t)L.B * L.Hkv * n_splits * G * (L.d + 4) * sizeof(float);
     return ws;
 }
 
 kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_dtype dt, int n_cur, int Hq,
-                             const kv_cache* cache, float tau, int jensen, int n_splits, void* out, int out_f32,
-                             float* lse, void* ws, cudaStream_t st) {
+                             const kv_cache* cache, float tau, int jensen, int n_splits, int n_ctas, void* out,
+                             int out_f32, float* lse, void* ws, cudaStream_t st) {
     const int d = cache->layout.d;
     const bool two = Hq / cache->layout.Hkv > 8;
     const bool m16 = cache->layout.meta_dtype == KV_F16;
@@ -1226,15 +1382,15 @@ kv_status launch_attn_decode(const void* Q, const void* Kc, const void* Vc, kv_d
     do {                                                                                                        \
         if (jensen == KV_JENSEN_TAYLOR2)                                                                        \
             return launch_dec_t<T, D, NT, KV_JENSEN_TAYLOR2, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, \
-                                                                   out, out_f32, lse, ws, st);                  \
+                                                                   n_ctas, out, out_f32, lse, ws, st);                  \
         if (jensen == KV_JENSEN_EXACT)                                                                          \
             return launch_dec_t<T, D, NT, KV_JENSEN_EXACT, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits,   \
-                                                                 out, out_f32, lse, ws, st);                    \
+                                                                 n_ctas, out, out_f32, lse, ws, st);                    \
         if (jensen == KV_JENSEN_ISOTROPIC)                                                                      \
             return launch_dec_t<T, D, NT, KV_JENSEN_ISOTROPIC, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau,         \
-                                                                     n_splits, out, out_f32, lse, ws, st);      \
-        return launch_dec_t<T, D, NT, KV_JENSEN_OFF, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, out,    \
-                                                           out_f32, lse, ws, st);                               \
+                                                                     n_splits, n_ctas, out, out_f32, lse, ws, st);      \
+        return launch_dec_t<T, D, NT, KV_JENSEN_OFF, M16>(Q, Kc, Vc, n_cur, Hq, cache, tau, n_splits, n_ctas, \
+                                                           out, out_f32, lse, ws, st);                               \
     } while (0)
 #define BITKV_DEC(T, D, NT)                                                                                    \
     do {                                                                                                        \

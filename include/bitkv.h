@@ -149,7 +149,9 @@ typedef struct {
     int32_t jensen;      /* kv_jensen; applies to quantised cached keys only ([JB]) */
     int32_t psac;        /* 1: add tau (U^T q) . coeff for CODEBOOK2 caches ([QWM] PSAC) */
     int32_t out_f32;     /* 1: `out` is fp32 whatever the I/O dtype */
-    int32_t num_splits;  /* key-range splits per (batch, head); 0 = automatic */
+    int32_t num_splits;  /* key-range splits per (batch, head); 0 = automatic (the decode path
+                            then launches one wave of resident CTAs, and streams past the first
+                            (CTAs mod B Hkv) take one split fewer than kv_attention_plan reports) */
     int32_t path;        /* kv_path */
 } kv_attn_opts;
 
@@ -190,8 +192,11 @@ size_t kv_attention_workspace(const kv_cache* cache, kv_dtype dtype, int n_q, in
                               const kv_attn_opts* opts);
 
 /* The kernel path (kv_path) and number of key-range splits kv_attention would
- * use for these arguments.  Host only; launches nothing.  One attention call
- * launches one kernel, plus one merge kernel when *splits_out > 1. */
+ * use for these arguments (on the decode path with automatic splits, the largest
+ * count of any (batch, kv head)).  Host only; launches nothing.  One attention
+ * call launches one kernel, plus one merge kernel when *splits_out > 1 on the
+ * tensor-core and CUDA-core paths; the decode path always launches its kernel and
+ * a merge kernel (which also writes the status words). */
 kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int n_cur, int Hq,
                             const kv_attn_opts* opts, int32_t* path_out, int32_t* splits_out);
 

@@ -33,7 +33,9 @@ def mixed_case(case, frac16=0.2, frac4=0.3):
 
 def test_decode_workload_full():
     """Batch 8, 28 query heads over 4 kv heads, d 64, 19600 cached tokens in 613 windows
-    (FP16 / INT4 / INT2 by similarity), fp16: every output row against the oracle."""
+    (FP16 / INT4 / INT2 by similarity), fp16: every output row against the oracle.  The
+    automatic split count spreads one wave of resident CTAs over the 32 streams, so streams
+    take different split counts; the two uniform counts around it are checked as well."""
     case = synth.decode_case()
     tc, oc = mixed_case(case)
     path, splits = B.kv_attention_plan(tc.c, B.KV_F16, 1, 1, 28)
@@ -44,6 +46,10 @@ def test_decode_workload_full():
         check(o, l, ro, rl)
         o16, l16 = run_attention(tc, case, jensen=jensen, out_f32=False)
         assert_rounding_of(o16, o, "f16")
+        if jensen == 1:
+            for sp in (splits - 1, splits):
+                o, l = run_attention(tc, case, jensen=jensen, out_f32=True, path=B.KV_PATH_DECODE, splits=sp)
+                check(o, l, ro, rl)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
