@@ -52,6 +52,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV attention cache GB/s and query-tokens/s, % of HBM/TC roofline"
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 126 << 20        # B300 L2
 
 
 # ------------------------------------------------------------ workloads ----
@@ -455,6 +456,60 @@ def max_over_ranks(times, dist, device):
     return tt.tolist()
 
 
+def e2e_pipelined(r, hin, hO, steps, stream, dev):
+    """Seconds per step of the end-to-end loop with the copies overlapped: step k+1's inputs go
+    host -> device on one copy stream and step k's output device -> host on another while step
+    k computes; device inputs and outputs are double-buffered, and every step still copies its
+    own inputs in and its own output out.  Timed with one event pair around all steps."""
+    import torch
+    sets = [list(r.inputs), [t.clone() for t in r.inputs]]
+    outs = [r.out, torch.empty_like(r.out)]
+    hOs = [hO, torch.empty_like(hO).pin_memory()]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    done = [torch.cuda.Event(), torch.cuda.Event()]      # the step that used buffer b has computed
+    fetched = [torch.cuda.Event(), torch.cuda.Event()]   # its output has reached the host
+    loaded = [torch.cuda.Event(), torch.cuda.Event()]    # inputs of the next user of buffer b are in
+    for e in done + fetched:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    up.wait_event(t0)
+    down.wait_event(t0)
+
+    def load(k):
+        b = k % 2
+        up.wait_event(done[b])
+        with torch.cuda.stream(up):
+            for dst, src in zip(sets[b], hin):
+                dst.copy_(src, non_blocking=True)
+        loaded[b].record(up)
+
+    sh = stream.cuda_stream
+    load(0)
+    for k in range(steps):
+        b = k % 2
+        if k + 1 < steps:
+            load(k + 1)
+        stream.wait_event(loaded[b])
+        stream.wait_event(fetched[b])
+        r.Q, r.Kc, r.Vc = sets[b]
+        r.out = outs[b]
+        r.attention(sh)
+        r.append(sh)
+        done[b].record(stream)
+        down.wait_event(done[b])
+        with torch.cuda.stream(down):
+            hOs[b].copy_(outs[b], non_blocking=True)
+        fetched[b].record(down)
+    stream.wait_stream(down)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    r.Q, r.Kc, r.Vc = sets[0]
+    r.out = outs[0]
+    return t0.elapsed_time(t1) / steps * 1e-3
+
+
 def job_value(units_per_rank, world, seconds):
     """Whole-job throughput: every rank's units over the slowest rank's time."""
     return world * units_per_rank / seconds
@@ -505,23 +560,29 @@ def run_own(args, rank, world, dist):
     hO = torch.empty_like(r.out, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = hO.numel() * hO.element_size()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    working = r.cache_bytes + h2d + d2h
+    pipelined = working > L2_BYTES
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    for k in range(args.steps):
-        flush(k)
-        e_ev[k][0].record(stream)
-        for dst, src in zip(r.inputs, hin):
-            dst.copy_(src, non_blocking=True)
-        r.attention(sh)
-        r.append(sh)
-        hO.copy_(r.out, non_blocking=True)
-        e_ev[k][1].record(stream)
-    torch.cuda.synchronize(dev)
+    if pipelined:
+        t_e2e = e2e_pipelined(r, hin, hO, args.steps, stream, dev)
+    else:
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush(k)
+            e_ev[k][0].record(stream)
+            for dst, src in zip(r.inputs, hin):
+                dst.copy_(src, non_blocking=True)
+            r.attention(sh)
+            r.append(sh)
+            hO.copy_(r.out, non_blocking=True)
+            e_ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_e2e = sum(a.elapsed_time(b) for a, b in e_ev) / args.steps * 1e-3
     if dist:
         dist.barrier()
-    t_e2e = sum(a.elapsed_time(b) for a, b in e_ev) / args.steps * 1e-3
 
     if dist:
         t_step, t_attn, t_app, t_e2e = max_over_ranks([t_step, t_attn, t_app, t_e2e], dist, dev)
@@ -561,7 +622,13 @@ def run_own(args, rank, world, dist):
         "attn_ms": t_attn * 1e3, "append_ms": t_app * 1e3,
         "roofline": roof,
         "e2e": {"value": job_value(rows, world, t_e2e), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "schedule": ("pipelined: step k+1's H2D and step k's D2H on two copy streams while step k "
+                             "computes (double-buffered device inputs and outputs), one event pair over all "
+                             f"steps; L2 not flushed, the step's {working / 1e6:.0f} MB exceed the 126 MB L2"
+                             if pipelined else
+                             "serial: H2D, attention, append, D2H on one stream per step, L2 flushed between "
+                             "steps")},
         "gpu_launches": r.launches_per_step * args.steps,
         "clocks": sampler.summary(),
     }
