@@ -231,9 +231,11 @@ kv_status kv_attention_plan(const kv_cache* cache, kv_dtype dtype, int n_q, int 
  *   NULL when n_cur == 0); out (device) [B][Hq][n_q][d] in dtype (fp32 if
  *   opts->out_f32); lse (device, nullable) fp32 [B][Hq][n_q] natural-log
  *   partition function.  workspace (device, 16-byte aligned) of ws_bytes >=
- *   kv_attention_workspace() (at least 256 bytes).  Its first 256 bytes are the
- *   call's status words, cleared by each call before its kernels run; read them
- *   with kv_attention_status() after the call.  Without BITKV_DEBUG_SYNC a
+ *   kv_attention_workspace() (at least 256 bytes); it needs no initialisation.
+ *   Its first 256 bytes are the call's status words: cleared by each call before
+ *   its kernels run (tensor-core and CUDA-core paths) or written by the call's
+ *   last kernel (decode path, from every CTA's own status word); read them with
+ *   kv_attention_status() after the call.  Without BITKV_DEBUG_SYNC a
  *   KV_OK return means the work was queued, not that no device-side wait gave
  *   up. */
 kv_status kv_attention(const void* Q, const void* Kcur, const void* Vcur, kv_dtype dtype, int n_q, int n_cur,
