@@ -456,6 +456,36 @@ def max_over_ranks(times, dist, device):
     return tt.tolist()
 
 
+def capture_step(r, spec, dev, stream):
+    """CUDA graphs of the step's attention call and of its append (when the workload appends),
+    captured once on a side stream; returns functions that replay them on `stream`.  The
+    graphs hold the calls' kernels with their arguments as captured: the same buffers and the
+    same cache length (the append re-appends the same blocks each replay, as the rewind does)."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        r.attention(side.cuda_stream)
+        r.append(side.cuda_stream)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=side):
+        r.attention(side.cuda_stream)
+    gp = None
+    if spec["kind"] == "chunk":
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp, stream=side):
+            r.append(side.cuda_stream)
+    torch.cuda.synchronize(dev)
+
+    def replay(g):
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    return (lambda: replay(ga)), ((lambda: replay(gp)) if gp is not None else (lambda: None))
+
+
 def e2e_pipelined(r, hin, hO, steps, stream, dev):
     """Seconds per step of the end-to-end loop with the copies overlapped: step k+1's inputs go
     host -> device on one copy stream and step k's output device -> host on another while step
@@ -536,6 +566,10 @@ def run_own(args, rank, world, dist):
             r.attention(sh)
             r.append(sh)
         torch.cuda.synchronize(dev)
+        # the step's calls as written (eager), or replayed from CUDA graphs captured once
+        attn_fn, app_fn = (lambda: r.attention(sh)), (lambda: r.append(sh))
+        if args.graph:
+            attn_fn, app_fn = capture_step(r, spec, dev, stream)
 
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         if dist:
@@ -544,9 +578,9 @@ def run_own(args, rank, world, dist):
         for k in range(args.steps):
             flush(k)                                   # evicts L2 (outside the timed events)
             ev[k][0].record(stream)
-            r.attention(sh)
+            attn_fn()
             ev[k][1].record(stream)
-            r.append(sh)
+            app_fn()
             ev[k][2].record(stream)
         torch.cuda.synchronize(dev)
         if dist:
@@ -575,8 +609,8 @@ def run_own(args, rank, world, dist):
             e_ev[k][0].record(stream)
             for dst, src in zip(r.inputs, hin):
                 dst.copy_(src, non_blocking=True)
-            r.attention(sh)
-            r.append(sh)
+            attn_fn()
+            app_fn()
             hO.copy_(r.out, non_blocking=True)
             e_ev[k][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -617,6 +651,7 @@ def run_own(args, rank, world, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic (seeded, PCG64)",
         "config": {"workload": spec["label"], "query_tokens": "B*Hq*n_q per step (one row per query head)",
                    "l2": "flushed between steps (512 MiB written, then another 512 MiB read)",
+                   "execution": "CUDA graph replay (graphs captured once)" if args.graph else "eager calls",
                    "parallelism": f"replicas x{world}"},
         "cache_gbs": world * cache_gbs,
         "attn_ms": t_attn * 1e3, "append_ms": t_app * 1e3,
@@ -793,6 +828,8 @@ def main():
                     help="override the workload's Jensen mode (0 off, 1 TAYLOR2, 2 EXACT, 3 ISOTROPIC)")
     ap.add_argument("--meta16", action="store_true",
                     help="fp16 step / zero-point metadata in the INT blocks (not for codebook)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each step's calls from CUDA graphs captured once (default: eager calls)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "own" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
