@@ -227,3 +227,26 @@ def test_rollout_workload_tc_sampled(jensen):
     splits = _workload_tc_sampled(case, [0, 19, 39], np.random.default_rng(2).choice(1560, 32, replace=False),
                                   jensen)
     assert splits >= 1
+
+
+@pytest.mark.parametrize("path", TC_PATHS)
+def test_tc_running_max_jumps(path):
+    """Rows whose logit maximum jumps by far more than 2^15 (log2 units) at a later key tile:
+    a cached key is set to a multiple of the row's query, so its logit is about 49 (log2) where
+    the others are a few units.  The jumps sit in the first tile (the two-pass softmax of a
+    row's first tile), in groups 0, 2 and 3 of later tiles (the one-pass softmax then rescales
+    the P groups already written), twice on one row, on a row of the pair's second CTA and in
+    the unquantised current chunk."""
+    case = synth.chunk_case(64, B=1, Hkv=2, d=128, chunks=[1000, 600], n_cur=130, n_q=130, dtype="bf16")
+    K, Kc, Q = case["K_cache"].copy(), case["K_cur"].copy(), case["Q"]
+    spikes = [(0, 0, 128 + 5, 3.0), (1, 1, 128 + 64 + 7, 3.0), (2, 0, 384 + 96 + 3, 3.0),
+              (3, 1, 640 + 33, 3.0), (4, 0, 20, 3.0), (5, 1, 256 + 40, 3.0), (5, 1, 1024 + 100, 6.0),
+              (129, 0, 896 + 70, 3.0), (128, 1, 1500, 4.0)]
+    for row, h, t, a in spikes:
+        K[0, h, t] = synth.to_dtype_values(a * Q[0, h, row], "bf16")
+    Kc[0, 1, 77] = synth.to_dtype_values(3.0 * Q[0, 1, 6], "bf16")
+    case = dict(case, K_cache=K, K_cur=Kc)
+    tc = gpu_uniform(case, 2)
+    ref, tight = refs(oracle_uniform(case, 2), case, "bf16", tc_path=True, jensen=1)
+    for splits in (1, 2):
+        attention_checked(tc, case, ref, "bf16", tight, jensen=1, path=path, splits=splits)
