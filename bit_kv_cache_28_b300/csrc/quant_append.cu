@@ -538,22 +538,24 @@ constexpr int kFastD = 128;
 // integer, ties to even, by adding 1.5 2^23 (exact for |q| < 2^22, which a code's quotient
 // always is) and read out of that sum's low mantissa bits.  e = q - rint(q) is exact, and
 // ||e| - 1/2| equals code_fast()'s |q - floor(q) - 1/2| bit for bit, so the same elements (within
-// 4e-6 of a half-integer, or r not finite) take the IEEE quotient.  Zero steps give code 0.
+// 4e-6 of a half-integer, or r not finite) take the IEEE quotient.  With |e| <= 1/2 that test is
+// one comparison: ||e| - 1/2| < 4e-6 (fp32) holds exactly when |e| > kTie, the float below
+// 0.4999960065 (checked over every fp32 in [0, 1/2]).  A zero step comes with r = 0, so its q
+// is 0 and its code 0.
 __device__ __forceinline__ void code_pair2(float x0, float x1, float s0, float s1, float r0, float r1, float z0,
                                            float z1, int qmax, uint32_t& c0, uint32_t& c1) {
     constexpr float kMagic = 12582912.0f;   // 1.5 2^23
+    const float kTie = __uint_as_float(0x3EFFFF79u);
     const f32x2 d = x2_sub(x2(x0, x1), x2(z0, z1));
     const f32x2 q = x2_mul(d, x2(r0, r1));
     const f32x2 t = x2_add(q, x2(kMagic, kMagic));
     const float2 e = x2_split(x2_sub(q, x2_sub(t, x2(kMagic, kMagic))));
     float2 tf = x2_split(t);
-    if (fabsf(fabsf(e.x) - 0.5f) < 4e-6f || !(r0 < INFINITY))
-        tf.x = __fadd_rn(__fdiv_rn(__fsub_rn(x0, z0), s0), kMagic);
-    if (fabsf(fabsf(e.y) - 0.5f) < 4e-6f || !(r1 < INFINITY))
-        tf.y = __fadd_rn(__fdiv_rn(__fsub_rn(x1, z1), s1), kMagic);
+    if (fabsf(e.x) > kTie || !(r0 < INFINITY)) tf.x = __fadd_rn(__fdiv_rn(__fsub_rn(x0, z0), s0), kMagic);
+    if (fabsf(e.y) > kTie || !(r1 < INFINITY)) tf.y = __fadd_rn(__fdiv_rn(__fsub_rn(x1, z1), s1), kMagic);
     const int k0 = (int)__float_as_uint(tf.x) - 0x4B400000, k1 = (int)__float_as_uint(tf.y) - 0x4B400000;
-    c0 = s0 > 0.0f ? (uint32_t)min(max(k0, 0), qmax) : 0u;
-    c1 = s1 > 0.0f ? (uint32_t)min(max(k1, 0), qmax) : 0u;
+    c0 = (uint32_t)min(max(k0, 0), qmax);
+    c1 = (uint32_t)min(max(k1, 0), qmax);
 }
 
 template <typename T, int BITS>
