@@ -69,6 +69,17 @@ def test_decode_mixed_ragged(dtype, n_cur):
             check(o, l, ro, rl)
 
 
+def test_decode_many_splits():
+    """The split merge past 16 splits: 24 splits (weights through shared memory) and 300 splits
+    over the 32 blocks (plain loops; most splits empty), 16 query heads per kv head."""
+    case = synth.decode_case(seed=85, B=1, Hq=16, Hkv=1, d=64, n_cache=1000)
+    tc, oc = mixed_case(case)
+    ro, rl = OA.attention_over_cache(oc, case["Q"], case["K_cur"], case["V_cur"], "f16", jensen=1)
+    for splits in (24, 300):
+        o, l = run_attention(tc, case, jensen=1, out_f32=True, path=B.KV_PATH_DECODE, splits=splits)
+        check(o, l, ro, rl)
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("d,Hq,Hkv", [(128, 3, 3), (64, 32, 2), (128, 16, 1)])
 def test_decode_uniform(bits, d, Hq, Hkv):
