@@ -97,7 +97,7 @@ def run_attention(tc, case, jensen=0, out_f32=False, path=B.KV_PATH_AUTO, splits
 
 
 def tol(io_dtype):
-    """The benchmark spec bound on outputs and lse against the oracle's definition: 2e-3 for fp32
+    """The required bound on outputs and lse against the oracle's definition: 2e-3 for fp32
     I/O; 1e-2 for 16-bit I/O (bf16 or fp16 inputs, whatever the output container)."""
     return 2e-3 if io_dtype == "f32" else 1e-2
 

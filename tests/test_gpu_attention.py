@@ -1,6 +1,6 @@
 """GPU parity of kv_attention against the oracle's one precision model (the exact definition).
 
-Every path is held to the benchmark spec bound for its I/O dtype against the definition
+Every path is held to the required bound for its I/O dtype against the definition
 (helpers.tol: 2e-3 for fp32 I/O, 1e-2 for 16-bit I/O).  The CUDA-core path keeps its
 operands exact, so it is also held to 2e-3 against the definition itself; the tensor-core
 path documents fp16 operand storage, so it is also held to 2e-3 against the definition

@@ -3,7 +3,7 @@
 The decode kernel never forms dequantised 16-bit key or value tiles: it folds the
 step sizes and zero points into the query (fp16 high + low parts, ~22 bits) and the
 attention weights, so it is held to 2e-3 against the oracle's definition itself (inside
-the benchmark spec 1e-2 for its 16-bit I/O); its 16-bit outputs must be the rounding of the
+the required 1e-2 for its 16-bit I/O); its 16-bit outputs must be the rounding of the
 fp32 result.
 """
 
