@@ -268,6 +268,34 @@ class L2Flush:
         self.r.sum()
 
 
+def pack_inputs(tensors):
+    """The step's input tensors as views of one contiguous device buffer (each view 16-byte
+    aligned), so that a step's inputs arrive in one host-to-device copy; returns (flat, views)."""
+    import torch
+    align = 16 // tensors[0].element_size()
+    offs, o = [], 0
+    for t in tensors:
+        offs.append(o)
+        o += (t.numel() + align - 1) // align * align
+    flat = torch.zeros(o, dtype=tensors[0].dtype, device=tensors[0].device)
+    views = views_of(flat, offs, [t.shape for t in tensors])
+    for v, t in zip(views, tensors):
+        v.copy_(t)
+    return flat, views
+
+
+def views_of(flat, offs, shapes):
+    import math
+    return [flat[a:a + math.prod(sh)].view(sh) for a, sh in zip(offs, shapes)]
+
+
+def input_layout(r):
+    """(offsets, shapes) of a runner's input views inside its flat buffer."""
+    base = r.in_flat.data_ptr()
+    es = r.in_flat.element_size()
+    return [(t.data_ptr() - base) // es for t in r.inputs], [t.shape for t in r.inputs]
+
+
 class ChunkRunner:
     """Device state of one replica of a chunk workload: the cache after the
     workload's cached chunks, and the step inputs."""
@@ -309,7 +337,7 @@ class ChunkRunner:
                                  self.dt, n, self.tc.c)
             t0 += n
         self.saved = (list(self.tc.c.n_blocks), self.tc.c.n_tokens)
-        self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
+        self.in_flat, self.inputs = pack_inputs([to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])])
         self.Q, self.Kc, self.Vc = self.inputs
         self.opts = B.kv_attn_opts(0.0, spec["jensen"], spec.get("psac", 0), 0, 0, B.KV_PATH_AUTO)
         self.out = torch.empty_like(self.Q)
@@ -374,7 +402,7 @@ class DecodeRunner:
         per_b = (lens[0].sum(1) * 2 * d * 2 + lens[1].sum(1) * 2 * d * 4 / 8 + nb[1] * meta
                  + lens[2].sum(1) * 2 * d * 2 / 8 + nb[2] * meta)
         self.cache_bytes = float(per_b.sum() * Hkv)
-        self.inputs = [to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])]
+        self.in_flat, self.inputs = pack_inputs([to(inputs["Q"]), to(inputs["K_cur"]), to(inputs["V_cur"])])
         self.Q, self.Kc, self.Vc = self.inputs
         self.opts = B.kv_attn_opts(0.0, spec["jensen"], 0, 0, 0, B.KV_PATH_AUTO)
         self.out = torch.empty_like(self.Q)
@@ -492,7 +520,9 @@ def e2e_pipelined(r, hin, hO, steps, stream, dev):
     k computes; device inputs and outputs are double-buffered, and every step still copies its
     own inputs in and its own output out.  Timed with one event pair around all steps."""
     import torch
-    sets = [list(r.inputs), [t.clone() for t in r.inputs]]
+    flats = [r.in_flat, torch.empty_like(r.in_flat)]
+    offs, shapes = input_layout(r)
+    sets = [list(r.inputs), views_of(flats[1], offs, shapes)]
     outs = [r.out, torch.empty_like(r.out)]
     hOs = [hO, torch.empty_like(hO).pin_memory()]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -511,8 +541,7 @@ def e2e_pipelined(r, hin, hO, steps, stream, dev):
         b = k % 2
         up.wait_event(done[b])
         with torch.cuda.stream(up):
-            for dst, src in zip(sets[b], hin):
-                dst.copy_(src, non_blocking=True)
+            flats[b].copy_(hin, non_blocking=True)
         loaded[b].record(up)
 
     sh = stream.cuda_stream
@@ -589,10 +618,11 @@ def run_own(args, rank, world, dist):
     t_attn = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps * 1e-3
     t_app = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps * 1e-3
 
-    # end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of the output
-    hin = [t.cpu().pin_memory() for t in r.inputs]
+    # end to end through the C ABI with host buffers: H2D of the step's inputs (one pinned buffer
+    # holding Q, K_cur and V_cur, one copy), D2H of the output
+    hin = r.in_flat.cpu().pin_memory()
     hO = torch.empty_like(r.out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in hin)
+    h2d = hin.numel() * hin.element_size()
     d2h = hO.numel() * hO.element_size()
     working = r.cache_bytes + h2d + d2h
     pipelined = working > L2_BYTES
@@ -607,8 +637,7 @@ def run_own(args, rank, world, dist):
         for k in range(args.steps):
             flush(k)
             e_ev[k][0].record(stream)
-            for dst, src in zip(r.inputs, hin):
-                dst.copy_(src, non_blocking=True)
+            r.in_flat.copy_(hin, non_blocking=True)
             attn_fn()
             app_fn()
             hO.copy_(r.out, non_blocking=True)
