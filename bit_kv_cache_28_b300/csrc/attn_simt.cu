@@ -25,9 +25,13 @@ constexpr int kSimtThreads = 128;
 
 struct SimtSmem {
     // offsets in floats
-    int qs, ks, vs, ss, sk, uq, cq;
+    int qs, ks, vs, ss, sk, uq, cq, stg;
     int total;
 };
+
+// A staged cache block: up to the size of a 16-bit block (32 tokens x d x 2 bytes x K and V),
+// the largest block of any class at head dim d.
+__host__ __device__ constexpr int simt_stage_bytes(int d) { return kSK * d * 2 * 2; }
 
 __host__ __device__ inline SimtSmem simt_smem(int d, int r) {
     SimtSmem s;
@@ -39,7 +43,8 @@ __host__ __device__ inline SimtSmem simt_smem(int d, int r) {
     s.sk = s.ss + kSQ * (kSK + 1);
     s.uq = s.sk + d;
     s.cq = s.uq + kSQ * (r > 0 ? r : 1);
-    s.total = s.cq + kSK * (r > 0 ? r : 1);
+    s.stg = (s.cq + kSK * (r > 0 ? r : 1) + 3) & ~3;   // 16-byte aligned
+    s.total = s.stg + simt_stage_bytes(d) / 4;
     return s;
 }
 
@@ -66,11 +71,15 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
     float* Sk = smem + L.sk;
     float* Uq = smem + L.uq;
     float* Cq = smem + L.cq;
+    uint4* stg = reinterpret_cast<uint4*>(smem + L.stg);
 
+    // loops with a fixed trip count and read-only loads, so that a thread's loads are all in
+    // flight before their results are stored
     const long long qbase = (((long long)b * Hq + hq) * n_q) * D;
-    for (int e = tid; e < kSQ * D; e += kSimtThreads) {
-        const int i = e / D, ch = e % D;
-        Qs[i * ld + ch] = (q0 + i < n_q) ? to_f32<T>(Q[qbase + (long long)(q0 + i) * D + ch]) : 0.0f;
+#pragma unroll 8
+    for (int it = 0; it < kSQ * D / kSimtThreads; ++it) {
+        const int e = tid + it * kSimtThreads, i = e / D, ch = e % D;
+        Qs[i * ld + ch] = (q0 + i < n_q) ? to_f32<T>(__ldg(Q + qbase + (long long)(q0 + i) * D + ch)) : 0.0f;
     }
     __syncthreads();
     if (r > 0) {
@@ -131,6 +140,26 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
             len = c.blk_len[gi];
             const unsigned char* blk = block_ptr(c, b, h, seg, i);
             const int cls = seg_class(c.kind, seg);
+            // the packed block into shared memory: one coalesced pass of 16-byte loads, all
+            // issued before the stores (the entries are then decoded from the staged copy)
+            constexpr int kPass = simt_stage_bytes(D) / (16 * kSimtThreads);
+            const int n16 = (int)(c.block_bytes[seg] >> 4);
+            if (n16 <= kPass * kSimtThreads) {
+                const uint4* src = reinterpret_cast<const uint4*>(blk);
+                uint4 tmp[kPass];
+#pragma unroll
+                for (int k = 0; k < kPass; ++k) {
+                    const int x = tid + k * kSimtThreads;
+                    tmp[k] = x < n16 ? __ldg(src + x) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < kPass; ++k) {
+                    const int x = tid + k * kSimtThreads;
+                    if (x < n16) stg[x] = tmp[k];
+                }
+                __syncthreads();
+                blk = reinterpret_cast<const unsigned char*>(stg);
+            }
             for (int e = tid; e < kSK * D; e += kSimtThreads) {
                 const int t = e / D, ch = e % D;
                 const float2 kv =
@@ -156,10 +185,11 @@ attn_simt_kernel(const T* __restrict__ Q, const T* __restrict__ Kcur, const T* _
             const int t0 = (u - units_cache) * kSK;
             len = min(kSK, n_cur - t0);
             const long long kb = (((long long)b * c.Hkv + h) * n_cur + t0) * D;
-            for (int e = tid; e < kSK * D; e += kSimtThreads) {
-                const int t = e / D, ch = e % D;
-                Ks[t * ld + ch] = t < len ? to_f32<T>(Kcur[kb + e]) : 0.0f;
-                Vs[t * ld + ch] = t < len ? to_f32<T>(Vcur[kb + e]) : 0.0f;
+#pragma unroll 8
+            for (int it = 0; it < kSK * D / kSimtThreads; ++it) {
+                const int e = tid + it * kSimtThreads, t = e / D, ch = e % D;
+                Ks[t * ld + ch] = t < len ? to_f32<T>(__ldg(Kcur + kb + e)) : 0.0f;
+                Vs[t * ld + ch] = t < len ? to_f32<T>(__ldg(Vcur + kb + e)) : 0.0f;
             }
         }
         __syncthreads();
