@@ -695,11 +695,16 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
     } else {
         // q^2 of the Q tile (bf16 q, so q^2 has at most 16 significant bits and splits
         // exactly into bf16 high + low) -> swizzled smem, rows beyond n_q zero; the
-        // Jensen weight tiles start zero (rows 8-15 stay zero)
+        // Jensen weight tiles start zero (rows 8-15 stay zero).  EXACT: the bf16 rows of q
+        // themselves in the high part's place, read by the softmax for every cache tile.
         for (int e = tid; e < kM * kD / 8; e += kThreads) {
             const int row = e >> 4, ch = e & 15;
             const uint4 v =
                 (q0 + row < n_q) ? __ldg(Qg + (long long)(q0 + row) * (kD / 8) + ch) : make_uint4(0, 0, 0, 0);
+            if (JENSEN == KV_JENSEN_EXACT) {
+                *reinterpret_cast<uint4*>(sm + M::q2h + sw_off(row, ch)) = v;
+                continue;
+            }
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
             uint32_t hq2[4], lq2[4];
 #pragma unroll
@@ -1090,16 +1095,33 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                 } else if (JENSEN == KV_JENSEN_EXACT) {
                     const float* SK = reinterpret_cast<const float*>(sm + M::w + (j & 3) * kExactW);
                     const float jt = 0.5f * tau;
-#pragma unroll 1
+#pragma unroll 2
                     for (int ch = 0; ch < 16; ++ch) {
-                        const uint4 qv = q0 + i < n_q ? __ldg(Qg + (long long)(q0 + i) * (kD / 8) + ch)
-                                                      : make_uint4(0, 0, 0, 0);
+                        const uint4 qv = *reinterpret_cast<const uint4*>(sm + M::q2h + sw_off(i, ch));
                         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+                        // the 32 arguments of these 8 channels; when none of the warp's
+                        // reaches 1/2 (almost every chunk) the series alone, without branches
+                        float xa[8][4];
+                        float xm = 0.0f;
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const float qf = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(jt * qf * SK[g * kD + 8 * ch + k]);
+                            for (int g = 0; g < 4; ++g) {
+                                xa[k][g] = fabsf(jt * qf * SK[g * kD + 8 * ch + k]);
+                                xm = fmaxf(xm, xa[k][g]);
+                            }
+                        }
+                        if (__any_sync(0xffffffffu, !(xm < 0.5f))) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(xa[k][g]);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc_series(xa[k][g]);
                         }
                     }
 #pragma unroll

@@ -238,20 +238,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // log(sinh(x)/x): the Taylor series of the log (Bernoulli-number
 // coefficients 1/6, -1/180, 1/2835, -1/37800) below 0.5, where its truncation
-// error is < 1e-8; above, x + log1p(-exp(-2x)) - log(2x).
+// error is < 1e-8; above, x + log(1 - exp(-2x)) - log(2x) with the fast
+// hardware exp and log: there 1 - exp(-2x) >= 0.63 and 2x >= 1, so nothing
+// cancels and the absolute error stays near 1e-6.
+__device__ __forceinline__ float log_sinhc_series(float x) {
+    const float x2 = x * x;
+    return x2 * (1.0f / 6.0f + x2 * (-1.0f / 180.0f + x2 * (1.0f / 2835.0f - x2 * (1.0f / 37800.0f))));
+}
 __device__ __forceinline__ float log_sinhc(float x) {
     x = fabsf(x);
-    if (x < 0.5f) {
-        const float x2 = x * x;
-        return x2 * (1.0f / 6.0f + x2 * (-1.0f / 180.0f + x2 * (1.0f / 2835.0f - x2 * (1.0f / 37800.0f))));
-    }
-    return x + log1pf(-expf(-2.0f * x)) - logf(2.0f * x);
+    if (x < 0.5f) return log_sinhc_series(x);
+    return x + __logf(1.0f - __expf(-2.0f * x)) - __logf(2.0f * x);
 }
 
 // Every attention workspace starts with a status header of kStatusBytes: int word 0
 // holds the code of a bounded device-side wait that gave up (0: none), word 1 the
-// range flag (an fp16 operand of the tensor-core path would be infinite).  Each
-// call clears the header before its kernels run.
+// range flag (an fp16 operand of the tensor-core path would be infinite).  The
+// tensor-core and CUDA-core calls clear the header before their kernels run; the
+// decode call's merge kernel writes it.
 constexpr size_t kStatusBytes = 256;
 
 // Host-side helpers shared by the launch code.
