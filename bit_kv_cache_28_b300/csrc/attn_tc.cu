@@ -1099,29 +1099,23 @@ attn_tc_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restr
                     for (int ch = 0; ch < 16; ++ch) {
                         const uint4 qv = *reinterpret_cast<const uint4*>(sm + M::q2h + sw_off(i, ch));
                         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-                        // the 32 arguments of these 8 channels; when none of the warp's
-                        // reaches 1/2 (almost every chunk) the series alone, without branches
-                        float xa[8][4];
-                        float xm = 0.0f;
+                        // per channel, the 4 blocks' arguments of the warp's 32 rows: when none
+                        // reaches 1/2 the series alone, without branches (the same value the
+                        // per-argument function gives); large-step channels take that function
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             const float qf = __uint_as_float(k & 1 ? (qw[k >> 1] & 0xFFFF0000u) : (qw[k >> 1] << 16));
+                            float xa[4];
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                xa[k][g] = fabsf(jt * qf * SK[g * kD + 8 * ch + k]);
-                                xm = fmaxf(xm, xa[k][g]);
+                            for (int g = 0; g < 4; ++g) xa[g] = fabsf(jt * qf * SK[g * kD + 8 * ch + k]);
+                            const float xm = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+                            if (__any_sync(0xffffffffu, !(xm < 0.5f))) {
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(xa[g]);
+                            } else {
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc_series(xa[g]);
                             }
-                        }
-                        if (__any_sync(0xffffffffu, !(xm < 0.5f))) {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k)
-#pragma unroll
-                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc(xa[k][g]);
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k)
-#pragma unroll
-                                for (int g = 0; g < 4; ++g) dl[g] += log_sinhc_series(xa[k][g]);
                         }
                     }
 #pragma unroll
