@@ -52,6 +52,26 @@ constexpr int kDThreads = 32 * kDW;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// EXACT Jensen terms log(sinh x / x), x = c qs[e], added to acc in the order e = 0 .. 3.  One
+// warp vote: when no lane's |x| reaches 1/2, the series alone without branches (the value
+// log_sinhc gives there); otherwise log_sinhc per term.  Called by the whole warp.
+__device__ __forceinline__ void exact_terms4(float& acc, float c, const float (&qs)[4]) {
+    float x[4];
+    float xm = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[e] = fabsf(c * qs[e]);
+        xm = fmaxf(xm, x[e]);
+    }
+    if (__any_sync(0xffffffffu, !(xm < 0.5f))) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc += log_sinhc(x[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc += log_sinhc_series(x[e]);
+    }
+}
+
 // ---- warp-level MMA and shared-memory matrix loads ---------------------------
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -239,9 +259,9 @@ __device__ __forceinline__ void int_block(const unsigned char* blk, int len, con
                 qs[e] = q[nt][4 * kk + e] * s[e];
                 qz[nt] = fmaf(q[nt][4 * kk + e], z[e], qz[nt]);
                 if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs[e], qs[e], jd[nt]);
-                else if (JENSEN == KV_JENSEN_EXACT) jd[nt] += log_sinhc(0.5f * tau * qs[e]);
                 else if (JENSEN == KV_JENSEN_ISOTROPIC) jd[nt] = fmaf(q[nt][4 * kk + e], q[nt][4 * kk + e], jd[nt]);
             }
+            if (JENSEN == KV_JENSEN_EXACT) exact_terms4(jd[nt], 0.5f * tau, qs);
             bh[nt][kk][0] = pack_f16(qs[0], qs[1]);
             bh[nt][kk][1] = pack_f16(qs[2], qs[3]);
             const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&bh[nt][kk][0]));
@@ -402,14 +422,16 @@ __device__ __forceinline__ void int_block_h(const unsigned char* blk, int len, c
                 for (int e = 0; e < 4; ++e) ss2 = fmaf(s[e], s[e], ss2);
             }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) {
+                float qs[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float qs = q[nt][4 * kk + e] * s[e];
-                    if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs, qs, jd[nt]);
-                    else if (JENSEN == KV_JENSEN_EXACT) jd[nt] += log_sinhc(0.5f * tau * qs);
+                    qs[e] = q[nt][4 * kk + e] * s[e];
+                    if (JENSEN == KV_JENSEN_TAYLOR2) jd[nt] = fmaf(qs[e], qs[e], jd[nt]);
                     else if (JENSEN == KV_JENSEN_ISOTROPIC) jd[nt] = fmaf(q[nt][4 * kk + e], q[nt][4 * kk + e], jd[nt]);
                 }
+                if (JENSEN == KV_JENSEN_EXACT) exact_terms4(jd[nt], 0.5f * tau, qs);
+            }
         }
     }
     // the Jensen bias of head g + 8 nt, gathered for the fragment's heads 2 tig, 2 tig + 1
